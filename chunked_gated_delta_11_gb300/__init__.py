@@ -1,0 +1,214 @@
+"""Python binding of libkda, the GB300 (sm_103a) Kimi Delta Attention forward.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels of ``libkda.so`` (built in-tree by ``build.py``); PyTorch supplies
+device memory and streams.  Names follow the C ABI in ``include/kda.h``.
+There is no fallback: if the library is missing, every call raises.
+
+Layout: q, k, v, g_raw bf16 [T_total, H, 128]; beta_raw bf16 [T_total, H];
+out bf16 [T_total, H, 128]; states fp32 [N, H, 128, 128] (value x key);
+cu_seqlens int32 [N + 1] (device) or None for N equal sequences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB as _LIB_PATH
+from .build import build as _build
+
+__all__ = [
+    "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
+    "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
+    "kda_forward_host", "REC_BYTES", "CHUNK", "HEAD_DIM",
+]
+
+CHUNK = 16
+HEAD_DIM = 128
+REC_BYTES = 34304
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
+          3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_LAUNCH", 5: "KDA_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)} "
+                         f"({kda_status_string(self.status)})")
+
+
+def load(build_if_missing: bool = False):
+    """Load libkda.so (optionally building it first).  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(f"libkda is not built ({_LIB_PATH} missing); "
+                                   "run chunked_gated_delta_11_gb300.build.build()")
+            _build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i64, i32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                ctypes.c_float, ctypes.c_size_t)
+        lib.kda_workspace_size.argtypes = [i64, i32, i32, i32]
+        lib.kda_workspace_size.restype = sz
+        lib.kda_fwd.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P, P, sz, P]
+        lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_chunk_prep.argtypes = [P, P, P, P, P, f32, f32, P, i64, i32, i32, i32, P, sz, P]
+        lib.kda_chunk_prep.restype = ctypes.c_int
+        lib.kda_chunk_recurrence.argtypes = [P, sz, P, P, i64, i32, i32, i32, P, P, P]
+        lib.kda_chunk_recurrence.restype = ctypes.c_int
+        lib.kda_device_status.argtypes = [P]
+        lib.kda_device_status.restype = ctypes.c_int
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_selftest_tcgen05.argtypes = [P, P, ctypes.c_int, P, P]
+        lib.kda_selftest_tcgen05.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise KdaError(status, where)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def kda_workspace_size(T_total: int, H: int, N: int, D: int = HEAD_DIM) -> int:
+    return int(load().kda_workspace_size(int(T_total), int(H), int(N), int(D)))
+
+
+def _geometry(q, cu_seqlens, N):
+    T_total, H, D = q.shape
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.shape[0] - 1
+    elif N is None:
+        N = 1
+    return T_total, H, D, int(N)
+
+
+def kda_fwd(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None, cu_seqlens=None,
+            N=None, out=None, final_state=None, workspace=None, stream=None,
+            output_final_state=True):
+    """One forward pass (K1 then K2) on device tensors; returns (out, final_state)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw)):
+        _need(t, name, torch.bfloat16, (T_total, H, D))
+    _need(beta_raw, "beta_raw", torch.bfloat16, (T_total, H))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T_total, H, D))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, D, D))
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    st = load().kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw), float(scale),
+                        float(lower_bound), _ptr(initial_state), _ptr(cu_seqlens), T_total, H, N,
+                        D, _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
+                        _stream(stream))
+    _check(st, "kda_fwd")
+    return out, final_state
+
+
+def kda_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, workspace, cu_seqlens=None,
+                   N=None, stream=None):
+    """K1 alone: writes the chunk records into `workspace` (uint8 device tensor)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    _need(workspace, "workspace", torch.uint8)
+    st = load().kda_chunk_prep(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                               float(scale), float(lower_bound), _ptr(cu_seqlens), T_total, H, N,
+                               D, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "kda_chunk_prep")
+    return workspace
+
+
+def kda_chunk_recurrence(workspace, T_total, H, out, initial_state=None, final_state=None,
+                         cu_seqlens=None, N=None, D=HEAD_DIM, stream=None):
+    """K2 alone, over records written by kda_chunk_prep."""
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+    N = 1 if N is None else int(N)
+    _need(workspace, "workspace", torch.uint8)
+    st = load().kda_chunk_recurrence(_ptr(workspace), workspace.numel(), _ptr(initial_state),
+                                     _ptr(cu_seqlens), int(T_total), int(H), N, int(D), _ptr(out),
+                                     _ptr(final_state), _stream(stream))
+    _check(st, "kda_chunk_recurrence")
+    return out, final_state
+
+
+def kda_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device error word: 0 or a status."""
+    return int(load().kda_device_status(_stream(stream)))
+
+
+def kda_selftest_tcgen05(kend_layout: int = 0, device="cuda"):
+    out1 = torch.zeros((128, 32), dtype=torch.float32, device=device)
+    out2 = torch.zeros((128, 128), dtype=torch.float32, device=device)
+    status = torch.zeros((1,), dtype=torch.int32, device=device)
+    rc = load().kda_selftest_tcgen05(_ptr(out1), _ptr(out2), int(kend_layout), _ptr(status),
+                                     _stream(None))
+    if rc != 0:
+        raise KdaError(rc, "kda_selftest_tcgen05")
+    torch.cuda.synchronize()
+    return out1, out2, int(status.item())
+
+
+def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
+                     cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
+                     stream=None):
+    """Forward pass on host (CPU, ideally pinned) tensors: copies the inputs to the
+    device, runs kda_fwd and copies `out` and the final state back into host
+    tensors (allocated pinned if not given).  Returns (out, final_state)."""
+    stream = torch.cuda.current_stream(device) if stream is None else stream
+    with torch.cuda.stream(stream):
+        dev = [None if x is None else x.to(device, non_blocking=True)
+               for x in (q, k, v, g_raw, beta_raw, initial_state, cu_seqlens)]
+        o_d, s_d = kda_fwd(*dev[:5], scale, lower_bound, dev[5], dev[6], N=N, stream=stream)
+        if out is None:
+            out = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
+        if final_state is None:
+            final_state = torch.empty(s_d.shape, dtype=s_d.dtype, pin_memory=True)
+        out.copy_(o_d, non_blocking=True)
+        final_state.copy_(s_d, non_blocking=True)
+    return out, final_state

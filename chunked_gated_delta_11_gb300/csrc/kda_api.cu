@@ -1,0 +1,200 @@
+// kda_api.cu -- host side of the libkda C ABI (include/kda.h): argument
+// validation, workspace sizing, kernel launches and the device error word.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+
+cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta_raw, float scale, float lower_bound, float eps,
+                              const int32_t* cu, int64_t T_total, int H, int N, void* ws,
+                              int sm_count, cudaStream_t stream);
+cudaError_t launch_recurrence(const void* ws, const float* init, const int32_t* cu,
+                              int64_t T_total, int H, int N, void* out, float* final_state,
+                              int* err, cudaStream_t stream);
+
+// Error word written by kernels when a bounded wait runs out.  Kernels get its
+// address as an argument; cudaGetSymbolAddress is resolved once per device.
+__device__ int g_kda_error = 0;
+
+namespace {
+
+constexpr float kNormEps = 1e-6f;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+kda_status device_info(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.err == nullptr) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kda_error) != cudaSuccess || p == nullptr)
+      return KDA_ERR_LAUNCH;
+    d.sm_count = sms;
+    d.err = static_cast<int*>(p);
+  }
+  out = d;
+  return KDA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_sizes(int64_t T_total, int32_t H, int32_t N, int32_t D,
+                       const int32_t* cu_seqlens) {
+  if (D != KDA_HEAD_DIM) return KDA_ERR_UNSUPPORTED;
+  if (T_total < 0 || H <= 0 || N <= 0) return KDA_ERR_INVALID_ARG;
+  if (!cu_seqlens && (T_total % N) != 0) return KDA_ERR_INVALID_ARG;
+  // grid and index limits: one CTA per (sequence, head); element offsets in int64
+  if (static_cast<int64_t>(N) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (T_total > (static_cast<int64_t>(1) << 40) / (static_cast<int64_t>(H) * KDA_HEAD_DIM))
+    return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status check_inputs(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta_raw, float scale, float lower_bound, int64_t T_total) {
+  if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_UNSUPPORTED;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARG;
+  if (T_total > 0) {
+    if (!q || !k || !v || !g || !beta_raw) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g))
+      return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(beta_raw) & 1u) != 0) return KDA_ERR_INVALID_ARG;
+  }
+  return KDA_OK;
+}
+
+kda_status check_outputs(const void* out, const float* initial_state, const float* final_state,
+                         int64_t T_total) {
+  if (T_total > 0 && (!out || !aligned16(out))) return KDA_ERR_INVALID_ARG;
+  if (initial_state && !aligned16(initial_state)) return KDA_ERR_INVALID_ARG;
+  if (final_state && !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D) {
+  if (check_sizes(T_total, H, N, D, reinterpret_cast<const int32_t*>(1)) != KDA_OK) return 0;
+  const int64_t bytes = slot_count(T_total, N) * H * static_cast<int64_t>(REC_BYTES);
+  return static_cast<size_t>((bytes + 255) & ~static_cast<int64_t>(255));
+}
+
+extern "C" kda_status kda_chunk_prep(const void* q, const void* k, const void* v,
+                                     const void* g_raw, const void* beta_raw, float scale,
+                                     float lower_bound, const int32_t* cu_seqlens,
+                                     int64_t T_total, int32_t H, int32_t N, int32_t D,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total);
+  if (s != KDA_OK) return s;
+  if (!workspace || !aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < kda_workspace_size(T_total, H, N, D)) return KDA_ERR_WORKSPACE;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  if (T_total == 0) return KDA_OK;
+  cudaError_t e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
+                                    cu_seqlens, T_total, H, N, workspace, info.sm_count,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_chunk_recurrence(const void* workspace, size_t workspace_bytes,
+                                           const float* initial_state,
+                                           const int32_t* cu_seqlens, int64_t T_total,
+                                           int32_t H, int32_t N, int32_t D, void* out,
+                                           float* final_state, void* stream) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
+  if (!workspace || !aligned16(workspace)) return KDA_ERR_INVALID_ARG;
+  if (workspace_bytes < kda_workspace_size(T_total, H, N, D)) return KDA_ERR_WORKSPACE;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  cudaError_t e = launch_recurrence(workspace, initial_state, cu_seqlens, T_total, H, N, out,
+                                    final_state, info.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g_raw,
+                              const void* beta_raw, float scale, float lower_bound,
+                              const float* initial_state, const int32_t* cu_seqlens,
+                              int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
+                              float* final_state, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total)) != KDA_OK)
+    return s;
+  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
+  const size_t need = kda_workspace_size(T_total, H, N, D);
+  if (workspace && (!aligned16(workspace) || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+      cudaGetLastError();
+      return KDA_ERR_WORKSPACE;
+    }
+  }
+  cudaError_t e = cudaSuccess;
+  if (T_total > 0)
+    e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, cu_seqlens,
+                          T_total, H, N, ws, info.sm_count, st);
+  if (e == cudaSuccess)
+    e = launch_recurrence(ws, initial_state, cu_seqlens, T_total, H, N, out, final_state,
+                          info.err, st);
+  if (!workspace) cudaFreeAsync(ws, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_device_status(void* stream) {
+  DeviceInfo info;
+  kda_status s = device_info(info);
+  if (s != KDA_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_LAUNCH;
+  int word = 0;
+  if (cudaMemcpy(&word, info.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(info.err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+    return KDA_ERR_TIMEOUT;
+  }
+  return KDA_OK;
+}
+
+extern "C" const char* kda_status_string(kda_status status) {
+  switch (status) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported size or parameter (D must be 128, lower_bound in [-5, 0])";
+    case KDA_ERR_WORKSPACE: return "workspace too small or not allocatable";
+    case KDA_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case KDA_ERR_TIMEOUT: return "a device-side wait ran out; outputs are invalid";
+  }
+  return "unknown status";
+}

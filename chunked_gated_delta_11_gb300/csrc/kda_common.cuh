@@ -1,0 +1,311 @@
+// kda_common.cuh -- device helpers and the chunk-record layout shared by the
+// sm_103a kernels of libkda (chunk kernel K1, recurrence kernel K2).
+//
+// The record is what one 16-token chunk of one head contributes to the
+// chunkwise KDA recurrence ("You Could Have Come Up with Kimi Delta
+// Attention", sec. 6.2-6.5), written so that the recurrence kernel can feed it
+// to tcgen05 MMAs with no reshuffling:
+//
+//   E^T  = U - W S_c^T                 (corrected errors, sec. 6.3, WY form)
+//   O    = Qdec S_c^T + Aqk E^T        (chunk outputs, sec. 6.5)
+//   S'   = S_c Diag(dlast) + E Kend    (state fast-forward, sec. 6.4)
+//
+// Byte layout of one record (REC_BYTES):
+//   [OFF_B1,  +16384)  [W ; Qdec], 32 rows x 128 key channels, fp32 rounded to
+//                      tf32, K-major with the 128-byte swizzle: 4 blocks of 32
+//                      channels, each 32 rows x 128 B; row n of block kb at
+//                      kb*4096 + n*128, its 16-byte piece c at (c ^ (n & 7))*16.
+//                      Rows 0..15 are W, rows 16..31 are Qdec.
+//   [OFF_KH,  +4096)   Kend high part (bf16), MMA operand indexed [d][j]:
+//   [OFF_KL,  +4096)   Kend low part (bf16) = bf16(Kend - high); same layout.
+//   [OFF_U,   +8192)   U^T fp32 [128 value channels][16 tokens].
+//   [OFF_AQK, +1024)   Aqk fp32 [16][16] (chi_ij for j <= i, zero above).
+//   [OFF_DL,  +512)    dlast fp32 [128] = diagonal of D_{0:C-1}.
+// Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace kda {
+
+constexpr int kChunk = 16;
+constexpr int kDim = 128;
+
+constexpr int OFF_B1 = 0;
+constexpr int OFF_KH = 16384;
+constexpr int OFF_KL = 20480;
+constexpr int OFF_U = 24576;
+constexpr int OFF_AQK = 32768;
+constexpr int OFF_DL = 33792;
+constexpr int REC_BYTES = 34304;
+constexpr int REC_STRIDE_SMEM = 34816;  // 1024-aligned stage stride in smem
+
+// Layout of the Kend tiles (MMA2 B operand, 128 rows d x 16 tokens j, bf16,
+// K-major).  0: 32-byte swizzle (row d at d*32, 16-byte piece p at
+// (p ^ ((d >> 2) & 1))*16).  1: no swizzle, 8x16-byte core matrices with
+// the K-direction core stride 128 B and the row-group stride 256 B.
+#ifndef KDA_KEND_LAYOUT
+#define KDA_KEND_LAYOUT 0
+#endif
+
+__host__ __device__ constexpr int b1_offset(int n, int d) {
+  // fp32 element (row n, channel d) of the [W ; Qdec] tile
+  return OFF_B1 + (d >> 5) * 4096 + n * 128 + ((((d & 31) >> 2) ^ (n & 7)) << 4) +
+         ((d & 3) << 2);
+}
+
+__host__ __device__ constexpr int kend_offset(int layout, int d, int j) {
+  // byte offset of bf16 element (d, j) inside one 4096-byte Kend tile
+  return layout == 0 ? d * 32 + ((((j >> 3) ^ (d >> 2)) & 1) << 4) + ((j & 7) << 1)
+                     : (d >> 3) * 256 + (j >> 3) * 128 + ((d & 7) << 4) + ((j & 7) << 1);
+}
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// sigma(x) = 1 / (1 + 2^(-x log2 e)), from the exponential and reciprocal units
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * x));
+}
+
+// fp32 -> tf32 (round to nearest, ties away), kept in an fp32 container
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Every wait in libkda is bounded: ~2^31 SM cycles (about a second) and then
+// the caller records an error and unwinds instead of hanging the GPU.
+constexpr long long kWaitLimitCycles = 1LL << 31;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// bulk (TMA, untiled) copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor core, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// D (tmem, fp32) (+)= A (tmem) * B (smem descriptor); A/B tf32, one K=8 step.
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (tmem, fp32) (+)= A (tmem) * B (smem descriptor); A/B bf16, one K=16 step.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for dense tcgen05.mma with fp32 accumulation.
+// fmt: 1 = bf16 operands (kind::f16), 2 = tf32 operands (kind::tf32).
+// Both operands K-major.  Bits: [4,6) D format (1 = f32), [7,10) A format,
+// [10,13) B format, [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, uint32_t M, uint32_t N) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (all >> 4), version 1 at bit 46, layout type at
+// bits [61,64): 0 = no swizzle, 2 = 128-byte, 4 = 64-byte, 6 = 32-byte swizzle.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns per thread
+#define KDA_R32(r)                                                                              \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),          \
+      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),  \
+      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),            \
+      "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),            \
+      "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define KDA_W32(r)                                                                              \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),      \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),        \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),      \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),      \
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : KDA_R32(r)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      KDA_W32(r)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Named barrier over the first `nthreads` threads (multiple of 32).
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// sequence geometry.  Chunk records of sequence n live at record slots
+// slot0(n) .. slot0(n) + nchunks(n) - 1 with slot0(n) = floor(bos_n / 16) + n,
+// which never overlap and stay below T_total / 16 + N + 1.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void seq_bounds(const int32_t* cu, int64_t T_total, int N, int n,
+                                           int64_t& bos, int64_t& eos) {
+  if (cu) {
+    bos = __ldg(cu + n);
+    eos = __ldg(cu + n + 1);
+  } else {
+    const int64_t L = T_total / N;
+    bos = static_cast<int64_t>(n) * L;
+    eos = bos + L;
+  }
+}
+
+__host__ __device__ __forceinline__ int64_t slot_count(int64_t T_total, int N) {
+  return T_total / kChunk + N + 1;
+}
+
+}  // namespace kda

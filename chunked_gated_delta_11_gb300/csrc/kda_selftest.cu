@@ -1,0 +1,124 @@
+// kda_selftest.cu -- one-CTA check of the tcgen05 operand conventions that the
+// recurrence kernel relies on, with values that are exact in tf32 / bf16 so
+// the fp32 results can be compared bit for bit on the host:
+//
+//   MMA1-like: D1[128 x 32]  = A1[128 x 128] (tf32, tensor memory)
+//                             * B1^T (fp32 [32 x 128] in the record's 128-byte
+//                               swizzled K-major layout), 16 K=8 steps.
+//   MMA2-like: D2[128 x 128] = D0 + A2[128 x 16] (bf16 pairs in tensor memory)
+//                             * B2^T (bf16 [128 x 16] in the Kend layout chosen
+//                               by `kend_layout`), one K=16 step, accumulating.
+//
+// Every smem address the descriptors can form stays inside the 20 KB tile
+// area whatever the layout, so a wrong convention gives wrong numbers only.
+#include "kda_common.cuh"
+
+namespace kda {
+
+__host__ __device__ inline float st_a1(int m, int k) { return ((m * 3 + k * 5) % 11 - 5) * 0.25f; }
+__host__ __device__ inline float st_b1(int n, int k) { return ((n * 7 + k * 3) % 13 - 6) * 0.125f; }
+__host__ __device__ inline float st_a2(int m, int j) { return ((m + 2 * j) % 7 - 3) * 0.5f; }
+__host__ __device__ inline float st_b2(int d, int j) { return ((d * 5 + j * 11) % 9 - 4) * 0.25f; }
+__host__ __device__ inline float st_d0(int m, int d) { return (m - d) * 0.0625f; }
+
+__global__ void __launch_bounds__(128, 1)
+selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int kend_layout,
+                        int* __restrict__ status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* b1 = smem;                       // 16 KB, record OFF_B1 layout
+  uint8_t* b2 = smem + 16384;               // 4 KB, Kend layout
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 20480);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 20488);
+  const int t = threadIdx.x, w = t >> 5;
+
+  for (int e = t; e < 32 * 128; e += 128) {
+    const int n = e >> 7, d = e & 127;
+    *reinterpret_cast<float*>(b1 + b1_offset(n, d)) = st_b1(n, d);
+  }
+  for (int e = t; e < 128 * 16; e += 128) {
+    const int d = e >> 4, j = e & 15;
+    *reinterpret_cast<__nv_bfloat16*>(b2 + kend_offset(kend_layout, d, j)) =
+        __float2bfloat16_rn(st_b2(d, j));
+  }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (w == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // generic-proxy smem writes must be visible to the tensor core (async proxy)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t A1 = tbase, D2 = tbase + 128, D1 = tbase + 256, A2 = tbase + 288;
+  const uint32_t lane_off = static_cast<uint32_t>(w * 32) << 16;
+  const int m = t;
+
+  // A1 row m (fp32), D0 row m, A2 row m (bf16 pairs, low half = even k)
+  for (int q = 0; q < 4; ++q) {
+    uint32_t r[32];
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(st_a1(m, q * 32 + i));
+    tmem_st32(A1 + lane_off + q * 32, r);
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(st_d0(m, q * 32 + i));
+    tmem_st32(D2 + lane_off + q * 32, r);
+  }
+  {
+    uint32_t r[16];
+    for (int c = 0; c < 8; ++c) r[c] = pack_bf16(st_a2(m, 2 * c), st_a2(m, 2 * c + 1));
+    for (int c = 8; c < 16; ++c) r[c] = 0u;
+    tmem_st16(A2 + lane_off, r);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (t == 0) {
+    const uint32_t id1 = make_idesc(2, 128, 32);
+    const uint32_t b1a = smem_u32(b1);
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint64_t bd = make_sdesc(b1a + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
+      mma_tf32_ts(D1, A1 + kk * 8, bd, id1, kk > 0);
+    }
+    const uint32_t id2 = make_idesc(1, 128, 128);
+    const uint64_t bd2 = kend_layout == 0 ? make_sdesc(smem_u32(b2), 16, 256, 6)
+                                          : make_sdesc(smem_u32(b2), 128, 256, 0);
+    mma_bf16_ts(D2, A2, bd2, id2, 1);
+    tc_commit(bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok && t == 0) atomicExch(status, 5);
+  tc_fence_after();
+  if (ok) {
+    uint32_t r[32];
+    tmem_ld32(D1 + lane_off, r);
+    tmem_wait_ld();
+    for (int i = 0; i < 32; ++i) out1[m * 32 + i] = __uint_as_float(r[i]);
+    for (int q = 0; q < 4; ++q) {
+      tmem_ld32(D2 + lane_off + q * 32, r);
+      tmem_wait_ld();
+      for (int i = 0; i < 32; ++i) out2[m * 128 + q * 32 + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (w == 0) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace kda
+
+extern "C" int kda_selftest_tcgen05(float* out1, float* out2, int kend_layout, int* status,
+                                    void* stream) {
+  if (!out1 || !out2 || !status || (kend_layout != 0 && kend_layout != 1)) return 1;
+  const int smem = 20480 + 64 + 1024;
+  kda::selftest_tcgen05_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+      out1, out2, kend_layout, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}

@@ -1,0 +1,137 @@
+/*
+ * kda.h -- C ABI of libkda, a GB300 (sm_103a) forward pass of Kimi Delta
+ * Attention (KDA), the chunkwise gated delta rule with per-channel decay.
+ *
+ * What is computed ("You Could Have Come Up with Kimi Delta Attention",
+ * sec. 4, the boxed KDA update; gates and norms as in "FlashKDA Delta
+ * Attention Algorithm", Core Architecture).  Per sequence n and head h, with
+ * state S (V x K, maps keys to values) starting at initial_state[n][h] or 0,
+ * for each token t of the sequence in order:
+ *
+ *     q^ = q_t / sqrt(|q_t|^2 + 1e-6),  k^ = k_t / sqrt(|k_t|^2 + 1e-6)
+ *     alpha[d] = exp(lower_bound * sigmoid(g_raw_t[d])),  beta = sigmoid(beta_raw_t)
+ *     S~ = S Diag(alpha)                         (forget, per key channel)
+ *     e  = beta (v_t - S~ k^)                    (predict and correct)
+ *     S  = S~ + e k^T                            (write)
+ *     o_t = S (scale q^)                         (read, after the write)
+ *
+ * and final_state[n][h] = S.  The GPU evaluates the same recurrence in
+ * 16-token chunks (sec. 6 of the same page): a token-parallel chunk kernel and
+ * a head-parallel recurrence kernel.
+ *
+ * Tensor conventions (all device pointers, caller-owned, contiguous, row-major,
+ * 16-byte aligned):
+ *   q, k, v, g_raw   bf16 [T_total, H, D]   (tokens of all sequences packed)
+ *   beta_raw         bf16 [T_total, H]
+ *   out              bf16 [T_total, H, D]
+ *   initial_state    fp32 [N, H, V, K] or NULL (= zeros), V = K = D
+ *   final_state      fp32 [N, H, V, K] or NULL (= not written)
+ *   cu_seqlens       int32 [N + 1] on the device, or NULL.  With it, sequence
+ *                    n is tokens [cu_seqlens[n], cu_seqlens[n+1]); it must
+ *                    start at 0, be non-decreasing and end at T_total (not
+ *                    checked: the values live on the device).  Without it
+ *                    there are N sequences of T_total / N tokens each.
+ *   D must be 128 (the head size the kernels are built for).
+ *
+ * Sequences of length 0 are allowed (their final state is the initial one).
+ * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ * stream); nothing synchronises inside.  Argument errors are reported before
+ * anything is launched; errors found on the device (a bounded wait that ran
+ * out) are latched in a device error word that kda_device_status() returns.
+ * libkda keeps no state between calls other than that error word.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null, misaligned or inconsistent argument        */
+  KDA_ERR_UNSUPPORTED = 2, /* D != 128 or lower_bound outside [-5, 0]          */
+  KDA_ERR_WORKSPACE = 3,   /* workspace too small, or its allocation failed     */
+  KDA_ERR_LAUNCH = 4,      /* a CUDA call or kernel launch failed               */
+  KDA_ERR_TIMEOUT = 5      /* a device-side wait ran out (see kda_device_status) */
+} kda_status;
+
+#define KDA_CHUNK 16
+#define KDA_HEAD_DIM 128
+
+/* Bytes of device workspace kda_fwd / kda_chunk_prep / kda_chunk_recurrence
+ * need for these sizes: one chunk record (34304 bytes) per (chunk slot, head),
+ * with T_total / 16 + N + 1 chunk slots, enough for any split of T_total
+ * tokens into N sequences.  Returns 0 for invalid sizes. */
+size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D);
+
+/* Whole forward pass: chunk kernel (K1) then recurrence kernel (K2).
+ * workspace: device buffer of at least kda_workspace_size(...) bytes, 256-byte
+ * aligned, or NULL, in which case libkda allocates it with cudaMallocAsync on
+ * `stream` and frees it with cudaFreeAsync after the kernels.
+ * scale: the read scale (1 / sqrt(D) in the pages); lower_bound in [-5, 0]:
+ * with 16-token chunks this keeps every cumulative decay factor and its
+ * inverse inside the normal fp32 range ("FlashKDA v1: A Deep Dive", sec. 1).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, LAUNCH as listed above. */
+kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g_raw,
+                   const void* beta_raw, float scale, float lower_bound,
+                   const float* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                   int32_t H, int32_t N, int32_t D, void* out, float* final_state,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* K1 alone: the token-parallel chunk kernel.  Writes one record per (chunk,
+ * head) into `workspace` (same size rule as kda_fwd; must not be NULL).  For
+ * chunk c (0-based) of sequence n and head h the record starts at byte
+ *   ((floor(bos_n / 16) + n + c) * H + h) * 34304
+ * with bos_n the first token of sequence n, and holds, for the chunk's tokens
+ * i < 16 (rows past the sequence end are zero), in this order:
+ *   [W ; Qdec] fp32 (tf32-rounded) 32 x 128, 128-byte-swizzled K-major tiles;
+ *   Kend as two bf16 tiles (high part, remainder), 128 x 16;
+ *   U^T fp32 [128][16];  Aqk fp32 [16][16];  dlast fp32 [128];
+ * where (sec. 6.1-6.6 of "You Could Have Come Up with Kimi Delta Attention")
+ *   Qdec_i = scale q^_i D_{0:i},  Kend_i = k^_i D_{i+1:last},
+ *   Akk = (I + R)^-1 with R_ij = beta_i <k^_j|D_{j+1:i}|k^_i> (j < i),
+ *   W = Akk diag(beta) [k^_i D_{0:i}],  U = Akk diag(beta) V,
+ *   Aqk_ij = scale <k^_j|D_{j+1:i}|q^_i> (j <= i),  dlast = diag(D_{0:last}).
+ * The byte layout of each tile is given in chunked_gated_delta_11_gb300/csrc/
+ * kda_common.cuh. */
+kda_status kda_chunk_prep(const void* q, const void* k, const void* v, const void* g_raw,
+                          const void* beta_raw, float scale, float lower_bound,
+                          const int32_t* cu_seqlens, int64_t T_total, int32_t H, int32_t N,
+                          int32_t D, void* workspace, size_t workspace_bytes, void* stream);
+
+/* K2 alone: the head-parallel recurrence over records written by
+ * kda_chunk_prep with the same sizes and cu_seqlens.  One CTA per (sequence,
+ * head) keeps the fp32 state in tensor memory and walks its chunks. */
+kda_status kda_chunk_recurrence(const void* workspace, size_t workspace_bytes,
+                                const float* initial_state, const int32_t* cu_seqlens,
+                                int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
+                                float* final_state, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: KDA_OK, or KDA_ERR_TIMEOUT if a kernel's bounded wait ran
+ * out since the last call (its outputs are then invalid), or KDA_ERR_LAUNCH if
+ * the synchronisation itself failed. */
+kda_status kda_device_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* kda_status_string(kda_status status);
+
+/* Diagnostic: one-CTA check of the tensor-core operand conventions used by
+ * the recurrence kernel (tf32 MMA with A in tensor memory and a 128-byte
+ * swizzled B tile; bf16 MMA with A in tensor memory and the Kend tile layout
+ * `kend_layout` (0 or 1) accumulating into a preset D).  Writes
+ * out1 fp32 [128][32] and out2 fp32 [128][128] (device), and 5 to *status
+ * (device int) if its wait ran out.  Returns 0, 1 for bad arguments, 4 on a
+ * launch error.  The expected values are closed-form small dyadic numbers
+ * (see the kernel source), exact in fp32. */
+int kda_selftest_tcgen05(float* out1, float* out2, int kend_layout, int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -112,6 +112,7 @@ static void recur_unit(const fwd_args *a, int n, int h, double *S,
   seq_bounds(a->cu, a->T_total, a->N, n, &bos, &eos);
   double *pred = work;     /* V */
   double *e = work + V;    /* V */
+  double *alpha = work + 2 * V;  /* K */
   for (int64_t t = bos; t < eos; ++t) {
     const double *qt = a->q + (t * H + h) * (int64_t)K;
     const double *kt = a->k + (t * H + h) * (int64_t)K;
@@ -119,8 +120,9 @@ static void recur_unit(const fwd_args *a, int n, int h, double *S,
     const double *lat = a->la + (t * H + h) * (int64_t)K;
     const double bt = a->beta[t * H + h];
     /* forget: every key channel (column) d decays by alpha_t[d] */
+    for (int d = 0; d < K; ++d) alpha[d] = exp(lat[d]);
     for (int vi = 0; vi < V; ++vi)
-      for (int d = 0; d < K; ++d) S[vi * K + d] *= exp(lat[d]);
+      for (int d = 0; d < K; ++d) S[vi * K + d] *= alpha[d];
     /* predict */
     for (int vi = 0; vi < V; ++vi) {
       double acc = 0.0;
@@ -249,7 +251,7 @@ static void *worker(void *p) {
   const fwd_args *a = w->a;
   const int K = a->K, V = a->V, C = a->chunk > 0 ? a->chunk : 1;
   const size_t wsz = (size_t)C * K + 3 * (size_t)C * V + 2 * (size_t)C * C +
-                     2 * (size_t)V;
+                     2 * (size_t)V + (size_t)K;
   double *S = (double *)malloc(sizeof(double) * (size_t)V * K);
   double *work = (double *)malloc(sizeof(double) * wsz);
   if (!S || !work) {

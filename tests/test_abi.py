@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/kda.h declares, sizes its workspace, and rejects bad
+arguments with the documented status before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import chunked_gated_delta_11_gb300 as kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_gated_delta_11_gb300 import build
+    build.build()
+    return kda.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "kda_fwd" in names and "kda_workspace_size" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in kda.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.build.LIB], capture_output=True,
+                         text=True).stdout
+    for name in names:
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_workspace_size(lib):
+    rec = kda.REC_BYTES
+    assert kda.kda_workspace_size(65536, 32, 8) == ((65536 // 16 + 8 + 1) * 32 * rec + 255) // 256 * 256
+    assert kda.kda_workspace_size(0, 1, 1) >= rec
+    assert kda.kda_workspace_size(64, 1, 1, D=64) == 0
+    assert kda.kda_workspace_size(-1, 1, 1) == 0
+    assert kda.kda_workspace_size(64, 0, 1) == 0
+
+
+FAKE = 1 << 20  # aligned, never dereferenced: validation fails first
+
+
+def call_fwd(lib, *, q=FAKE, out=FAKE, T=64, H=1, N=1, D=128, lb=-5.0, scale=0.1, beta=FAKE,
+             init=None, final=None, ws=None, ws_bytes=0):
+    P = ctypes.c_void_p
+    return lib.kda_fwd(P(q), P(FAKE), P(FAKE), P(FAKE), P(beta), scale, lb, P(init) if init else None,
+                       None, T, H, N, D, P(out), P(final) if final else None,
+                       P(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), 2),                 # head size other than 128
+    (dict(lb=-6.0), 2),              # lower_bound outside [-5, 0]
+    (dict(lb=0.5), 2),
+    (dict(lb=float("nan")), 2),
+    (dict(H=0), 1),
+    (dict(N=0), 1),
+    (dict(T=-1), 1),
+    (dict(T=65, N=2), 1),            # equal split impossible without cu_seqlens
+    (dict(q=0), 1),                  # null input
+    (dict(q=FAKE + 8), 1),           # misaligned input
+    (dict(beta=FAKE + 1), 1),        # misaligned bf16 beta
+    (dict(out=0), 1),                # null output
+    (dict(init=FAKE + 4), 1),        # misaligned state
+    (dict(scale=float("nan")), 1),
+    (dict(ws=FAKE, ws_bytes=100), 3),  # workspace too small
+])
+def test_fwd_rejects_bad_arguments(lib, kw, status):
+    assert call_fwd(lib, **kw) == status
+
+
+def test_stage_entry_points_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    # K1 needs a workspace
+    assert lib.kda_chunk_prep(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0.1, -5.0, None, 64, 1,
+                              1, 128, None, 0, None) == 1
+    assert lib.kda_chunk_prep(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0.1, -5.0, None, 64, 1,
+                              1, 128, P(FAKE), 16, None) == 3
+    # K2: size and output checks
+    assert lib.kda_chunk_recurrence(P(FAKE), 1 << 30, None, None, 64, 1, 1, 100, P(FAKE), None,
+                                    None) == 2
+    assert lib.kda_chunk_recurrence(P(FAKE), 1 << 30, None, None, 64, 1, 1, 128, None, None,
+                                    None) == 1
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = kda.kda_status_string(code)
+        assert isinstance(s, str) and s
+    assert kda.kda_status_string(99) == "unknown status"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import chunked_gated_delta_11_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        m.load()

@@ -1,0 +1,261 @@
+"""GPU parity of libkda against the fp64 oracle, through the C ABI.
+
+Order: tensor-core convention self-test, chunk-kernel records against the
+oracle's chunk factors, then the whole forward pass on every workload (full
+comparison where the oracle is fast, sampled (sequence, head) units at full
+size otherwise), edge cases and properties."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import chunked_gated_delta_11_gb300 as kda
+from chunked_gated_delta_11_gb300 import synth
+from kda_testlib import assert_close, compare_units, f64, oracle_case
+
+pytestmark = pytest.mark.gpu
+
+KEND_LAYOUT = 0  # the layout compiled into the recurrence kernel (KDA_KEND_LAYOUT)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    kda.build.build()
+    kda.load()
+    yield
+    assert kda.kda_device_status() == 0
+
+
+def run(inp, **kw):
+    out, fs = kda.kda_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                          inp["scale"], inp["lower_bound"], inp["initial_state"],
+                          inp["cu_seqlens"], N=inp["N"], **kw)
+    assert kda.kda_device_status() == 0
+    return out, fs
+
+
+def to_dev(inp):
+    out = dict(inp)
+    for key in ("q", "k", "v", "g_raw", "beta_raw", "initial_state", "cu_seqlens"):
+        if inp[key] is not None:
+            out[key] = inp[key].cuda()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 operand conventions (values exact in tf32 / bf16 / fp32)
+# ---------------------------------------------------------------------------
+def _selftest_expected():
+    m = np.arange(128)[:, None]
+    k = np.arange(128)[None, :]
+    A1 = ((m * 3 + k * 5) % 11 - 5) * 0.25
+    n = np.arange(32)[:, None]
+    B1 = ((n * 7 + k * 3) % 13 - 6) * 0.125
+    j = np.arange(16)[None, :]
+    A2 = ((m + 2 * j) % 7 - 3) * 0.5
+    d = np.arange(128)[:, None]
+    B2 = ((d * 5 + j * 11) % 9 - 4) * 0.25
+    D0 = (m - np.arange(128)[None, :]) * 0.0625
+    return A1 @ B1.T, D0 + A2 @ B2.T
+
+
+@pytest.mark.parametrize("layout", [KEND_LAYOUT])
+def test_tcgen05_operand_conventions(layout):
+    out1, out2, status = kda.kda_selftest_tcgen05(layout)
+    assert status == 0
+    e1, e2 = _selftest_expected()
+    np.testing.assert_array_equal(out1.cpu().numpy(), e1.astype(np.float32))
+    np.testing.assert_array_equal(out2.cpu().numpy(), e2.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# K1 records against the oracle's chunk factors
+# ---------------------------------------------------------------------------
+def _b1_offset(n, d):
+    return (d >> 5) * 4096 + n * 128 + ((((d & 31) >> 2) ^ (n & 7)) << 4) + ((d & 3) << 2)
+
+
+def _kend_offset(d, j):
+    if KEND_LAYOUT == 0:
+        return d * 32 + ((((j >> 3) ^ (d >> 2)) & 1) << 4) + ((j & 7) << 1)
+    return (d >> 3) * 256 + (j >> 3) * 128 + ((d & 7) << 4) + ((j & 7) << 1)
+
+
+def decode_record(rec):
+    rec = np.asarray(rec, dtype=np.uint8)
+    nn, dd = np.meshgrid(np.arange(32), np.arange(128), indexing="ij")
+    b1 = rec[:16384].view(np.float32)[(_b1_offset(nn, dd)) // 4]
+    jj, dd2 = np.meshgrid(np.arange(16), np.arange(128), indexing="ij")
+    off = _kend_offset(dd2, jj)
+
+    def bf16_at(base):
+        raw = rec[base:base + 4096].view(np.uint16)[off // 2].astype(np.uint32) << 16
+        return raw.view(np.float32).astype(np.float64)
+
+    kend = bf16_at(16384) + bf16_at(20480)
+    U = rec[24576:32768].view(np.float32).reshape(128, 16).T
+    Aqk = rec[32768:33792].view(np.float32).reshape(16, 16)
+    dl = rec[33792:34304].view(np.float32)
+    return {"W": b1[:16], "Qdec": b1[16:], "Kend": kend, "U": U, "Aqk": Aqk, "dlast": dl}
+
+
+@pytest.mark.parametrize("lengths,H", [([64], 1), ([45], 2), ([7, 0, 33, 16], 2)])
+def test_chunk_records_match_oracle_factors(lengths, H):
+    inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=11, init_std=0.02))
+    T, N = inp["T_total"], inp["N"]
+    ws = torch.zeros(kda.kda_workspace_size(T, H, N), dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_prep(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+                       inp["lower_bound"], ws, inp["cu_seqlens"], N=N)
+    torch.cuda.synchronize()
+    wsh = ws.cpu().numpy()
+    qh, kh, la, beta = oracle.prepare(f64(inp["q"]), f64(inp["k"]), f64(inp["g_raw"]),
+                                      f64(inp["beta_raw"]), inp["lower_bound"])
+    cu = inp["cu_seqlens"].cpu().numpy()
+    f = oracle.chunk_factors(qh, kh, f64(inp["v"]), la, beta, inp["scale"], cu_seqlens=cu)
+    got = {k_: [] for k_ in f if k_ != "Akk"}
+    ref = {k_: [] for k_ in got}
+    chunk = 0
+    for n in range(N):
+        bos, eos = int(cu[n]), int(cu[n + 1])
+        for c in range((eos - bos + 15) // 16):
+            for h in range(H):
+                slot = bos // 16 + n + c
+                r = decode_record(wsh[(slot * H + h) * kda.REC_BYTES:][:kda.REC_BYTES])
+                for key in got:
+                    got[key].append(r[key].reshape(-1))
+                    ref[key].append(f[key][chunk, h].reshape(-1))
+            chunk += 1
+    for key in got:
+        g_ = np.concatenate(got[key])
+        r_ = np.concatenate(ref[key])
+        mx = np.abs(g_ - r_).max() / np.abs(r_).max()
+        fro = np.linalg.norm(g_ - r_) / np.linalg.norm(r_)
+        assert mx < 2e-3 and fro < 1e-3, f"{key}: max_rel {mx:.2e} fro {fro:.2e}"
+
+
+# ---------------------------------------------------------------------------
+# whole forward pass
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "h16"])
+def test_fwd_small_workloads_full(name):
+    inp = to_dev(synth.workload_inputs(name))
+    out, fs = run(inp)
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, f"{name} out")
+    assert_close(f64(fs), rs, f"{name} final_state")
+
+
+@pytest.mark.parametrize("lengths,H,init", [
+    ([1], 1, False), ([15], 1, True), ([16], 3, False), ([17], 2, True), ([33], 1, False),
+    ([0, 5, 0, 17, 32, 1], 2, True), ([300, 1, 47], 4, True),
+])
+def test_fwd_edge_cases(lengths, H, init):
+    inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=sum(lengths) + H,
+                                   init_std=0.02 if init else None))
+    out, fs = run(inp)
+    ro, rs = oracle_case(inp)
+    if inp["T_total"]:
+        assert_close(f64(out), ro, "out")
+    assert_close(f64(fs), rs, "final_state")
+
+
+def test_fwd_equal_batches_without_cu_seqlens():
+    inp = to_dev(synth.make_inputs(3 * 80, 2, 3, seed=5, init_std=0.02))
+    out, fs = run(inp)
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "out")
+    assert_close(f64(fs), rs, "final_state")
+
+
+def test_fwd_empty_input_returns_initial_state():
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[0, 0], seed=1, init_std=0.02))
+    out, fs = run(inp)
+    assert torch.equal(fs, inp["initial_state"])
+
+
+@pytest.mark.parametrize("name,units", [
+    ("b8", [(0, 0), (3, 17), (7, 31)]),
+    ("long", [(0, 0), (0, 31)]),
+    ("slow", [(0, 5)]),
+])
+def test_fwd_full_size_sampled_units(name, units):
+    inp = synth.workload_inputs(name, device="cuda")
+    out, fs = run(inp)
+    compare_units(inp, out, fs, units)
+
+
+def test_fwd_varlen_full_size_sampled_units():
+    inp = synth.workload_inputs("varlen", device="cuda")
+    out, fs = run(inp)
+    cu = inp["cu_seqlens"].cpu().numpy()
+    lens = np.diff(cu)
+    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+    compare_units(inp, out, fs, [(longest, 3), (shortest, 30), (1, 0)])
+
+
+# ---------------------------------------------------------------------------
+# properties
+# ---------------------------------------------------------------------------
+def test_deterministic():
+    inp = to_dev(synth.workload_inputs("h16"))
+    o1, s1 = run(inp)
+    o2, s2 = run(inp)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_streaming_split_chains_state():
+    inp = to_dev(synth.workload_inputs("h16"))
+    o, s = run(inp)
+    for t1, exact in ((2048, True), (1000, False)):
+        a = {k: inp[k] for k in inp}
+        b = {k: inp[k] for k in inp}
+        for key in ("q", "k", "v", "g_raw", "beta_raw"):
+            a[key] = inp[key][:t1].contiguous()
+            b[key] = inp[key][t1:].contiguous()
+        a["T_total"], b["T_total"] = t1, inp["T_total"] - t1
+        oa, sa = run(a)
+        b["initial_state"] = sa
+        ob, sb = run(b)
+        oc = torch.cat([oa, ob])
+        if exact:  # chunk-aligned split: the same chunks, bit for bit
+            assert torch.equal(oc, o) and torch.equal(sb, s)
+        else:
+            assert_close(f64(oc), f64(o), "split out")
+            assert_close(f64(sb), f64(s), "split state")
+
+
+def test_varlen_packing_equals_separate_calls():
+    lengths = [37, 16, 100]
+    inp = to_dev(synth.make_inputs(0, 2, lengths=lengths, seed=3, init_std=0.02))
+    o, s = run(inp)
+    cu = inp["cu_seqlens"].cpu().tolist()
+    for n in range(3):
+        sl = slice(cu[n], cu[n + 1])
+        one = {k: inp[k] for k in inp}
+        for key in ("q", "k", "v", "g_raw", "beta_raw"):
+            one[key] = inp[key][sl].contiguous()
+        one["initial_state"] = inp["initial_state"][n:n + 1].contiguous()
+        one["cu_seqlens"], one["N"], one["T_total"] = None, 1, lengths[n]
+        on, sn = run(one)
+        assert torch.equal(on, o[sl]) and torch.equal(sn[0], s[n])
+
+
+def test_beta_zero_is_pure_decay():
+    inp = to_dev(synth.make_inputs(64, 2, 1, seed=9, init_std=0.02))
+    inp["beta_raw"] = torch.full_like(inp["beta_raw"], float("-inf"))
+    out, fs = run(inp)
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "out")
+    assert_close(f64(fs), rs, "final_state")
+
+
+def test_host_buffer_entry_point():
+    inp = synth.workload_inputs("tiny")
+    out, fs = kda.kda_forward_host(inp["q"].pin_memory(), inp["k"].pin_memory(),
+                                   inp["v"].pin_memory(), inp["g_raw"].pin_memory(),
+                                   inp["beta_raw"].pin_memory(), inp["scale"],
+                                   inp["lower_bound"])
+    torch.cuda.synchronize()
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "out")
+    assert_close(f64(fs), rs, "final_state")
