@@ -39,6 +39,7 @@ def errors(got, ref):
 
 def assert_close(got, ref, what):
     mx, fro = errors(got, ref)
+    print(f"[parity] {what}: max_rel {mx:.3e} fro {fro:.3e}")
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     assert mx <= MAX_REL and fro <= FRO_REL, f"{what}: max_rel {mx:.3e} fro {fro:.3e}"
     return mx, fro

@@ -241,7 +241,8 @@ def test_varlen_packing_equals_separate_calls():
 
 
 def test_beta_zero_is_pure_decay():
-    inp = to_dev(synth.make_inputs(64, 2, 1, seed=9, init_std=0.02))
+    # slow decay (g_raw ~ N(-4, 1)) so that the decayed state stays in fp32 range
+    inp = to_dev(synth.make_inputs(64, 2, 1, seed=9, init_std=0.02, g_mean=-4.0))
     inp["beta_raw"] = torch.full_like(inp["beta_raw"], float("-inf"))
     out, fs = run(inp)
     ro, rs = oracle_case(inp)
