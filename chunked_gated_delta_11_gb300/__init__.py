@@ -23,7 +23,7 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
-    "kda_forward_host", "REC_BYTES", "CHUNK", "HEAD_DIM",
+    "kda_forward_host", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
 ]
 
 CHUNK = 16
@@ -62,6 +62,9 @@ def load(build_if_missing: bool = False):
         lib.kda_workspace_size.restype = sz
         lib.kda_fwd.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P, P, sz, P]
         lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_fwd_noalloc.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P,
+                                        P]
+        lib.kda_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_prep.argtypes = [P, P, P, P, P, f32, f32, P, i64, i32, i32, i32, P, sz, P]
         lib.kda_chunk_prep.restype = ctypes.c_int
         lib.kda_chunk_recurrence.argtypes = [P, sz, P, P, i64, i32, i32, i32, P, P, P]
@@ -148,6 +151,25 @@ def kda_fwd(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None, cu
                         D, _ptr(out), _ptr(final_state), _ptr(workspace), ws_bytes,
                         _stream(stream))
     _check(st, "kda_fwd")
+    return out, final_state
+
+
+NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
+
+
+def kda_fwd_noalloc(q, k, v, g_raw, beta_raw, scale, lower_bound, out, final_state=None,
+                    initial_state=None, cu_seqlens=None, N=None, stream=None):
+    """kda_fwd for callers that cannot allocate device memory: the chunk records
+    go to a fixed 64 MiB array inside libkda, so the call allocates nothing.
+    `out` (and `final_state`, if wanted) must be given.  Sizes whose workspace
+    exceeds 64 MiB raise KdaError(KDA_ERR_WORKSPACE).  Calls that overlap on the
+    GPU share that array and race."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    st = load().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                                float(scale), float(lower_bound), _ptr(initial_state),
+                                _ptr(cu_seqlens), T_total, H, N, D, _ptr(out), _ptr(final_state),
+                                _stream(stream))
+    _check(st, "kda_fwd_noalloc")
     return out, final_state
 
 

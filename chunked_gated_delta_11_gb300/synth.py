@@ -20,6 +20,7 @@ Workloads (all D = d_k = d_v = 128, lower_bound = -5, scale = 128 ** -0.5):
  long    1 sequence of 131072 tokens, H = 32; g_raw ~ N(2, 1); zero state
  slow    unscored stress variant of ``long`` with g_raw ~ N(-6, 1), i.e.
          retention close to 1 (long-range accumulation)
+ b2      profiling size: 2 sequences of 8192 tokens, H = 32
 ======  =====================================================================
 
 Draw order is q, k, v, g_raw, beta_raw, initial_state; sequence lengths come
@@ -58,6 +59,8 @@ WORKLOADS = {
     "varlen": Workload("varlen", H=32, N=64, T=None, init_std=0.02, max_len=16384, seed=3),
     "long": Workload("long", H=32, N=1, T=131072, init_std=None, g_mean=2.0, seed=4),
     "slow": Workload("slow", H=32, N=1, T=131072, init_std=None, g_mean=-6.0, seed=5),
+    # profiling size: like b8 with 2 sequences (inputs 537 MB, still larger than L2)
+    "b2": Workload("b2", H=32, N=2, T=8192, init_std=None, seed=6),
 }
 
 

@@ -82,6 +82,34 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g_ra
                    int32_t H, int32_t N, int32_t D, void* out, float* final_state,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the fixed workspace array used by kda_fwd_noalloc (64 MiB). */
+#define KDA_NOALLOC_WORKSPACE_BYTES (64 * 1024 * 1024)
+
+/* kda_fwd without any allocation, for callers that cannot allocate device
+ * memory (for example a plugin inside a host engine that owns all device
+ * memory and offers no allocator).  The pages have no counterpart to this
+ * entry point; it exists for such callers only.
+ * Same arguments and results as kda_fwd, minus the workspace: the K1->K2
+ * records go to a fixed 64 MiB device array inside libkda, which every GPU that
+ * loads the library's device code holds until the process exits.
+ * Limit: kda_workspace_size(T_total, H, N, D) must not exceed
+ * KDA_NOALLOC_WORKSPACE_BYTES (e.g. T_total + 16 (N + 1) <= 976 tokens at
+ * H = 32, <= 31,296 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
+ * anything is launched.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (once per device, with that device current), so make
+ * that first call before any stream capture.  All calls share the one array:
+ * calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race on it and their results are undefined; calls ordered on one stream are
+ * fine.  The array keeps the previous call's contents; nothing in it needs to
+ * start at zero.  No cudaMalloc, cudaFree or other allocating routine is
+ * called. */
+kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const void* g_raw,
+                           const void* beta_raw, float scale, float lower_bound,
+                           const float* initial_state, const int32_t* cu_seqlens,
+                           int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
+                           float* final_state, void* stream);
+
 /* K1 alone: the token-parallel chunk kernel.  Writes one record per (chunk,
  * head) into `workspace` (same size rule as kda_fwd; must not be NULL).  For
  * chunk c (0-based) of sequence n and head h the record starts at byte
