@@ -4,8 +4,8 @@
 Default workload: B = 8 sequences x T = 8192 tokens, H = 32 heads, D = 128,
 bf16, lower_bound = -5, zero initial state (seeded synthetic inputs; see
 chunked_gated_delta_11_gb300/synth.py).  A step is one whole forward pass
-(kda_fwd: chunk kernel, then recurrence kernel) over that batch, inputs and
-workspace resident in HBM.  Inputs (2.1 GB) are larger than the 129 MB L2, so
+over that batch (default: kda_fwd_fused, one kernel; --path split: kda_fwd,
+chunk kernel then recurrence kernel), inputs resident in HBM.  Inputs (2.1 GB) are larger than the 129 MB L2, so
 no flush runs between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -208,6 +208,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b8")
+    ap.add_argument("--path", choices=["fused", "split"], default="fused",
+                    help="fused: kda_fwd_fused (one kernel); split: kda_fwd (K1 + K2)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=0,
                     help="oracle sample size for cpu_baseline (0 = one unit per core)")
@@ -237,8 +239,13 @@ def main():
     a = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
          inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"])
 
-    def step():
+    def step_split():
         kda.kda_fwd(*a, N=N, out=out, final_state=fs, workspace=ws, stream=stream)
+
+    def step_fused():
+        kda.kda_fwd_fused(*a, N=N, out=out, final_state=fs, stream=stream)
+
+    step = step_fused if args.path == "fused" else step_split
 
     for _ in range(args.warmup):
         step()
@@ -259,10 +266,19 @@ def main():
     ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
     assert kda.kda_device_status() == 0
 
-    # per-kernel durations on the same stream (K1 = chunk kernel, K2 = recurrence)
+    # the other path, and the split path's per-kernel durations, on the same stream
+    reps = max(10, min(args.steps, 50))
+    other = step_split if args.path == "fused" else step_fused
+    for _ in range(3):
+        other()
+    ev0.record(stream)
+    for _ in range(reps):
+        other()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    other_ms = ev0.elapsed_time(ev1) / reps
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     k1_ms = k2_ms = 0.0
-    reps = max(10, min(args.steps, 50))
     for _ in range(reps):
         evs[0].record(stream)
         kda.kda_chunk_prep(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
@@ -287,7 +303,8 @@ def main():
     def e2e_step():
         kda.kda_forward_host(host["q"], host["k"], host["v"], host["g_raw"], host["beta_raw"],
                              inp["scale"], inp["lower_bound"], host["initial_state"],
-                             host["cu_seqlens"], N=N, out=out_h, final_state=fs_h, stream=stream)
+                             host["cu_seqlens"], N=N, out=out_h, final_state=fs_h, stream=stream,
+                             fused=args.path == "fused")
 
     e2e_ms = None
     if args.e2e_steps > 0:
@@ -322,26 +339,30 @@ def main():
             "global_batch": N * world, "seq_len": T // N if inp["cu_seqlens"] is None else None,
             "heads": H, "head_dim": 128, "tokens_per_step": tokens_per_step,
             "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
-            "path": "kda_fwd = chunk_prep_kernel (K1) + recurrence_kernel (K2, tcgen05)",
+            "path": ("kda_fwd_fused = fused_kernel (chunk math + tcgen05 recurrence, one launch)"
+                     if args.path == "fused" else
+                     "kda_fwd = chunk_prep_kernel (K1) + recurrence_kernel (K2, tcgen05)"),
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "traffic": None,
-            "kernel": "whole kda_fwd step (K1 + K2)",
+            "kernel": "fused_kernel (the whole step)" if args.path == "fused"
+                      else "whole kda_fwd step (K1 + K2)",
             "alg_bytes_per_launch": alg_bytes, "alg_flop_per_launch": alg_flop,
             "tensor_frac": alg_flop / (ms * 1e-3) / 1e12 / tc,
             "roofline_ms": max(alg_bytes / hbm / 1e9, alg_flop / tc / 1e12) * 1e3,
             "peak_source": f"{peak_src} (hbm_gbs; bf16_tflops for tensor_frac)",
         },
         "kernels": {
-            "chunk_prep_kernel": {"ms": k1_ms, "share": k1_ms / (k1_ms + k2_ms)},
-            "recurrence_kernel": {"ms": k2_ms, "share": k2_ms / (k1_ms + k2_ms)},
+            "fused_kernel": {"ms": ms if args.path == "fused" else other_ms},
+            "split_path": {"ms": other_ms if args.path == "fused" else ms,
+                           "chunk_prep_kernel_ms": k1_ms, "recurrence_kernel_ms": k2_ms},
         },
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {
             "value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if args.path == "fused" else 2) * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1

@@ -23,7 +23,7 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
-    "kda_forward_host", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
+    "kda_forward_host", "kda_fwd_fused", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
 ]
 
 CHUNK = 16
@@ -62,6 +62,8 @@ def load(build_if_missing: bool = False):
         lib.kda_workspace_size.restype = sz
         lib.kda_fwd.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P, P, sz, P]
         lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_fwd_fused.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P, P]
+        lib.kda_fwd_fused.restype = ctypes.c_int
         lib.kda_fwd_noalloc.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P,
                                         P]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
@@ -154,6 +156,32 @@ def kda_fwd(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None, cu
     return out, final_state
 
 
+def kda_fwd_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
+                  cu_seqlens=None, N=None, out=None, final_state=None, stream=None,
+                  output_final_state=True):
+    """One forward pass in a single kernel (records stay in shared memory);
+    returns (out, final_state)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw)):
+        _need(t, name, torch.bfloat16, (T_total, H, D))
+    _need(beta_raw, "beta_raw", torch.bfloat16, (T_total, H))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T_total, H, D))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, D, D))
+    st = load().kda_fwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                              float(scale), float(lower_bound), _ptr(initial_state),
+                              _ptr(cu_seqlens), T_total, H, N, D, _ptr(out), _ptr(final_state),
+                              _stream(stream))
+    _check(st, "kda_fwd_fused")
+    return out, final_state
+
+
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 
@@ -218,15 +246,17 @@ def kda_selftest_tcgen05(kend_layout: int = 0, device="cuda"):
 
 def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
                      cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
-                     stream=None):
+                     stream=None, fused=True):
     """Forward pass on host (CPU, ideally pinned) tensors: copies the inputs to the
-    device, runs kda_fwd and copies `out` and the final state back into host
-    tensors (allocated pinned if not given).  Returns (out, final_state)."""
+    device, runs kda_fwd_fused (or kda_fwd with fused=False) and copies `out` and
+    the final state back into host tensors (allocated pinned if not given).
+    Returns (out, final_state)."""
     stream = torch.cuda.current_stream(device) if stream is None else stream
+    fwd = kda_fwd_fused if fused else kda_fwd
     with torch.cuda.stream(stream):
         dev = [None if x is None else x.to(device, non_blocking=True)
                for x in (q, k, v, g_raw, beta_raw, initial_state, cu_seqlens)]
-        o_d, s_d = kda_fwd(*dev[:5], scale, lower_bound, dev[5], dev[6], N=N, stream=stream)
+        o_d, s_d = fwd(*dev[:5], scale, lower_bound, dev[5], dev[6], N=N, stream=stream)
         if out is None:
             out = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
         if final_state is None:

@@ -16,6 +16,10 @@ cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const
 cudaError_t launch_recurrence(const void* ws, const float* init, const int32_t* cu,
                               int64_t T_total, int H, int N, void* out, float* final_state,
                               int* err, cudaStream_t stream);
+cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
+                         const void* beta_raw, float scale, float lower_bound, float eps,
+                         const float* init, const int32_t* cu, int64_t T_total, int H, int N,
+                         void* out, float* final_state, int* err, cudaStream_t stream);
 
 // Error word written by kernels when a bounded wait runs out.  Kernels get its
 // address as an argument; cudaGetSymbolAddress is resolved once per device.
@@ -167,6 +171,25 @@ extern "C" kda_status kda_fwd(const void* q, const void* k, const void* v, const
     e = launch_recurrence(ws, initial_state, cu_seqlens, T_total, H, N, out, final_state,
                           info.err, st);
   if (!workspace) cudaFreeAsync(ws, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_fwd_fused(const void* q, const void* k, const void* v,
+                                    const void* g_raw, const void* beta_raw, float scale,
+                                    float lower_bound, const float* initial_state,
+                                    const int32_t* cu_seqlens, int64_t T_total, int32_t H,
+                                    int32_t N, int32_t D, void* out, float* final_state,
+                                    void* stream) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total)) != KDA_OK)
+    return s;
+  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  cudaError_t e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
+                               initial_state, cu_seqlens, T_total, H, N, out, final_state,
+                               info.err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

@@ -101,6 +101,10 @@ __device__ __forceinline__ void lower_mul(const float (*P)[17], const float (*Q)
   }
 }
 
+// Barrier over the 128 threads that build records (named barrier 1, so that a
+// larger CTA can run other warps beside them).
+__device__ __forceinline__ void chunk_sync() { named_bar(1, 128); }
+
 // Build the record of one chunk.  All 128 threads of the group must call it.
 // q..g point at token t0, head h of [T, H, 128] bf16 tensors (row stride
 // `row_stride` elements); beta_raw points at [t0][h] (stride H).  `rec` is the
@@ -134,7 +138,7 @@ __device__ __forceinline__ void build_chunk_record(
   if (t < 16) {
     S.beta[t] = (t < nc) ? sigmoid_fast(__bfloat162float(beta_raw[t * beta_stride])) : 0.f;
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- per-token inverse norms (warp w: tokens 4w .. 4w+3) ----
 #pragma unroll
@@ -156,7 +160,7 @@ __device__ __forceinline__ void build_chunk_record(
       S.rk[i] = rsqrtf(sk + eps);
     }
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- gates, decayed factors (thread t = key channel d) ----
   {
@@ -222,7 +226,7 @@ __device__ __forceinline__ void build_chunk_record(
     }
     reinterpret_cast<float*>(rec + OFF_DL)[d] = dlast;
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- Mkk (warps 0,1) and Mqk (warps 2,3), split-bf16 mma.sync ----
   {
@@ -249,7 +253,7 @@ __device__ __forceinline__ void build_chunk_record(
     S.M[mat][r0 + 8][c0] = acc[2];
     S.M[mat][r0 + 8][c0 + 1] = acc[3];
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- R, I - R, Aqk ----
   {
@@ -263,21 +267,21 @@ __device__ __forceinline__ void build_chunk_record(
       reinterpret_cast<float*>(rec + OFF_AQK)[i * 16 + j] = (j <= i) ? S.M[1][i][j] : 0.f;
     }
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) ----
   lower_mul(S.mat[0], S.mat[0], S.mat[2], false, t);  // R^2
-  __syncthreads();
+  chunk_sync();
   lower_mul(S.mat[1], S.mat[2], S.mat[3], true, t);   // (I - R)(I + R^2)
-  __syncthreads();
+  chunk_sync();
   lower_mul(S.mat[2], S.mat[2], S.mat[0], false, t);  // R^4
-  __syncthreads();
+  chunk_sync();
   lower_mul(S.mat[3], S.mat[0], S.mat[1], true, t);   // ... (I + R^4)
-  __syncthreads();
+  chunk_sync();
   lower_mul(S.mat[0], S.mat[0], S.mat[2], false, t);  // R^8
-  __syncthreads();
+  chunk_sync();
   lower_mul(S.mat[1], S.mat[2], S.mat[3], true, t);   // ... (I + R^8) = A
-  __syncthreads();
+  chunk_sync();
 
   // ---- A diag(beta), split into bf16 high / low ----
   {
@@ -291,7 +295,7 @@ __device__ __forceinline__ void build_chunk_record(
       S.abl[i * AS + j] = lo;
     }
   }
-  __syncthreads();
+  chunk_sync();
 
   // ---- W = A diag(beta) Kdec, U = A diag(beta) V (warp w: channels 32w..32w+31) ----
   {
@@ -328,7 +332,7 @@ __device__ __forceinline__ void build_chunk_record(
       }
     }
   }
-  __syncthreads();
+  chunk_sync();
 }
 
 // Locate record slot `slot`: the sequence n with slot0(n) <= slot < slot0(n+1)

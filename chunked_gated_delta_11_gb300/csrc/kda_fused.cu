@@ -1,0 +1,153 @@
+// kda_fused.cu -- the single-kernel forward path.  One CTA per (sequence,
+// head) builds each chunk record in shared memory and runs the recurrence on
+// it, so the records never travel through HBM: HBM traffic is the algorithmic
+// q, k, v, g_raw, beta_raw in and out out (plus the states).
+//
+// Roles (288 threads, two CTAs per SM):
+//   warps 0-3  state threads (tensor-memory lanes 0-127)      kda_state.cuh
+//   warp 4     lane 0 issues the tcgen05 MMAs                 kda_state.cuh
+//   warps 5-8  chunk threads: build record c+1 into the other stage of a
+//              2-stage ring while the state threads work on record c
+//                                                             kda_chunk.cuh
+// The chunk threads write the records with ordinary shared-memory stores; each
+// of them fences those stores against the tensor core's (async-proxy) reads
+// and then arrives on full[s].
+//
+// FlashKDA measured its fused prototype as slower than the two-kernel split
+// ("FlashKDA v1: A Deep Dive", sec. 2) because the token-parallel work waited
+// on the serial recurrence; here the chunk math of chunk c+1 overlaps the
+// recurrence of chunk c inside every CTA instead.
+#include "kda_chunk.cuh"
+#include "kda_state.cuh"
+
+namespace kda {
+
+constexpr int F_NST = 2;
+constexpr int F_THREADS = 288;
+constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
+constexpr int F_CTL_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
+constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
+
+// AND of `pred` over the 128 chunk threads (named barrier 1).
+__device__ __forceinline__ bool chunk_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(F_THREADS, 2)
+fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+             const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+             const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e, float eps,
+             const float* __restrict__ init, const int32_t* __restrict__ cu, int64_t T_total,
+             int H, int N, __nv_bfloat16* __restrict__ out, float* __restrict__ final_state,
+             int* __restrict__ err) {
+  constexpr int NST = F_NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  ChunkSmem& CS = *reinterpret_cast<ChunkSmem*>(smem + F_CHUNK_OFF);
+  auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + F_CTL_OFF);
+  const int t = threadIdx.x, w = t >> 5, l = t & 31;
+  const int unit = blockIdx.x;
+  const int n = unit / H, h = unit - (unit / H) * H;
+  int64_t bos, eos;
+  seq_bounds(cu, T_total, N, n, bos, eos);
+  const int nchunks = static_cast<int>((eos - bos + kChunk - 1) / kChunk);
+
+  if (t == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&ctl->full[s], 128);
+      mbar_init(&ctl->empty[s], 129);
+    }
+    mbar_init(&ctl->mma1, 1);
+    mbar_init(&ctl->mma2, 1);
+    mbar_init(&ctl->eready, 128);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (w == 0) {
+    tmem_alloc(&ctl->tmem, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = ctl->tmem;
+  const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
+  const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
+  if (w < 4)
+    load_state(tb, lane_off, init ? init + state_base + static_cast<int64_t>(t) * kDim : nullptr);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (w >= 5) {
+    // ---------------- chunk threads ----------------
+    const int tc = t - 160;
+    const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % NST;
+      bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
+      ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
+      if (!chunk_all(ok)) break;
+      const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
+      const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
+      const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
+      build_chunk_record(CS, q + base, k + base, v + base, g + base, beta_raw + t0 * H + h,
+                         row_stride, H, nc, scale, lb_log2e, eps, smem + s * REC_STRIDE_SMEM, tc);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&ctl->full[s]);
+    }
+  } else if (w == 4) {
+    if (l == 0) {
+      int mma_chunks = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % NST;
+        if (!issue_chunk_mmas(ctl, c, s, smem_u32(smem + s * REC_STRIDE_SMEM), tb, err)) break;
+        ++mma_chunks;
+      }
+      if (*reinterpret_cast<volatile int*>(&ctl->abort)) {
+        mbar_wait(&ctl->mma1, mma_chunks & 1);  // MMA1 of the chunk that stopped, if issued
+        if (mma_chunks) mbar_wait(&ctl->mma2, (mma_chunks - 1) & 1);
+      }
+    }
+  } else {
+    state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
+               final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
+               err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (w == 0) tmem_dealloc(tb, TM_COLS);
+}
+
+cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
+                         const void* beta_raw, float scale, float lower_bound, float eps,
+                         const float* init, const int32_t* cu, int64_t T_total, int H, int N,
+                         void* out, float* final_state, int* err, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t units = static_cast<int64_t>(N) * H;
+  if (units == 0) return cudaSuccess;
+  fused_kernel<<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
+      static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
+      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, err);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

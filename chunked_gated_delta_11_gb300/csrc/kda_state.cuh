@@ -1,0 +1,205 @@
+// kda_state.cuh -- the recurrence side of the chunkwise KDA forward pass
+// ("You Could Have Come Up with Kimi Delta Attention", sec. 6.3-6.5), shared by
+// the head-parallel recurrence kernel (records streamed from HBM) and the fused
+// kernel (records built in shared memory by the same CTA).
+//
+// One CTA owns one (sequence, head) unit.  Its 128 x 128 fp32 state S lives in
+// tensor memory, row v in lane v.  For each chunk record (kda_common.cuh):
+//
+//   MMA1 (tcgen05 kind::tf32, M=128 N=32 K=128, issued by one thread):
+//        D1[v][n] = sum_d S[v][d] B1[n][d],  B1 = [W ; Qdec]
+//        -> D1[v][i] = (W S^T)[i][v],  D1[v][16+i] = (Qdec S^T)[i][v]
+//   state threads (thread v = row v):
+//        S[v][:] *= dlast                                  (forget, sec. 6.4)
+//        e[v][i] = U[i][v] - D1[v][i]                       (corrected errors)
+//        E^T -> tensor memory as bf16 high part + bf16 remainder
+//   MMA2 (tcgen05 kind::f16 bf16, M=128 N=128 K=16, three instructions):
+//        S += E^T_hi Kend_hi + E^T_lo Kend_hi + E^T_hi Kend_lo   (write, sec. 6.4)
+//   state threads, overlapping MMA2 and the next MMA1:
+//        o[i][v] = D1[v][16+i] + sum_{j<=i} Aqk[i][j] e[v][j]      (read, sec. 6.5)
+//
+// MMA1 takes the fp32 state as its A operand directly (the tensor core reads its
+// tf32 part), so no operand copy of S is kept.  Barriers per CTA (mbarriers):
+// full[s] (record s ready), empty[s] (record s consumed: 128 state threads + one
+// MMA commit), mma1/mma2 (MMA completion), eready (128 state threads wrote E^T).
+// Every wait is bounded; a timeout sets the CTA's abort flag and the error word.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_A2H = 160, TM_A2L = 168, TM_COLS = 256;
+
+template <int NST>
+struct StateCtl {
+  uint64_t full[NST];
+  uint64_t empty[NST];
+  uint64_t mma1, mma2, eready;
+  uint32_t tmem;
+  int abort;
+};
+
+template <class Ctl>
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+      atomicExch(err, 5);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t kend_desc(uint32_t saddr) {
+#if KDA_KEND_LAYOUT == 0
+  return make_sdesc(saddr, 16, 256, 6);
+#else
+  return make_sdesc(saddr, 128, 256, 0);
+#endif
+}
+
+// Initial state (or zeros) -> tensor memory.  State threads only (t < 128).
+__device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
+                                           const float* __restrict__ src) {
+#pragma unroll
+  for (int qd = 0; qd < 4; ++qd) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const float4 x = src ? __ldg(reinterpret_cast<const float4*>(src + qd * 32 + i))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      r[i] = __float_as_uint(x.x);
+      r[i + 1] = __float_as_uint(x.y);
+      r[i + 2] = __float_as_uint(x.z);
+      r[i + 3] = __float_as_uint(x.w);
+    }
+    tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+  }
+  tmem_wait_st();
+}
+
+// MMA1 and MMA2 of chunk c on the record at shared address `sb` (issuing thread
+// only).  Returns false if a wait gave up.
+template <int NST>
+__device__ __forceinline__ bool issue_chunk_mmas(StateCtl<NST>* ctl, int c, int s, uint32_t sb,
+                                                 uint32_t tb, int* err) {
+  const uint32_t id1 = make_idesc(2, 128, 32), id2 = make_idesc(1, 128, 128);
+  if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) return false;
+  if (c > 0 && !wait_or_abort(&ctl->mma2, (c - 1) & 1, ctl, err)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < 16; ++kk) {
+    const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
+    mma_tf32_ts(tb + TM_D1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+  }
+  tc_commit(&ctl->mma1);
+  if (!wait_or_abort(&ctl->eready, c & 1, ctl, err)) return false;
+  tc_fence_after();
+  const uint64_t kh = kend_desc(sb + OFF_KH), kl = kend_desc(sb + OFF_KL);
+  mma_bf16_ts(tb + TM_S, tb + TM_A2H, kh, id2, 1u);
+  mma_bf16_ts(tb + TM_S, tb + TM_A2L, kh, id2, 1u);
+  mma_bf16_ts(tb + TM_S, tb + TM_A2H, kl, id2, 1u);
+  tc_commit(&ctl->mma2);
+  tc_commit(&ctl->empty[s]);
+  return true;
+}
+
+// The state threads' work for all chunks, then the final state.  `ring` is the
+// 1024-aligned record ring (stage stride REC_STRIDE_SMEM).
+template <int NST>
+__device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, const uint8_t* ring, int nchunks,
+                                           uint32_t tb, uint32_t lane_off, int v, int64_t bos,
+                                           int64_t eos, int H, int h,
+                                           __nv_bfloat16* __restrict__ out,
+                                           float* __restrict__ final_dst, int* err) {
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int s = c % NST;
+    const uint8_t* st = ring + s * REC_STRIDE_SMEM;
+    if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) { ok = false; break; }
+    if (!wait_or_abort(&ctl->mma1, c & 1, ctl, err)) { ok = false; break; }
+    tc_fence_after();
+    // forget: S[v][:] *= dlast (MMA1 has finished reading S)
+    const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      uint32_t r[32];
+      tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 dv = dl4[qd * 8 + i4];
+        r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
+        r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
+        r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
+        r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
+      }
+      tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+    }
+    uint32_t d1[32];
+    tmem_ld32(tb + TM_D1 + lane_off, d1);
+    tmem_wait_ld();
+    // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v]
+    const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
+    float e[16];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4) {
+      const float4 u = U4[i4];
+      e[i4 * 4 + 0] = u.x - __uint_as_float(d1[i4 * 4 + 0]);
+      e[i4 * 4 + 1] = u.y - __uint_as_float(d1[i4 * 4 + 1]);
+      e[i4 * 4 + 2] = u.z - __uint_as_float(d1[i4 * 4 + 2]);
+      e[i4 * 4 + 3] = u.w - __uint_as_float(d1[i4 * 4 + 3]);
+    }
+    {
+      uint32_t pk[16];
+#pragma unroll
+      for (int c2 = 0; c2 < 8; ++c2) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(e[2 * c2]);
+        const __nv_bfloat16 h1 = __float2bfloat16_rn(e[2 * c2 + 1]);
+        pk[c2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                 (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        pk[8 + c2] =
+            pack_bf16(e[2 * c2] - __bfloat162float(h0), e[2 * c2 + 1] - __bfloat162float(h1));
+      }
+      tmem_st16(tb + TM_A2H + lane_off, pk);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&ctl->eready);
+    // outputs o[i][v] = (Qdec S^T)[i][v] + sum_{j <= i} Aqk[i][j] e[v][j]
+    const float* Aq = reinterpret_cast<const float*>(st + OFF_AQK);
+    const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
+    const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
+    __nv_bfloat16* orow = out + (t0 * H + h) * kDim + v;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float o = __uint_as_float(d1[16 + i]);
+#pragma unroll
+      for (int j = 0; j <= i; ++j) o = fmaf(Aq[i * 16 + j], e[j], o);
+      if (i < nc) orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(o);
+    }
+    mbar_arrive(&ctl->empty[s]);
+  }
+  if (ok && nchunks > 0 && !wait_or_abort(&ctl->mma2, (nchunks - 1) & 1, ctl, err)) ok = false;
+  tc_fence_after();
+  if (ok && final_dst) {
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      uint32_t r[32];
+      tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(final_dst + qd * 32 + i) =
+            make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                        __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+    }
+  }
+}
+
+}  // namespace kda

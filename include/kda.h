@@ -82,6 +82,18 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const void* g_ra
                    int32_t H, int32_t N, int32_t D, void* out, float* final_state,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same forward pass in one kernel: each (sequence, head) CTA builds the
+ * chunk records in shared memory (the K1 arithmetic) and runs the recurrence
+ * on them (the K2 arithmetic), so the records never go through HBM and no
+ * workspace is needed.  Same arguments, results and errors as kda_fwd minus the
+ * workspace; results agree with kda_fwd to rounding (identical arithmetic in a
+ * different schedule). */
+kda_status kda_fwd_fused(const void* q, const void* k, const void* v, const void* g_raw,
+                         const void* beta_raw, float scale, float lower_bound,
+                         const float* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                         int32_t H, int32_t N, int32_t D, void* out, float* final_state,
+                         void* stream);
+
 /* Size of the fixed workspace array used by kda_fwd_noalloc (64 MiB). */
 #define KDA_NOALLOC_WORKSPACE_BYTES (64 * 1024 * 1024)
 

@@ -26,10 +26,13 @@ def _built():
     assert kda.kda_device_status() == 0
 
 
-def run(inp, **kw):
-    out, fs = kda.kda_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
-                          inp["scale"], inp["lower_bound"], inp["initial_state"],
-                          inp["cu_seqlens"], N=inp["N"], **kw)
+PATHS = ["split", "fused"]  # kda_fwd (K1 + K2) and kda_fwd_fused (one kernel)
+
+
+def run(inp, path="split", **kw):
+    fn = kda.kda_fwd if path == "split" else kda.kda_fwd_fused
+    out, fs = fn(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+                 inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"], N=inp["N"], **kw)
     assert kda.kda_device_status() == 0
     return out, fs
 
@@ -137,9 +140,10 @@ def test_chunk_records_match_oracle_factors(lengths, H):
 # whole forward pass
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("name", ["tiny", "h16"])
-def test_fwd_small_workloads_full(name):
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_small_workloads_full(name, path):
     inp = to_dev(synth.workload_inputs(name))
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, f"{name} out")
     assert_close(f64(fs), rs, f"{name} final_state")
@@ -149,27 +153,30 @@ def test_fwd_small_workloads_full(name):
     ([1], 1, False), ([15], 1, True), ([16], 3, False), ([17], 2, True), ([33], 1, False),
     ([0, 5, 0, 17, 32, 1], 2, True), ([300, 1, 47], 4, True),
 ])
-def test_fwd_edge_cases(lengths, H, init):
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_edge_cases(lengths, H, init, path):
     inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=sum(lengths) + H,
                                    init_std=0.02 if init else None))
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     ro, rs = oracle_case(inp)
     if inp["T_total"]:
         assert_close(f64(out), ro, "out")
     assert_close(f64(fs), rs, "final_state")
 
 
-def test_fwd_equal_batches_without_cu_seqlens():
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_equal_batches_without_cu_seqlens(path):
     inp = to_dev(synth.make_inputs(3 * 80, 2, 3, seed=5, init_std=0.02))
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, "out")
     assert_close(f64(fs), rs, "final_state")
 
 
-def test_fwd_empty_input_returns_initial_state():
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_empty_input_returns_initial_state(path):
     inp = to_dev(synth.make_inputs(0, 2, lengths=[0, 0], seed=1, init_std=0.02))
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     assert torch.equal(fs, inp["initial_state"])
 
 
@@ -178,15 +185,17 @@ def test_fwd_empty_input_returns_initial_state():
     ("long", [(0, 0), (0, 31)]),
     ("slow", [(0, 5)]),
 ])
-def test_fwd_full_size_sampled_units(name, units):
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_full_size_sampled_units(name, units, path):
     inp = synth.workload_inputs(name, device="cuda")
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     compare_units(inp, out, fs, units)
 
 
-def test_fwd_varlen_full_size_sampled_units():
+@pytest.mark.parametrize("path", PATHS)
+def test_fwd_varlen_full_size_sampled_units(path):
     inp = synth.workload_inputs("varlen", device="cuda")
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     cu = inp["cu_seqlens"].cpu().numpy()
     lens = np.diff(cu)
     longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
@@ -196,16 +205,18 @@ def test_fwd_varlen_full_size_sampled_units():
 # ---------------------------------------------------------------------------
 # properties
 # ---------------------------------------------------------------------------
-def test_deterministic():
+@pytest.mark.parametrize("path", PATHS)
+def test_deterministic(path):
     inp = to_dev(synth.workload_inputs("h16"))
-    o1, s1 = run(inp)
-    o2, s2 = run(inp)
+    o1, s1 = run(inp, path)
+    o2, s2 = run(inp, path)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
-def test_streaming_split_chains_state():
+@pytest.mark.parametrize("path", PATHS)
+def test_streaming_split_chains_state(path):
     inp = to_dev(synth.workload_inputs("h16"))
-    o, s = run(inp)
+    o, s = run(inp, path)
     for t1, exact in ((2048, True), (1000, False)):
         a = {k: inp[k] for k in inp}
         b = {k: inp[k] for k in inp}
@@ -213,9 +224,9 @@ def test_streaming_split_chains_state():
             a[key] = inp[key][:t1].contiguous()
             b[key] = inp[key][t1:].contiguous()
         a["T_total"], b["T_total"] = t1, inp["T_total"] - t1
-        oa, sa = run(a)
+        oa, sa = run(a, path)
         b["initial_state"] = sa
-        ob, sb = run(b)
+        ob, sb = run(b, path)
         oc = torch.cat([oa, ob])
         if exact:  # chunk-aligned split: the same chunks, bit for bit
             assert torch.equal(oc, o) and torch.equal(sb, s)
@@ -224,10 +235,11 @@ def test_streaming_split_chains_state():
             assert_close(f64(sb), f64(s), "split state")
 
 
-def test_varlen_packing_equals_separate_calls():
+@pytest.mark.parametrize("path", PATHS)
+def test_varlen_packing_equals_separate_calls(path):
     lengths = [37, 16, 100]
     inp = to_dev(synth.make_inputs(0, 2, lengths=lengths, seed=3, init_std=0.02))
-    o, s = run(inp)
+    o, s = run(inp, path)
     cu = inp["cu_seqlens"].cpu().tolist()
     for n in range(3):
         sl = slice(cu[n], cu[n + 1])
@@ -236,15 +248,16 @@ def test_varlen_packing_equals_separate_calls():
             one[key] = inp[key][sl].contiguous()
         one["initial_state"] = inp["initial_state"][n:n + 1].contiguous()
         one["cu_seqlens"], one["N"], one["T_total"] = None, 1, lengths[n]
-        on, sn = run(one)
+        on, sn = run(one, path)
         assert torch.equal(on, o[sl]) and torch.equal(sn[0], s[n])
 
 
-def test_beta_zero_is_pure_decay():
+@pytest.mark.parametrize("path", PATHS)
+def test_beta_zero_is_pure_decay(path):
     # slow decay (g_raw ~ N(-4, 1)) so that the decayed state stays in fp32 range
     inp = to_dev(synth.make_inputs(64, 2, 1, seed=9, init_std=0.02, g_mean=-4.0))
     inp["beta_raw"] = torch.full_like(inp["beta_raw"], float("-inf"))
-    out, fs = run(inp)
+    out, fs = run(inp, path)
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, "out")
     assert_close(f64(fs), rs, "final_state")
@@ -260,3 +273,12 @@ def test_host_buffer_entry_point():
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, "out")
     assert_close(f64(fs), rs, "final_state")
+
+
+def test_fused_agrees_with_split_on_b8():
+    inp = synth.workload_inputs("b8", device="cuda")
+    o1, s1 = run(inp, "split")
+    o2, s2 = run(inp, "fused")
+    assert_close(f64(o2), f64(o1), "fused vs split out")
+    assert_close(f64(s2), f64(s1), "fused vs split state")
+    print(f"[parity] fused vs split bit-identical: out {torch.equal(o1, o2)} state {torch.equal(s1, s2)}")
