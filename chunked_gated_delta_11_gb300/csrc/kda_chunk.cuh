@@ -1,8 +1,9 @@
 // kda_chunk.cuh -- the per-chunk work of the chunkwise KDA forward pass
 // ("You Could Have Come Up with Kimi Delta Attention", sec. 6.1-6.6; gates and
 // norms as in "FlashKDA Delta Attention Algorithm", Core Architecture), done
-// by one 128-thread group for one (chunk, head) and written as one record
-// (layout in kda_common.cuh).  Used by the token-parallel chunk kernel (K1).
+// by one group of 128 threads for one (chunk, head) and written as one record
+// (layout in kda_common.cuh).  Used by the chunk kernel (K1) and by the chunk
+// warps of the fused kernel.
 //
 // Steps, for the n_c <= 16 tokens i of the chunk and key channel d:
 //   beta_i = sigma(beta_raw_i)
@@ -23,43 +24,81 @@
 // remainder (three products per tile), which keeps ~16 mantissa bits; the
 // inverse runs in fp32.  W and Qdec are stored as tf32 (the recurrence reads
 // them with tf32 MMAs), U and Aqk as fp32, Kend as a bf16 high/low pair.
+//
+// Raw input tiles (q, k, v, g_raw: 16 rows of 128 bf16) live in shared memory
+// wherever the caller puts them (RawTiles), rows of 256 bytes whose 16-byte
+// pieces are XOR-swizzled by (row & 7).  The fused kernel places them in the
+// W/U area of the record stage they belong to and loads them one chunk ahead;
+// W and U are written only after every thread has finished reading them.
 #pragma once
 
 #include "kda_common.cuh"
 
 namespace kda {
 
-constexpr int TS = 136;  // bf16 row stride of the 16 x 128 tiles (272 B: no ldmatrix conflicts)
-constexpr int AS = 24;   // bf16 row stride of the 16 x 16 tiles (48 B)
+constexpr int AS = 24;  // bf16 row stride of the 16 x 16 tiles (48 B)
 
+// Per-group scratch.  Derived operand tiles are stored transposed, [128
+// channels][16 tokens] bf16 (32 B per channel), 16-byte halves swizzled by
+// bit 2 of the channel, so each thread writes its channel with two 16-byte
+// stores and ldmatrix reads are conflict-free.
 struct ChunkSmem {
-  __nv_bfloat16 q[16 * TS];    // raw q, then Qdec high
-  __nv_bfloat16 k[16 * TS];    // raw k, then Kdec high
-  __nv_bfloat16 v[16 * TS];    // raw v (exact bf16 operand of U)
-  __nv_bfloat16 g[16 * TS];    // raw g_raw, then Qdec low
-  __nv_bfloat16 kdl[16 * TS];  // Kdec low
-  __nv_bfloat16 kih[16 * TS];  // Kinv high
-  __nv_bfloat16 kil[16 * TS];  // Kinv low
-  float M[2][16][17];          // Mkk, Mqk
-  float mat[4][16][17];        // inverse workspace
+  uint8_t kdh[4096];  // Kdec high
+  uint8_t kdl[4096];  // Kdec low
+  uint8_t kih[4096];  // Kinv high
+  uint8_t kil[4096];  // Kinv low
+  uint8_t qdh[4096];  // Qdec high
+  uint8_t qdl[4096];  // Qdec low
+  float M[2][16][17];    // Mkk, Mqk
+  float mat[4][16][17];  // inverse workspace
   __nv_bfloat16 abh[16 * AS];  // A diag(beta), high
   __nv_bfloat16 abl[16 * AS];  // A diag(beta), low
   float rq[16], rk[16], beta[16];
 };
+
+// Where the four raw tiles live: rows 0-7 of tile x at lo[x], rows 8-15 at hi[x].
+struct RawTiles {
+  uint8_t* lo[4];
+  uint8_t* hi[4];
+};
+enum { RAW_Q = 0, RAW_K = 1, RAW_V = 2, RAW_G = 3 };
+
+__device__ __forceinline__ uint8_t* raw_row(const RawTiles& R, int x, int i) {
+  return (i < 8 ? R.lo[x] : R.hi[x]) + (i & 7) * 256;
+}
+// byte offset of 16-byte piece c of raw row i
+__device__ __forceinline__ int raw_piece(int i, int c) { return (c ^ (i & 7)) << 4; }
+// byte offset of (channel d, token-half p) in a derived tile
+__device__ __forceinline__ int drv_off(int d, int p) { return d * 32 + ((p ^ ((d >> 2) & 1)) << 4); }
+
+// Raw tiles placed in the W/U area of a record (the fused kernel): U^T holds
+// q and k; the W rows (first 2 KB of each 4 KB block of [W ; Qdec]) hold v, g.
+__device__ __forceinline__ RawTiles raw_tiles_in_record(uint8_t* rec) {
+  RawTiles R;
+  R.lo[RAW_Q] = rec + OFF_U;
+  R.hi[RAW_Q] = rec + OFF_U + 2048;
+  R.lo[RAW_K] = rec + OFF_U + 4096;
+  R.hi[RAW_K] = rec + OFF_U + 6144;
+  R.lo[RAW_V] = rec + OFF_B1;
+  R.hi[RAW_V] = rec + OFF_B1 + 4096;
+  R.lo[RAW_G] = rec + OFF_B1 + 8192;
+  R.hi[RAW_G] = rec + OFF_B1 + 12288;
+  return R;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(p)));
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_u32(p)));
-}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
                : "r"(smem_u32(p)));
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -76,67 +115,102 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// (x0, x1) -> packed bf16 high pair and packed bf16 remainder pair
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
                : "memory");
 }
 
-// C = P * (I + Q) or P * Q for lower-triangular 16 x 16 P, Q (fp32, smem);
-// thread t of 128 writes entries (t / 8, 2 (t % 8) + {0, 1}).
-__device__ __forceinline__ void lower_mul(const float (*P)[17], const float (*Q)[17],
-                                          float (*Cm)[17], bool plus_identity, int t) {
-  const int i = t >> 3, j0 = (t & 7) * 2;
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const int j = j0 + jj;
-    float acc = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      if (m >= j && m <= i) {
-        const float qv = Q[m][j] + ((plus_identity && m == j) ? 1.f : 0.f);
-        acc = fmaf(P[i][m], qv, acc);
-      }
-    }
-    Cm[i][j] = (j <= i) ? acc : 0.f;
-  }
+__device__ __forceinline__ float bf16_at(const uint8_t* p) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
 
 // Barrier over the 128 threads that build records (named barrier 1, so that a
 // larger CTA can run other warps beside them).
 __device__ __forceinline__ void chunk_sync() { named_bar(1, 128); }
 
-// Build the record of one chunk.  All 128 threads of the group must call it.
-// q..g point at token t0, head h of [T, H, 128] bf16 tensors (row stride
-// `row_stride` elements); beta_raw points at [t0][h] (stride H).  `rec` is the
-// record base (global or shared).  Ends with the group's shared memory free.
-__device__ __forceinline__ void build_chunk_record(
-    ChunkSmem& S, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
-    const __nv_bfloat16* __restrict__ beta_raw, int64_t row_stride, int64_t beta_stride, int nc,
-    float scale, float lb_log2e, float eps, uint8_t* __restrict__ rec, int t) {
-  const int w = t >> 5, l = t & 31;
-
-  // ---- load the four 16 x 128 tiles (rows past nc are zero) ----
-  {
-    const __nv_bfloat16* src[4] = {q, k, v, g};
-    __nv_bfloat16* dst[4] = {S.q, S.k, S.v, S.g};
+// Issue the loads of one chunk's four raw tiles (rows past nc are zeroed) as
+// one cp.async group.  q..g point at token t0, head h (row stride
+// `row_stride` elements).
+__device__ __forceinline__ void issue_raw_loads(const RawTiles& R,
+                                                const __nv_bfloat16* __restrict__ q,
+                                                const __nv_bfloat16* __restrict__ k,
+                                                const __nv_bfloat16* __restrict__ v,
+                                                const __nv_bfloat16* __restrict__ g,
+                                                int64_t row_stride, int nc, int t) {
+  const __nv_bfloat16* src[4] = {q, k, v, g};
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
+  for (int x = 0; x < 4; ++x) {
 #pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int p = t + rep * 128;
-        const int row = p >> 4, col = (p & 15) * 8;
-        __nv_bfloat16* d = dst[x] + row * TS + col;
-        if (row < nc)
-          cp_async16(d, src[x] + row * row_stride + col);
-        else
-          *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
-      }
+    for (int rep = 0; rep < 2; ++rep) {
+      const int p = t + rep * 128;
+      const int row = p >> 4, c = p & 15;
+      uint8_t* d = raw_row(R, x, row) + raw_piece(row, c);
+      if (row < nc)
+        cp_async16(d, src[x] + row * row_stride + c * 8);
+      else
+        *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
     }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Order of the 136 lower-triangle entries (i >= j) by decreasing i - j, so that
+// the threads of one warp get similar loop lengths in the triangular products.
+struct EntryTable {
+  uint8_t ij[136];
+};
+__host__ __device__ constexpr EntryTable make_entry_table() {
+  EntryTable t{};
+  int e = 0;
+  for (int dl = 15; dl >= 0; --dl)
+    for (int j = 0; j + dl < 16; ++j) t.ij[e++] = static_cast<uint8_t>(((j + dl) << 4) | j);
+  return t;
+}
+__constant__ EntryTable kEntries = make_entry_table();
+
+// One entry of C = B + X Y for lower-triangular X (zero where i - m < gx) and
+// Y (zero where m - j < gy): C[i][j] = base + sum_{m=j+gy}^{i-gx} X[i][m] Y[m][j].
+__device__ __forceinline__ void tri_entry(const float (*X)[17], const float (*Y)[17],
+                                          const float (*B)[17], float (*Cm)[17], int i, int j,
+                                          int gx, int gy) {
+  float acc = B ? B[i][j] : 0.f;
+  for (int m = j + gy; m <= i - gx; ++m) acc = fmaf(X[i][m], Y[m][j], acc);
+  Cm[i][j] = acc;
+}
+// Thread t of 128 computes entries e1 = kEntries[t] and, for t < 8, e2 =
+// kEntries[128 + t] (packed (i << 4) | j, loaded once per chunk).
+__device__ __forceinline__ void tri_product(const float (*X)[17], const float (*Y)[17],
+                                            const float (*B)[17], float (*Cm)[17], int gx,
+                                            int gy, int e1, int e2, int t) {
+  tri_entry(X, Y, B, Cm, e1 >> 4, e1 & 15, gx, gy);
+  if (t < 8) tri_entry(X, Y, B, Cm, e2 >> 4, e2 & 15, gx, gy);
+}
+
+// Build the record of one chunk from raw tiles already issued with
+// issue_raw_loads (this call waits for them).  All 128 threads of the group
+// must call it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
+// beta_raw (any value for t >= nc).  `rec` is the record base (global or
+// shared).  `after_d` runs on all threads once the raw q, k and g tiles are no
+// longer needed (the fused kernel issues the next chunk's loads there).
+template <class Hook>
+__device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles& R,
+                                                   uint32_t beta_raw_bits, int nc, float scale,
+                                                   float lb_log2e, float eps, uint8_t* rec,
+                                                   int t, Hook&& after_d) {
+  const int w = t >> 5, l = t & 31;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (t < 16) {
-    S.beta[t] = (t < nc) ? sigmoid_fast(__bfloat162float(beta_raw[t * beta_stride])) : 0.f;
+    const float br = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(beta_raw_bits)));
+    S.beta[t] = (t < nc) ? sigmoid_fast(br) : 0.f;
   }
   chunk_sync();
 
@@ -144,10 +218,13 @@ __device__ __forceinline__ void build_chunk_record(
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
     const int i = w * 4 + ii;
-    const __nv_bfloat162* qr = reinterpret_cast<const __nv_bfloat162*>(S.q + i * TS + l * 4);
-    const __nv_bfloat162* kr = reinterpret_cast<const __nv_bfloat162*>(S.k + i * TS + l * 4);
-    float2 q0 = __bfloat1622float2(qr[0]), q1 = __bfloat1622float2(qr[1]);
-    float2 k0 = __bfloat1622float2(kr[0]), k1 = __bfloat1622float2(kr[1]);
+    const int off = raw_piece(i, l >> 1) + (l & 1) * 8;
+    const uint2 qv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_Q, i) + off);
+    const uint2 kv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_K, i) + off);
+    const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
+    const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
+    const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
+    const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
     float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
     float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
 #pragma unroll
@@ -165,11 +242,14 @@ __device__ __forceinline__ void build_chunk_record(
   // ---- gates, decayed factors (thread t = key channel d) ----
   {
     const int d = t;
+    const int dp = d >> 3, db = (d & 7) * 2;
     float a[16];
+    // a = 2^(lb log2e sigma(x)), sigma(x) = 1/2 + tanh(x/2)/2
+    const float hl = 0.5f * lb_log2e;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float gv = __bfloat162float(S.g[i * TS + d]);
-      a[i] = (i < nc) ? ex2_approx(lb_log2e * sigmoid_fast(gv)) : 1.f;
+      const float gv = bf16_at(raw_row(R, RAW_G, i) + raw_piece(i, dp) + db);
+      a[i] = (i < nc) ? ex2_approx(fmaf(hl, tanh_approx(0.5f * gv), hl)) : 1.f;
     }
     float P[16], Qs[16];
     float p = 1.f;
@@ -186,63 +266,68 @@ __device__ __forceinline__ void build_chunk_record(
       Qs[i] = sfx;
       sfx *= a[i];
     }
-    uint32_t kh[8], kl[8];
+    uint32_t qh[8], ql[8], kdh[8], kdl[8], kih[8], kil[8], keh[8], kel[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float qv = __bfloat162float(S.q[i * TS + d]) * S.rq[i];
-      const float kv = __bfloat162float(S.k[i * TS + d]) * S.rk[i];
-      const float Qd = scale * qv * P[i];
-      const float Kd = kv * P[i];
-      const float Ke = kv * Qs[i];
-      const float Ki = Ke * inv_dl;
-      *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd);
-      __nv_bfloat16 hi, lo;
-      split_bf16(Qd, hi, lo);
-      S.q[i * TS + d] = hi;
-      S.g[i * TS + d] = lo;
-      split_bf16(Kd, hi, lo);
-      S.k[i * TS + d] = hi;
-      S.kdl[i * TS + d] = lo;
-      split_bf16(Ki, hi, lo);
-      S.kih[i * TS + d] = hi;
-      S.kil[i * TS + d] = lo;
-      split_bf16(Ke, hi, lo);
-      const uint32_t hb = __bfloat16_as_ushort(hi), lbits = __bfloat16_as_ushort(lo);
-      if (i & 1) {
-        kh[i >> 1] |= hb << 16;
-        kl[i >> 1] |= lbits << 16;
-      } else {
-        kh[i >> 1] = hb;
-        kl[i >> 1] = lbits;
+    for (int i2 = 0; i2 < 8; ++i2) {
+      float Qd[2], Kd[2], Ke[2], Ki[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = 2 * i2 + u;
+        const int off = raw_piece(i, dp) + db;
+        const float qv = bf16_at(raw_row(R, RAW_Q, i) + off) * S.rq[i];
+        const float kv = bf16_at(raw_row(R, RAW_K, i) + off) * S.rk[i];
+        Qd[u] = scale * qv * P[i];
+        Kd[u] = kv * P[i];
+        Ke[u] = kv * Qs[i];
+        Ki[u] = Ke[u] * inv_dl;
+        *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd[u]);
       }
+      split_pair(Qd[0], Qd[1], qh[i2], ql[i2]);
+      split_pair(Kd[0], Kd[1], kdh[i2], kdl[i2]);
+      split_pair(Ki[0], Ki[1], kih[i2], kil[i2]);
+      split_pair(Ke[0], Ke[1], keh[i2], kel[i2]);
     }
 #pragma unroll
-    for (int piece = 0; piece < 2; ++piece) {
-      const int off = kend_offset(KDA_KEND_LAYOUT, d, piece * 8);
-      *reinterpret_cast<uint4*>(rec + OFF_KH + off) =
-          make_uint4(kh[piece * 4], kh[piece * 4 + 1], kh[piece * 4 + 2], kh[piece * 4 + 3]);
-      *reinterpret_cast<uint4*>(rec + OFF_KL + off) =
-          make_uint4(kl[piece * 4], kl[piece * 4 + 1], kl[piece * 4 + 2], kl[piece * 4 + 3]);
+    for (int half = 0; half < 2; ++half) {
+      const int o = drv_off(d, half), h4 = half * 4;
+      *reinterpret_cast<uint4*>(S.qdh + o) = make_uint4(qh[h4], qh[h4 + 1], qh[h4 + 2], qh[h4 + 3]);
+      *reinterpret_cast<uint4*>(S.qdl + o) = make_uint4(ql[h4], ql[h4 + 1], ql[h4 + 2], ql[h4 + 3]);
+      *reinterpret_cast<uint4*>(S.kdh + o) =
+          make_uint4(kdh[h4], kdh[h4 + 1], kdh[h4 + 2], kdh[h4 + 3]);
+      *reinterpret_cast<uint4*>(S.kdl + o) =
+          make_uint4(kdl[h4], kdl[h4 + 1], kdl[h4 + 2], kdl[h4 + 3]);
+      *reinterpret_cast<uint4*>(S.kih + o) =
+          make_uint4(kih[h4], kih[h4 + 1], kih[h4 + 2], kih[h4 + 3]);
+      *reinterpret_cast<uint4*>(S.kil + o) =
+          make_uint4(kil[h4], kil[h4 + 1], kil[h4 + 2], kil[h4 + 3]);
+      const int ko = kend_offset(KDA_KEND_LAYOUT, d, half * 8);
+      *reinterpret_cast<uint4*>(rec + OFF_KH + ko) =
+          make_uint4(keh[h4], keh[h4 + 1], keh[h4 + 2], keh[h4 + 3]);
+      *reinterpret_cast<uint4*>(rec + OFF_KL + ko) =
+          make_uint4(kel[h4], kel[h4 + 1], kel[h4 + 2], kel[h4 + 3]);
     }
     reinterpret_cast<float*>(rec + OFF_DL)[d] = dlast;
   }
   chunk_sync();
 
-  // ---- Mkk (warps 0,1) and Mqk (warps 2,3), split-bf16 mma.sync ----
+  // ---- Mkk (warps 0,1) and Mqk (warps 2,3), split-bf16 mma.sync over 8 k-steps ----
   {
     const int mat = w >> 1, nt = w & 1;
-    const __nv_bfloat16* Ah = mat ? S.q : S.k;
-    const __nv_bfloat16* Al = mat ? S.g : S.kdl;
+    const uint8_t* Ah = mat ? S.qdh : S.kdh;
+    const uint8_t* Al = mat ? S.qdl : S.kdl;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int mi = l >> 3;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
+      const int arow = kk * 16 + (l & 7) + (mi >> 1) * 8;   // channel
+      const int aoff = drv_off(arow, mi & 1);                // token half
+      const int brow = kk * 16 + (l & 7) + ((l >> 3) & 1) * 8;
+      const int boff = drv_off(brow, nt);
       uint32_t ah[4], al[4], bh[2], bl[2];
-      const int aoff = (l & 15) * TS + kk * 16 + (l >> 4) * 8;
-      const int boff = (nt * 8 + (l & 7)) * TS + kk * 16 + ((l >> 3) & 1) * 8;
-      ldsm_x4(ah, Ah + aoff);
-      ldsm_x4(al, Al + aoff);
-      ldsm_x2(bh, S.kih + boff);
-      ldsm_x2(bl, S.kil + boff);
+      ldsm_x4_t(ah, Ah + aoff);
+      ldsm_x4_t(al, Al + aoff);
+      ldsm_x2_t(bh, S.kih + boff);
+      ldsm_x2_t(bl, S.kil + boff);
       mma16816(acc, ah, bh[0], bh[1]);
       mma16816(acc, ah, bl[0], bl[1]);
       mma16816(acc, al, bh[0], bh[1]);
@@ -267,21 +352,23 @@ __device__ __forceinline__ void build_chunk_record(
       reinterpret_cast<float*>(rec + OFF_AQK)[i * 16 + j] = (j <= i) ? S.M[1][i][j] : 0.f;
     }
   }
+  after_d();
   chunk_sync();
 
-  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) ----
-  lower_mul(S.mat[0], S.mat[0], S.mat[2], false, t);  // R^2
-  chunk_sync();
-  lower_mul(S.mat[1], S.mat[2], S.mat[3], true, t);   // (I - R)(I + R^2)
-  chunk_sync();
-  lower_mul(S.mat[2], S.mat[2], S.mat[0], false, t);  // R^4
-  chunk_sync();
-  lower_mul(S.mat[3], S.mat[0], S.mat[1], true, t);   // ... (I + R^4)
-  chunk_sync();
-  lower_mul(S.mat[0], S.mat[0], S.mat[2], false, t);  // R^8
-  chunk_sync();
-  lower_mul(S.mat[1], S.mat[2], S.mat[3], true, t);   // ... (I + R^8) = A
-  chunk_sync();
+  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent steps ----
+  {
+    const int e1 = kEntries.ij[t], e2 = t < 8 ? kEntries.ij[128 + t] : 0;
+    tri_product(S.mat[0], S.mat[0], nullptr, S.mat[2], 1, 1, e1, e2, t);  // R^2
+    chunk_sync();
+    tri_product(S.mat[1], S.mat[2], S.mat[1], S.mat[3], 0, 2, e1, e2, t);  // P1 = (I-R)(I+R^2)
+    tri_product(S.mat[2], S.mat[2], nullptr, S.mat[0], 2, 2, e1, e2, t);   // R^4
+    chunk_sync();
+    tri_product(S.mat[3], S.mat[0], S.mat[3], S.mat[1], 0, 4, e1, e2, t);  // P2 = P1 (I+R^4)
+    tri_product(S.mat[0], S.mat[0], nullptr, S.mat[2], 4, 4, e1, e2, t);   // R^8
+    chunk_sync();
+    tri_product(S.mat[1], S.mat[2], S.mat[1], S.mat[3], 0, 8, e1, e2, t);  // A = P2 (I+R^8)
+    chunk_sync();
+  }
 
   // ---- A diag(beta), split into bf16 high / low ----
   {
@@ -290,7 +377,7 @@ __device__ __forceinline__ void build_chunk_record(
     for (int jj = 0; jj < 2; ++jj) {
       const int j = j0 + jj;
       __nv_bfloat16 hi, lo;
-      split_bf16(S.mat[3][i][j] * S.beta[j], hi, lo);
+      split_bf16((j <= i) ? S.mat[3][i][j] * S.beta[j] : 0.f, hi, lo);
       S.abh[i * AS + j] = hi;
       S.abl[i * AS + j] = lo;
     }
@@ -298,41 +385,60 @@ __device__ __forceinline__ void build_chunk_record(
   chunk_sync();
 
   // ---- W = A diag(beta) Kdec, U = A diag(beta) V (warp w: channels 32w..32w+31) ----
+  float wa[4][4], ua[4][4];
   {
     uint32_t ah[4], al[4];
     const int aoff = (l & 15) * AS + (l >> 4) * 8;
     ldsm_x4(ah, S.abh + aoff);
     ldsm_x4(al, S.abl + aoff);
+    const int mi = l >> 3;
 #pragma unroll
     for (int pair = 0; pair < 2; ++pair) {
       const int n0 = w * 32 + pair * 16;
-      const int boff = ((l & 7) + ((l >> 3) & 1) * 8) * TS + n0 + (l >> 4) * 8;
+      // Kdec^T tile [d][j] is B in [n][k] order: plain ldmatrix
+      const int koff = drv_off(n0 + (l & 7) + (mi >> 1) * 8, mi & 1);
+      // raw V [j][d] is B in [k][n] order: transposed ldmatrix
+      const int vrow = (l & 7) + (mi & 1) * 8;
+      const uint8_t* vaddr = raw_row(R, RAW_V, vrow) + raw_piece(vrow, (n0 >> 3) + (mi >> 1));
       uint32_t bkh[4], bkl[4], bv[4];
-      ldsm_x4_t(bkh, S.k + boff);
-      ldsm_x4_t(bkl, S.kdl + boff);
-      ldsm_x4_t(bv, S.v + boff);
+      ldsm_x4(bkh, S.kdh + koff);
+      ldsm_x4(bkl, S.kdl + koff);
+      ldsm_x4_t(bv, vaddr);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        float wa[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
-        mma16816(wa, ah, bkh[2 * half], bkh[2 * half + 1]);
-        mma16816(wa, ah, bkl[2 * half], bkl[2 * half + 1]);
-        mma16816(wa, al, bkh[2 * half], bkh[2 * half + 1]);
-        mma16816(ua, ah, bv[2 * half], bv[2 * half + 1]);
-        mma16816(ua, al, bv[2 * half], bv[2 * half + 1]);
-        const int r0 = l >> 2, c = n0 + half * 8 + (l & 3) * 2;
-        *reinterpret_cast<float2*>(rec + b1_offset(r0, c)) =
-            make_float2(to_tf32(wa[0]), to_tf32(wa[1]));
-        *reinterpret_cast<float2*>(rec + b1_offset(r0 + 8, c)) =
-            make_float2(to_tf32(wa[2]), to_tf32(wa[3]));
-        float* U = reinterpret_cast<float*>(rec + OFF_U);
-        U[c * 16 + r0] = ua[0];
-        U[(c + 1) * 16 + r0] = ua[1];
-        U[c * 16 + r0 + 8] = ua[2];
-        U[(c + 1) * 16 + r0 + 8] = ua[3];
+        float* W4 = wa[pair * 2 + half];
+        float* U4 = ua[pair * 2 + half];
+        float wacc[4] = {0.f, 0.f, 0.f, 0.f}, uacc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(wacc, ah, bkh[2 * half], bkh[2 * half + 1]);
+        mma16816(wacc, ah, bkl[2 * half], bkl[2 * half + 1]);
+        mma16816(wacc, al, bkh[2 * half], bkh[2 * half + 1]);
+        mma16816(uacc, ah, bv[2 * half], bv[2 * half + 1]);
+        mma16816(uacc, al, bv[2 * half], bv[2 * half + 1]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          W4[e] = wacc[e];
+          U4[e] = uacc[e];
+        }
       }
     }
   }
-  chunk_sync();
+  chunk_sync();  // every read of the raw tiles is done: W and U may overwrite them
+  {
+    const int r0 = l >> 2;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int c = w * 32 + nt * 8 + (l & 3) * 2;
+      *reinterpret_cast<float2*>(rec + b1_offset(r0, c)) =
+          make_float2(to_tf32(wa[nt][0]), to_tf32(wa[nt][1]));
+      *reinterpret_cast<float2*>(rec + b1_offset(r0 + 8, c)) =
+          make_float2(to_tf32(wa[nt][2]), to_tf32(wa[nt][3]));
+      float* U = reinterpret_cast<float*>(rec + OFF_U);
+      U[c * 16 + r0] = ua[nt][0];
+      U[(c + 1) * 16 + r0] = ua[nt][1];
+      U[c * 16 + r0 + 8] = ua[nt][2];
+      U[(c + 1) * 16 + r0 + 8] = ua[nt][3];
+    }
+  }
 }
 
 // Locate record slot `slot`: the sequence n with slot0(n) <= slot < slot0(n+1)

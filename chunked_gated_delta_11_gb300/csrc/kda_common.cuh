@@ -69,6 +69,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// First 1024-byte-aligned byte of a dynamic shared-memory buffer.  Pointer
+// arithmetic on the __shared__ array itself (no round trip through an integer)
+// keeps the shared address space visible to the compiler.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -51,8 +51,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
              int* __restrict__ err) {
   constexpr int NST = F_NST;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   ChunkSmem& CS = *reinterpret_cast<ChunkSmem*>(smem + F_CHUNK_OFF);
   auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + F_CTL_OFF);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
@@ -91,21 +90,51 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 
   if (w >= 5) {
     // ---------------- chunk threads ----------------
+    // The raw tiles of chunk c are loaded into stage c % 2 while chunk c - 1 is
+    // being built, so their latency hides behind that work.
     const int tc = t - 160;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+    auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
+      t0 = bos + static_cast<int64_t>(c) * kChunk;
+      nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
+    };
+    auto issue = [&](int c, int s) -> uint32_t {
+      int64_t t0;
+      int nc;
+      chunk_geom(c, t0, nc);
+      const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
+      issue_raw_loads(raw_tiles_in_record(smem + s * REC_STRIDE_SMEM), q + base, k + base,
+                      v + base, g + base, row_stride, nc, tc);
+      return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
+    };
+    uint32_t bbits = nchunks > 0 ? issue(0, 0) : 0u;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
-      bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
-      ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
-      if (!chunk_all(ok)) break;
-      const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
-      const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      build_chunk_record(CS, q + base, k + base, v + base, g + base, beta_raw + t0 * H + h,
-                         row_stride, H, nc, scale, lb_log2e, eps, smem + s * REC_STRIDE_SMEM, tc);
+      uint32_t next_bits = 0u;
+      bool stop = false;
+      auto prefetch = [&] {
+        if (c + 1 >= nchunks) return;
+        const int s1 = (c + 1) % NST;
+        bool ok = c + 1 < NST ||
+                  wait_or_abort(&ctl->empty[s1], (((c + 1) / NST) - 1) & 1, ctl, err);
+        ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
+        if (chunk_all(ok))
+          next_bits = issue(c + 1, s1);
+        else
+          stop = true;
+      };
+      int64_t t0;
+      int nc;
+      chunk_geom(c, t0, nc);
+      uint8_t* rec = smem + s * REC_STRIDE_SMEM;
+      build_chunk_record(CS, raw_tiles_in_record(rec), bbits, nc, scale, lb_log2e, eps, rec, tc,
+                         prefetch);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&ctl->full[s]);
+      if (stop) break;
+      bbits = next_bits;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else if (w == 4) {
     if (l == 0) {
       int mma_chunks = 0;

@@ -8,6 +8,11 @@
 
 namespace kda {
 
+struct PrepSmem {
+  ChunkSmem chunk;
+  uint8_t raw[4 * 4096];  // q, k, v, g_raw tiles of the current chunk
+};
+
 __global__ void __launch_bounds__(128, 4)
 chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
@@ -15,7 +20,13 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   float eps, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
                   uint8_t* __restrict__ ws, int64_t n_items) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  ChunkSmem& S = *reinterpret_cast<ChunkSmem*>(smem_raw);
+  PrepSmem& P = *reinterpret_cast<PrepSmem*>(smem_raw);
+  RawTiles R;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    R.lo[x] = P.raw + x * 4096;
+    R.hi[x] = P.raw + x * 4096 + 2048;
+  }
   const int t = threadIdx.x;
   const int64_t row_stride = static_cast<int64_t>(H) * kDim;
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -27,9 +38,11 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int64_t t0 = bos + c * kChunk;
     const int nc = static_cast<int>(((eos - t0) < kChunk ? (eos - t0) : kChunk));
     const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-    build_chunk_record(S, q + base, k + base, v + base, g + base, beta_raw + t0 * H + h,
-                       row_stride, H, nc, scale, lb_log2e, eps,
-                       ws + static_cast<int64_t>(item) * REC_BYTES, t);
+    issue_raw_loads(R, q + base, k + base, v + base, g + base, row_stride, nc, t);
+    const uint32_t bbits =
+        (t < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + t) * H + h]) : 0u;
+    build_chunk_record(P.chunk, R, bbits, nc, scale, lb_log2e, eps,
+                       ws + static_cast<int64_t>(item) * REC_BYTES, t, [] {});
   }
 }
 
@@ -38,7 +51,7 @@ cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const
                               const int32_t* cu, int64_t T_total, int H, int N, void* ws,
                               int sm_count, cudaStream_t stream) {
   const int64_t n_items = slot_count(T_total, N) * H;
-  const int smem = static_cast<int>(sizeof(ChunkSmem));
+  const int smem = static_cast<int>(sizeof(PrepSmem));
   static bool attr_done = false;  // per process; the attribute is per function
   if (!attr_done) {
     cudaError_t e =

@@ -23,8 +23,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
                   int* __restrict__ err) {
   constexpr int NST = K2_NST;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + NST * REC_STRIDE_SMEM);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int unit = blockIdx.x;

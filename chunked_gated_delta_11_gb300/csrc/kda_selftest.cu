@@ -25,8 +25,7 @@ __global__ void __launch_bounds__(128, 1)
 selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int kend_layout,
                         int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   uint8_t* b1 = smem;                       // 16 KB, record OFF_B1 layout
   uint8_t* b2 = smem + 16384;               // 4 KB, Kend layout
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 20480);
