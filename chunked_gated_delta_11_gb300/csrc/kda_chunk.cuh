@@ -23,7 +23,7 @@
 // accumulate) with each fp32 operand split into a bf16 high part and a bf16
 // remainder (three products per tile), which keeps ~16 mantissa bits; the
 // inverse runs in fp32.  W and Qdec are stored as tf32 (the recurrence reads
-// them with tf32 MMAs), U and Aqk as fp32, Kend as a bf16 high/low pair.
+// them with tf32 MMAs), U as fp32, Kend and Aqk as bf16 high/low pairs.
 //
 // Raw input tiles (q, k, v, g_raw: 16 rows of 128 bf16) live in shared memory
 // wherever the caller puts them (RawTiles), rows of 256 bytes whose 16-byte
@@ -113,15 +113,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-}
-
-// (x0, x1) -> packed bf16 high pair and packed bf16 remainder pair
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -282,10 +273,10 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
         Ki[u] = Ke[u] * inv_dl;
         *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd[u]);
       }
-      split_pair(Qd[0], Qd[1], qh[i2], ql[i2]);
-      split_pair(Kd[0], Kd[1], kdh[i2], kdl[i2]);
-      split_pair(Ki[0], Ki[1], kih[i2], kil[i2]);
-      split_pair(Ke[0], Ke[1], keh[i2], kel[i2]);
+      split_pair2(Qd[0], Qd[1], qh[i2], ql[i2]);
+      split_pair2(Kd[0], Kd[1], kdh[i2], kdl[i2]);
+      split_pair2(Ki[0], Ki[1], kih[i2], kil[i2]);
+      split_pair2(Ke[0], Ke[1], keh[i2], kel[i2]);
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -349,7 +340,10 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       const float r = (j < i) ? S.beta[i] * S.M[0][i][j] : 0.f;
       S.mat[0][i][j] = r;
       S.mat[1][i][j] = ((i == j) ? 1.f : 0.f) - r;
-      reinterpret_cast<float*>(rec + OFF_AQK)[i * 16 + j] = (j <= i) ? S.M[1][i][j] : 0.f;
+      __nv_bfloat16 ah, al;
+      split_bf16((j <= i) ? S.M[1][i][j] : 0.f, ah, al);
+      *reinterpret_cast<__nv_bfloat16*>(rec + OFF_AQK + aqk_offset(i, j)) = ah;
+      *reinterpret_cast<__nv_bfloat16*>(rec + OFF_AQK + 512 + aqk_offset(i, j)) = al;
     }
   }
   after_d();

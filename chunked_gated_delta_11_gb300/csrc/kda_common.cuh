@@ -19,7 +19,10 @@
 //   [OFF_KH,  +4096)   Kend high part (bf16), MMA operand indexed [d][j]:
 //   [OFF_KL,  +4096)   Kend low part (bf16) = bf16(Kend - high); same layout.
 //   [OFF_U,   +8192)   U^T fp32 [128 value channels][16 tokens].
-//   [OFF_AQK, +1024)   Aqk fp32 [16][16] (chi_ij for j <= i, zero above).
+//   [OFF_AQK, +512)    Aqk high part (bf16) [16 rows i][16 j] (chi_ij for j <= i,
+//                      zero above), K-major with the 32-byte swizzle: row i at
+//                      i*32, 16-byte piece p at (p ^ ((i >> 2) & 1))*16.
+//   [OFF_AQK+512,+512) Aqk low part (bf16) = bf16(Aqk - high); same layout.
 //   [OFF_DL,  +512)    dlast fp32 [128] = diagonal of D_{0:C-1}.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
@@ -54,6 +57,11 @@ __host__ __device__ constexpr int b1_offset(int n, int d) {
   // fp32 element (row n, channel d) of the [W ; Qdec] tile
   return OFF_B1 + (d >> 5) * 4096 + n * 128 + ((((d & 31) >> 2) ^ (n & 7)) << 4) +
          ((d & 3) << 2);
+}
+
+__host__ __device__ constexpr int aqk_offset(int i, int j) {
+  // byte offset of bf16 element (i, j) inside one 512-byte Aqk tile
+  return i * 32 + ((((j >> 3) ^ (i >> 2)) & 1) << 4) + ((j & 7) << 1);
 }
 
 __host__ __device__ constexpr int kend_offset(int layout, int d, int j) {
@@ -109,6 +117,15 @@ __device__ __forceinline__ float to_tf32(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// (x0, x1) -> packed bf16 pair of high parts and packed pair of remainders
+__device__ __forceinline__ void split_pair2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // ---------------------------------------------------------------------------
@@ -280,6 +297,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -4,7 +4,7 @@
 // kernel (records built in shared memory by the same CTA).
 //
 // One CTA owns one (sequence, head) unit.  Its 128 x 128 fp32 state S lives in
-// tensor memory, row v in lane v.  For each chunk record (kda_common.cuh):
+// tensor memory, row v in lane v.  For each chunk record c (kda_common.cuh):
 //
 //   MMA1 (tcgen05 kind::tf32, M=128 N=32 K=128, issued by one thread):
 //        D1[v][n] = sum_d S[v][d] B1[n][d],  B1 = [W ; Qdec]
@@ -15,13 +15,16 @@
 //        E^T -> tensor memory as bf16 high part + bf16 remainder
 //   MMA2 (tcgen05 kind::f16 bf16, M=128 N=128 K=16, three instructions):
 //        S += E^T_hi Kend_hi + E^T_lo Kend_hi + E^T_hi Kend_lo   (write, sec. 6.4)
-//   state threads, overlapping MMA2 and the next MMA1:
-//        o[i][v] = D1[v][16+i] + sum_{j<=i} Aqk[i][j] e[v][j]      (read, sec. 6.5)
+//   MMA3 (kind::f16 bf16, M=128 N=16 K=16, three instructions):
+//        D1[v][16+i] += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v]     (read, sec. 6.5)
+//   state threads, while MMA1 of chunk c+1 runs: o -> bf16 -> out.
 //
 // MMA1 takes the fp32 state as its A operand directly (the tensor core reads its
-// tf32 part), so no operand copy of S is kept.  Barriers per CTA (mbarriers):
-// full[s] (record s ready), empty[s] (record s consumed: 128 state threads + one
-// MMA commit), mma1/mma2 (MMA completion), eready (128 state threads wrote E^T).
+// tf32 part), so no operand copy of S is kept.  D1 alternates between two
+// tensor-memory buffers so that chunk c's outputs can be read while MMA1 of
+// chunk c+1 writes the other one.  Barriers per CTA (mbarriers): full[s]
+// (record s ready), empty[s] (record s consumed: 128 state threads + one MMA
+// commit), mma1/mma2 (MMA completion), eready (128 state threads wrote E^T).
 // Every wait is bounded; a timeout sets the CTA's abort flag and the error word.
 #pragma once
 
@@ -29,7 +32,9 @@
 
 namespace kda {
 
-constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_A2H = 160, TM_A2L = 168, TM_COLS = 256;
+constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_A2H = 192, TM_A2L = 200, TM_COLS = 256;
+// D1 of chunk c: columns TM_D1 + 32 * (c & 1) .. + 31
+__device__ __forceinline__ uint32_t d1_col(int c) { return TM_D1 + 32u * static_cast<uint32_t>(c & 1); }
 
 template <int NST>
 struct StateCtl {
@@ -83,19 +88,21 @@ __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
   tmem_wait_st();
 }
 
-// MMA1 and MMA2 of chunk c on the record at shared address `sb` (issuing thread
-// only).  Returns false if a wait gave up.
+// MMA1, MMA2 and MMA3 of chunk c on the record at shared address `sb`
+// (issuing thread only).  Returns false if a wait gave up.
 template <int NST>
 __device__ __forceinline__ bool issue_chunk_mmas(StateCtl<NST>* ctl, int c, int s, uint32_t sb,
                                                  uint32_t tb, int* err) {
-  const uint32_t id1 = make_idesc(2, 128, 32), id2 = make_idesc(1, 128, 128);
+  const uint32_t id1 = make_idesc(2, 128, 32), id2 = make_idesc(1, 128, 128),
+                 id3 = make_idesc(1, 128, 16);
+  const uint32_t d1 = tb + d1_col(c);
   if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) return false;
   if (c > 0 && !wait_or_abort(&ctl->mma2, (c - 1) & 1, ctl, err)) return false;
   tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
-    mma_tf32_ts(tb + TM_D1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+    mma_tf32_ts(d1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
   }
   tc_commit(&ctl->mma1);
   if (!wait_or_abort(&ctl->eready, c & 1, ctl, err)) return false;
@@ -104,6 +111,11 @@ __device__ __forceinline__ bool issue_chunk_mmas(StateCtl<NST>* ctl, int c, int 
   mma_bf16_ts(tb + TM_S, tb + TM_A2H, kh, id2, 1u);
   mma_bf16_ts(tb + TM_S, tb + TM_A2L, kh, id2, 1u);
   mma_bf16_ts(tb + TM_S, tb + TM_A2H, kl, id2, 1u);
+  const uint64_t ah = make_sdesc(sb + OFF_AQK, 16, 256, 6),
+                 al = make_sdesc(sb + OFF_AQK + 512, 16, 256, 6);
+  mma_bf16_ts(d1 + 16, tb + TM_A2H, ah, id3, 1u);
+  mma_bf16_ts(d1 + 16, tb + TM_A2L, ah, id3, 1u);
+  mma_bf16_ts(d1 + 16, tb + TM_A2H, al, id3, 1u);
   tc_commit(&ctl->mma2);
   tc_commit(&ctl->empty[s]);
   return true;
@@ -124,66 +136,66 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, const uint8_t* ri
     if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) { ok = false; break; }
     if (!wait_or_abort(&ctl->mma1, c & 1, ctl, err)) { ok = false; break; }
     tc_fence_after();
-    // forget: S[v][:] *= dlast (MMA1 has finished reading S)
+    // forget: S[v][:] *= dlast (MMA1 has finished reading S); two 32-column
+    // loads are in flight per wait
     const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
 #pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      uint32_t r[32];
-      tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+    for (int hq = 0; hq < 2; ++hq) {
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tb + TM_S + lane_off + hq * 64, ra);
+      tmem_ld32(tb + TM_S + lane_off + hq * 64 + 32, rb);
       tmem_wait_ld();
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 dv = dl4[qd * 8 + i4];
-        r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
-        r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
-        r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
-        r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
+        const float4 da = dl4[hq * 16 + i4];
+        const float4 db = dl4[hq * 16 + 8 + i4];
+        ra[4 * i4 + 0] = __float_as_uint(__uint_as_float(ra[4 * i4 + 0]) * da.x);
+        ra[4 * i4 + 1] = __float_as_uint(__uint_as_float(ra[4 * i4 + 1]) * da.y);
+        ra[4 * i4 + 2] = __float_as_uint(__uint_as_float(ra[4 * i4 + 2]) * da.z);
+        ra[4 * i4 + 3] = __float_as_uint(__uint_as_float(ra[4 * i4 + 3]) * da.w);
+        rb[4 * i4 + 0] = __float_as_uint(__uint_as_float(rb[4 * i4 + 0]) * db.x);
+        rb[4 * i4 + 1] = __float_as_uint(__uint_as_float(rb[4 * i4 + 1]) * db.y);
+        rb[4 * i4 + 2] = __float_as_uint(__uint_as_float(rb[4 * i4 + 2]) * db.z);
+        rb[4 * i4 + 3] = __float_as_uint(__uint_as_float(rb[4 * i4 + 3]) * db.w);
       }
-      tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+      tmem_st32(tb + TM_S + lane_off + hq * 64, ra);
+      tmem_st32(tb + TM_S + lane_off + hq * 64 + 32, rb);
     }
-    uint32_t d1[32];
-    tmem_ld32(tb + TM_D1 + lane_off, d1);
+    uint32_t d1[16];
+    tmem_ld16(tb + d1_col(c) + lane_off, d1);
     tmem_wait_ld();
     // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v]
     const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
-    float e[16];
-#pragma unroll
-    for (int i4 = 0; i4 < 4; ++i4) {
-      const float4 u = U4[i4];
-      e[i4 * 4 + 0] = u.x - __uint_as_float(d1[i4 * 4 + 0]);
-      e[i4 * 4 + 1] = u.y - __uint_as_float(d1[i4 * 4 + 1]);
-      e[i4 * 4 + 2] = u.z - __uint_as_float(d1[i4 * 4 + 2]);
-      e[i4 * 4 + 3] = u.w - __uint_as_float(d1[i4 * 4 + 3]);
-    }
     {
       uint32_t pk[16];
 #pragma unroll
-      for (int c2 = 0; c2 < 8; ++c2) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(e[2 * c2]);
-        const __nv_bfloat16 h1 = __float2bfloat16_rn(e[2 * c2 + 1]);
-        pk[c2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                 (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-        pk[8 + c2] =
-            pack_bf16(e[2 * c2] - __bfloat162float(h0), e[2 * c2 + 1] - __bfloat162float(h1));
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 u = U4[i4];
+        const float e0 = u.x - __uint_as_float(d1[i4 * 4 + 0]);
+        const float e1 = u.y - __uint_as_float(d1[i4 * 4 + 1]);
+        const float e2 = u.z - __uint_as_float(d1[i4 * 4 + 2]);
+        const float e3 = u.w - __uint_as_float(d1[i4 * 4 + 3]);
+        split_pair2(e0, e1, pk[2 * i4], pk[8 + 2 * i4]);
+        split_pair2(e2, e3, pk[2 * i4 + 1], pk[8 + 2 * i4 + 1]);
       }
       tmem_st16(tb + TM_A2H + lane_off, pk);
     }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&ctl->eready);
-    // outputs o[i][v] = (Qdec S^T)[i][v] + sum_{j <= i} Aqk[i][j] e[v][j]
-    const float* Aq = reinterpret_cast<const float*>(st + OFF_AQK);
+    mbar_arrive(&ctl->empty[s]);  // U and dlast are read; the MMAs hold the rest
+    // outputs: D1[v][16 + i] = o[i][v] once MMA2/MMA3 of this chunk are done
+    if (!wait_or_abort(&ctl->mma2, c & 1, ctl, err)) { ok = false; break; }
+    tc_fence_after();
+    uint32_t o[16];
+    tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
+    tmem_wait_ld();
     const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
     const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
     __nv_bfloat16* orow = out + (t0 * H + h) * kDim + v;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float o = __uint_as_float(d1[16 + i]);
-#pragma unroll
-      for (int j = 0; j <= i; ++j) o = fmaf(Aq[i * 16 + j], e[j], o);
-      if (i < nc) orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(o);
-    }
-    mbar_arrive(&ctl->empty[s]);
+    for (int i = 0; i < 16; ++i)
+      if (i < nc) orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
   }
   if (ok && nchunks > 0 && !wait_or_abort(&ctl->mma2, (nchunks - 1) & 1, ctl, err)) ok = false;
   tc_fence_after();

@@ -97,7 +97,14 @@ def decode_record(rec):
 
     kend = bf16_at(16384) + bf16_at(20480)
     U = rec[24576:32768].view(np.float32).reshape(128, 16).T
-    Aqk = rec[32768:33792].view(np.float32).reshape(16, 16)
+    ii, jj2 = np.meshgrid(np.arange(16), np.arange(16), indexing="ij")
+    aoff = ii * 32 + ((((jj2 >> 3) ^ (ii >> 2)) & 1) << 4) + ((jj2 & 7) << 1)
+
+    def aqk_at(base):
+        raw = rec[base:base + 512].view(np.uint16)[aoff // 2].astype(np.uint32) << 16
+        return raw.view(np.float32).astype(np.float64)
+
+    Aqk = aqk_at(32768) + aqk_at(33280)
     dl = rec[33792:34304].view(np.float32)
     return {"W": b1[:16], "Qdec": b1[16:], "Kend": kend, "U": U, "Aqk": Aqk, "dlast": dl}
 
