@@ -50,7 +50,15 @@ struct ChunkSmem {
   uint8_t qdh[4096];  // Qdec high
   uint8_t qdl[4096];  // Qdec low
   float M[2][16][17];    // Mkk, Mqk
-  float mat[4][16][17];  // inverse workspace
+  // inverse workspace, rows of 20 floats (16-byte aligned, conflict-free):
+  // row-major copies (X role) and transposed copies (Y role) of the factors
+  float Rr[16][20];   // R, later R^4 (rows)
+  float RT[16][20];   // R^T, later (R^8)^T
+  float R2r[16][20];  // R^2 (rows)
+  float R2T[16][20];  // (R^2)^T
+  float R4T[16][20];  // (R^4)^T
+  float P0[16][20];   // I - R, later P2 = (I-R)(I+R^2)(I+R^4)
+  float P1[16][20];   // P1 = (I-R)(I+R^2), later A = P2 (I+R^8)
   __nv_bfloat16 abh[16 * AS];  // A diag(beta), high
   __nv_bfloat16 abl[16 * AS];  // A diag(beta), low
   float rq[16], rk[16], beta[16];
@@ -168,22 +176,47 @@ __host__ __device__ constexpr EntryTable make_entry_table() {
 }
 __constant__ EntryTable kEntries = make_entry_table();
 
-// One entry of C = B + X Y for lower-triangular X (zero where i - m < gx) and
-// Y (zero where m - j < gy): C[i][j] = base + sum_{m=j+gy}^{i-gx} X[i][m] Y[m][j].
-__device__ __forceinline__ void tri_entry(const float (*X)[17], const float (*Y)[17],
-                                          const float (*B)[17], float (*Cm)[17], int i, int j,
-                                          int gx, int gy) {
-  float acc = B ? B[i][j] : 0.f;
-  for (int m = j + gy; m <= i - gx; ++m) acc = fmaf(X[i][m], Y[m][j], acc);
-  Cm[i][j] = acc;
+// Entry (i, j), i >= j, of C = B + X Y for 16 x 16 lower-triangular X, Y whose
+// never-written triangles hold zeros: a dense 16-term dot product of row i of
+// X with column j of Y (read as row j of Y^T), all loads issued up front.
+// Writes C[i][j] and, if CT, CT[j][i].
+__device__ __forceinline__ void tri_entry(const float (*X)[20], const float (*YT)[20],
+                                          const float (*B)[20], float (*Cm)[20], float (*CT)[20],
+                                          int i, int j) {
+  const float4* xr = reinterpret_cast<const float4*>(X[i]);
+  const float4* yr = reinterpret_cast<const float4*>(YT[j]);
+  float4 x[4], y[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    x[q] = xr[q];
+    y[q] = yr[q];
+  }
+  float a0 = B ? B[i][j] : 0.f, a1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    a0 = fmaf(x[q].x, y[q].x, a0);
+    a1 = fmaf(x[q].y, y[q].y, a1);
+    a0 = fmaf(x[q].z, y[q].z, a0);
+    a1 = fmaf(x[q].w, y[q].w, a1);
+  }
+  const float c = a0 + a1;
+  Cm[i][j] = c;
+  if (CT) CT[j][i] = c;
 }
 // Thread t of 128 computes entries e1 = kEntries[t] and, for t < 8, e2 =
 // kEntries[128 + t] (packed (i << 4) | j, loaded once per chunk).
-__device__ __forceinline__ void tri_product(const float (*X)[17], const float (*Y)[17],
-                                            const float (*B)[17], float (*Cm)[17], int gx,
-                                            int gy, int e1, int e2, int t) {
-  tri_entry(X, Y, B, Cm, e1 >> 4, e1 & 15, gx, gy);
-  if (t < 8) tri_entry(X, Y, B, Cm, e2 >> 4, e2 & 15, gx, gy);
+__device__ __forceinline__ void tri_product(const float (*X)[20], const float (*YT)[20],
+                                            const float (*B)[20], float (*Cm)[20],
+                                            float (*CT)[20], int e1, int e2, int t) {
+  tri_entry(X, YT, B, Cm, CT, e1 >> 4, e1 & 15);
+  if (t < 8) tri_entry(X, YT, B, Cm, CT, e2 >> 4, e2 & 15);
+}
+
+// Zero the inverse workspace once (its unwritten triangles must stay zero).
+__device__ __forceinline__ void clear_inverse_workspace(ChunkSmem& S, int t) {
+  float* p = &S.Rr[0][0];
+  const int n = static_cast<int>(7 * 16 * 20);
+  for (int e = t; e < n; e += 128) p[e] = 0.f;
 }
 
 // Build the record of one chunk from raw tiles already issued with
@@ -231,6 +264,8 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
   chunk_sync();
 
   // ---- gates, decayed factors (thread t = key channel d) ----
+  // forward pass: prefix products P_i -> Qdec, Kdec; backward pass: suffix
+  // products Q_i -> Kend, Kinv.  Eight tokens are packed and stored at a time.
   {
     const int d = t;
     const int dp = d >> 3, db = (d & 7) * 2;
@@ -242,62 +277,61 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       const float gv = bf16_at(raw_row(R, RAW_G, i) + raw_piece(i, dp) + db);
       a[i] = (i < nc) ? ex2_approx(fmaf(hl, tanh_approx(0.5f * gv), hl)) : 1.f;
     }
-    float P[16], Qs[16];
     float p = 1.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      p *= a[i];
-      P[i] = p;
+    for (int half = 0; half < 2; ++half) {
+      uint32_t qh[4], ql[4], kh[4], kl[4];
+#pragma unroll
+      for (int i2 = 0; i2 < 4; ++i2) {
+        float Qd[2], Kd[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = half * 8 + i2 * 2 + u;
+          const int off = raw_piece(i, dp) + db;
+          p *= a[i];
+          const float qv = bf16_at(raw_row(R, RAW_Q, i) + off) * S.rq[i];
+          const float kv = bf16_at(raw_row(R, RAW_K, i) + off) * S.rk[i];
+          Qd[u] = scale * qv * p;
+          Kd[u] = kv * p;
+          *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd[u]);
+        }
+        split_pair2(Qd[0], Qd[1], qh[i2], ql[i2]);
+        split_pair2(Kd[0], Kd[1], kh[i2], kl[i2]);
+      }
+      const int o = drv_off(d, half);
+      *reinterpret_cast<uint4*>(S.qdh + o) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+      *reinterpret_cast<uint4*>(S.qdl + o) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+      *reinterpret_cast<uint4*>(S.kdh + o) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+      *reinterpret_cast<uint4*>(S.kdl + o) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
     }
     const float dlast = p;
     const float inv_dl = rcp_approx(dlast);
-    float sfx = 1.f;
-#pragma unroll
-    for (int i = 15; i >= 0; --i) {
-      Qs[i] = sfx;
-      sfx *= a[i];
-    }
-    uint32_t qh[8], ql[8], kdh[8], kdl[8], kih[8], kil[8], keh[8], kel[8];
-#pragma unroll
-    for (int i2 = 0; i2 < 8; ++i2) {
-      float Qd[2], Kd[2], Ke[2], Ki[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = 2 * i2 + u;
-        const int off = raw_piece(i, dp) + db;
-        const float qv = bf16_at(raw_row(R, RAW_Q, i) + off) * S.rq[i];
-        const float kv = bf16_at(raw_row(R, RAW_K, i) + off) * S.rk[i];
-        Qd[u] = scale * qv * P[i];
-        Kd[u] = kv * P[i];
-        Ke[u] = kv * Qs[i];
-        Ki[u] = Ke[u] * inv_dl;
-        *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd[u]);
-      }
-      split_pair2(Qd[0], Qd[1], qh[i2], ql[i2]);
-      split_pair2(Kd[0], Kd[1], kdh[i2], kdl[i2]);
-      split_pair2(Ki[0], Ki[1], kih[i2], kil[i2]);
-      split_pair2(Ke[0], Ke[1], keh[i2], kel[i2]);
-    }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int o = drv_off(d, half), h4 = half * 4;
-      *reinterpret_cast<uint4*>(S.qdh + o) = make_uint4(qh[h4], qh[h4 + 1], qh[h4 + 2], qh[h4 + 3]);
-      *reinterpret_cast<uint4*>(S.qdl + o) = make_uint4(ql[h4], ql[h4 + 1], ql[h4 + 2], ql[h4 + 3]);
-      *reinterpret_cast<uint4*>(S.kdh + o) =
-          make_uint4(kdh[h4], kdh[h4 + 1], kdh[h4 + 2], kdh[h4 + 3]);
-      *reinterpret_cast<uint4*>(S.kdl + o) =
-          make_uint4(kdl[h4], kdl[h4 + 1], kdl[h4 + 2], kdl[h4 + 3]);
-      *reinterpret_cast<uint4*>(S.kih + o) =
-          make_uint4(kih[h4], kih[h4 + 1], kih[h4 + 2], kih[h4 + 3]);
-      *reinterpret_cast<uint4*>(S.kil + o) =
-          make_uint4(kil[h4], kil[h4 + 1], kil[h4 + 2], kil[h4 + 3]);
-      const int ko = kend_offset(KDA_KEND_LAYOUT, d, half * 8);
-      *reinterpret_cast<uint4*>(rec + OFF_KH + ko) =
-          make_uint4(keh[h4], keh[h4 + 1], keh[h4 + 2], keh[h4 + 3]);
-      *reinterpret_cast<uint4*>(rec + OFF_KL + ko) =
-          make_uint4(kel[h4], kel[h4 + 1], kel[h4 + 2], kel[h4 + 3]);
-    }
     reinterpret_cast<float*>(rec + OFF_DL)[d] = dlast;
+    float sfx = 1.f;  // prod_{m > i} a_m while token i is processed
+#pragma unroll
+    for (int half = 1; half >= 0; --half) {
+      uint32_t eh[4], el[4], ih[4], il[4];
+#pragma unroll
+      for (int i2 = 3; i2 >= 0; --i2) {
+        float Ke[2], Ki[2];
+#pragma unroll
+        for (int u = 1; u >= 0; --u) {
+          const int i = half * 8 + i2 * 2 + u;
+          const float kv = bf16_at(raw_row(R, RAW_K, i) + raw_piece(i, dp) + db) * S.rk[i];
+          Ke[u] = kv * sfx;
+          Ki[u] = Ke[u] * inv_dl;
+          sfx *= a[i];
+        }
+        split_pair2(Ke[0], Ke[1], eh[i2], el[i2]);
+        split_pair2(Ki[0], Ki[1], ih[i2], il[i2]);
+      }
+      const int o = drv_off(d, half);
+      *reinterpret_cast<uint4*>(S.kih + o) = make_uint4(ih[0], ih[1], ih[2], ih[3]);
+      *reinterpret_cast<uint4*>(S.kil + o) = make_uint4(il[0], il[1], il[2], il[3]);
+      const int ko = kend_offset(KDA_KEND_LAYOUT, d, half * 8);
+      *reinterpret_cast<uint4*>(rec + OFF_KH + ko) = make_uint4(eh[0], eh[1], eh[2], eh[3]);
+      *reinterpret_cast<uint4*>(rec + OFF_KL + ko) = make_uint4(el[0], el[1], el[2], el[3]);
+    }
   }
   chunk_sync();
 
@@ -306,7 +340,9 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
     const int mat = w >> 1, nt = w & 1;
     const uint8_t* Ah = mat ? S.qdh : S.kdh;
     const uint8_t* Al = mat ? S.qdl : S.kdl;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // three independent accumulator chains (high*high, high*low, low*high)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f},
+          acc2[4] = {0.f, 0.f, 0.f, 0.f};
     const int mi = l >> 3;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -320,9 +356,11 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       ldsm_x2_t(bh, S.kih + boff);
       ldsm_x2_t(bl, S.kil + boff);
       mma16816(acc, ah, bh[0], bh[1]);
-      mma16816(acc, ah, bl[0], bl[1]);
-      mma16816(acc, al, bh[0], bh[1]);
+      mma16816(acc1, ah, bl[0], bl[1]);
+      mma16816(acc2, al, bh[0], bh[1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] += acc1[e] + acc2[e];
     const int r0 = l >> 2, c0 = nt * 8 + (l & 3) * 2;
     S.M[mat][r0][c0] = acc[0];
     S.M[mat][r0][c0 + 1] = acc[1];
@@ -338,8 +376,9 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
     for (int jj = 0; jj < 2; ++jj) {
       const int j = j0 + jj;
       const float r = (j < i) ? S.beta[i] * S.M[0][i][j] : 0.f;
-      S.mat[0][i][j] = r;
-      S.mat[1][i][j] = ((i == j) ? 1.f : 0.f) - r;
+      S.Rr[i][j] = r;
+      S.RT[j][i] = r;
+      S.P0[i][j] = ((i == j) ? 1.f : 0.f) - r;
       __nv_bfloat16 ah, al;
       split_bf16((j <= i) ? S.M[1][i][j] : 0.f, ah, al);
       *reinterpret_cast<__nv_bfloat16*>(rec + OFF_AQK + aqk_offset(i, j)) = ah;
@@ -352,15 +391,15 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
   // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent steps ----
   {
     const int e1 = kEntries.ij[t], e2 = t < 8 ? kEntries.ij[128 + t] : 0;
-    tri_product(S.mat[0], S.mat[0], nullptr, S.mat[2], 1, 1, e1, e2, t);  // R^2
+    tri_product(S.Rr, S.RT, nullptr, S.R2r, S.R2T, e1, e2, t);   // R^2
     chunk_sync();
-    tri_product(S.mat[1], S.mat[2], S.mat[1], S.mat[3], 0, 2, e1, e2, t);  // P1 = (I-R)(I+R^2)
-    tri_product(S.mat[2], S.mat[2], nullptr, S.mat[0], 2, 2, e1, e2, t);   // R^4
+    tri_product(S.P0, S.R2T, S.P0, S.P1, nullptr, e1, e2, t);    // P1 = (I-R)(I+R^2)
+    tri_product(S.R2r, S.R2T, nullptr, S.Rr, S.R4T, e1, e2, t);  // R^4 (rows into Rr)
     chunk_sync();
-    tri_product(S.mat[3], S.mat[0], S.mat[3], S.mat[1], 0, 4, e1, e2, t);  // P2 = P1 (I+R^4)
-    tri_product(S.mat[0], S.mat[0], nullptr, S.mat[2], 4, 4, e1, e2, t);   // R^8
+    tri_product(S.P1, S.R4T, S.P1, S.P0, nullptr, e1, e2, t);    // P2 = P1 (I+R^4)
+    tri_product(S.Rr, S.R4T, nullptr, S.R2r, S.RT, e1, e2, t);   // R^8 (only R8^T kept)
     chunk_sync();
-    tri_product(S.mat[1], S.mat[2], S.mat[1], S.mat[3], 0, 8, e1, e2, t);  // A = P2 (I+R^8)
+    tri_product(S.P0, S.RT, S.P0, S.P1, nullptr, e1, e2, t);     // A = P2 (I+R^8)
     chunk_sync();
   }
 
@@ -371,7 +410,7 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
     for (int jj = 0; jj < 2; ++jj) {
       const int j = j0 + jj;
       __nv_bfloat16 hi, lo;
-      split_bf16((j <= i) ? S.mat[3][i][j] * S.beta[j] : 0.f, hi, lo);
+      split_bf16((j <= i) ? S.P1[i][j] * S.beta[j] : 0.f, hi, lo);
       S.abh[i * AS + j] = hi;
       S.abl[i * AS + j] = lo;
     }

@@ -3,10 +3,10 @@
 // it, so the records never travel through HBM: HBM traffic is the algorithmic
 // q, k, v, g_raw, beta_raw in and out out (plus the states).
 //
-// Roles (288 threads, two CTAs per SM):
-//   warps 0-3  state threads (tensor-memory lanes 0-127)      kda_state.cuh
-//   warp 4     lane 0 issues the tcgen05 MMAs                 kda_state.cuh
-//   warps 5-8  chunk threads: build record c+1 into the other stage of a
+// Roles (256 threads, two CTAs per SM):
+//   warps 0-3  state threads (tensor-memory lanes 0-127); thread 0 also
+//              issues the tcgen05 MMAs                        kda_state.cuh
+//   warps 4-7  chunk threads: build record c+1 into the other stage of a
 //              2-stage ring while the state threads work on record c
 //                                                             kda_chunk.cuh
 // The chunk threads write the records with ordinary shared-memory stores; each
@@ -23,7 +23,7 @@
 namespace kda {
 
 constexpr int F_NST = 2;
-constexpr int F_THREADS = 288;
+constexpr int F_THREADS = 256;
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
 constexpr int F_CTL_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
@@ -64,11 +64,10 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   if (t == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&ctl->full[s], 128);
-      mbar_init(&ctl->empty[s], 129);
+      mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
     mbar_init(&ctl->mma2, 1);
-    mbar_init(&ctl->eready, 128);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -88,11 +87,11 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   __syncthreads();
   tc_fence_after();
 
-  if (w >= 5) {
+  if (w >= 4) {
     // ---------------- chunk threads ----------------
     // The raw tiles of chunk c are loaded into stage c % 2 while chunk c - 1 is
     // being built, so their latency hides behind that work.
-    const int tc = t - 160;
+    const int tc = t - 128;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
     auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
       t0 = bos + static_cast<int64_t>(c) * kChunk;
@@ -107,6 +106,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
                       v + base, g + base, row_stride, nc, tc);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
+    clear_inverse_workspace(CS, tc);
     uint32_t bbits = nchunks > 0 ? issue(0, 0) : 0u;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
@@ -135,23 +135,12 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       bbits = next_bits;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-  } else if (w == 4) {
-    if (l == 0) {
-      int mma_chunks = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % NST;
-        if (!issue_chunk_mmas(ctl, c, s, smem_u32(smem + s * REC_STRIDE_SMEM), tb, err)) break;
-        ++mma_chunks;
-      }
-      if (*reinterpret_cast<volatile int*>(&ctl->abort)) {
-        mbar_wait(&ctl->mma1, mma_chunks & 1);  // MMA1 of the chunk that stopped, if issued
-        if (mma_chunks) mbar_wait(&ctl->mma2, (mma_chunks - 1) & 1);
-      }
-    }
   } else {
+    // ---------------- state threads (thread 0 issues the MMAs) ----------------
+    auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err);
+               err, release);
   }
   tc_fence_before();
   __syncthreads();

@@ -29,6 +29,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   }
   const int t = threadIdx.x;
   const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+  clear_inverse_workspace(P.chunk, t);
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int64_t slot = item / H;
     const int h = static_cast<int>(item - slot * H);

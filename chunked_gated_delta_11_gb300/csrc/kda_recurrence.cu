@@ -3,16 +3,16 @@
 // records in order ("FlashKDA Delta Attention Algorithm", Kernel K2; the
 // per-chunk arithmetic is in kda_state.cuh).
 //
-// Roles (160 threads): warps 0-3 are the state threads (tensor-memory lanes
-// 0-127, state row v = thread id); warp 4 lane 0 streams the records written
-// by the chunk kernel from HBM into a 3-stage shared-memory ring with one
-// cp.async.bulk per record, and issues every tcgen05 MMA.
+// 128 threads, the state threads (tensor-memory lanes 0-127, state row v =
+// thread id).  Thread 0 also streams the records written by the chunk kernel
+// from HBM into a 3-stage shared-memory ring (one cp.async.bulk per record,
+// refilled as soon as a record's MMAs have finished) and issues every MMA.
 #include "kda_state.cuh"
 
 namespace kda {
 
 constexpr int K2_NST = 3;
-constexpr int K2_THREADS = 160;
+constexpr int K2_THREADS = 128;
 constexpr int K2_SMEM =
     K2_NST * REC_STRIDE_SMEM + 1024 + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 64;
 
@@ -38,11 +38,10 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   if (t == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 129);
+      mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
     mbar_init(&ctl->mma2, 1);
-    mbar_init(&ctl->eready, 128);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -56,48 +55,36 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   const uint32_t tb = ctl->tmem;
   const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
   const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
-  if (w < 4)
-    load_state(tb, lane_off, init ? init + state_base + static_cast<int64_t>(t) * kDim : nullptr);
+  load_state(tb, lane_off, init ? init + state_base + static_cast<int64_t>(t) * kDim : nullptr);
+  int issued = 0;
+  if (t == 0) {
+    const int pre = nchunks < NST ? nchunks : NST;
+    for (int p = 0; p < pre; ++p) {
+      mbar_arrive_expect_tx(&ctl->full[p], REC_BYTES);
+      bulk_g2s(smem + p * REC_STRIDE_SMEM, rec0 + p * rec_step, REC_BYTES, &ctl->full[p]);
+      ++issued;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-
-  if (w == 4) {
-    if (l == 0) {
-      int issued = 0, mma_chunks = 0;
-      const int pre = nchunks < NST ? nchunks : NST;
-      for (int p = 0; p < pre; ++p) {
-        mbar_arrive_expect_tx(&ctl->full[p], REC_BYTES);
-        bulk_g2s(smem + p * REC_STRIDE_SMEM, rec0 + p * rec_step, REC_BYTES, &ctl->full[p]);
-        ++issued;
-      }
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % NST;
-        if (!issue_chunk_mmas(ctl, c, s, smem_u32(smem + s * REC_STRIDE_SMEM), tb, err)) break;
-        ++mma_chunks;
-        // refill the stage of chunk c-1 with chunk c-1+NST
-        if (c >= 1 && c - 1 + NST < nchunks) {
-          const int ps = (c - 1) % NST;
-          if (!wait_or_abort(&ctl->empty[ps], ((c - 1) / NST) & 1, ctl, err)) break;
-          const int p = c - 1 + NST;
-          mbar_arrive_expect_tx(&ctl->full[ps], REC_BYTES);
-          bulk_g2s(smem + ps * REC_STRIDE_SMEM, rec0 + p * rec_step, REC_BYTES, &ctl->full[ps]);
-          ++issued;
-        }
-      }
-      if (*reinterpret_cast<volatile int*>(&ctl->abort)) {
-        // let the copies and MMAs in flight land before the CTA releases its memory
-        // (only the last copy issued into each stage can still be in flight)
-        for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)
-          mbar_wait(&ctl->full[p % NST], (p / NST) & 1);
-        mbar_wait(&ctl->mma1, mma_chunks & 1);  // MMA1 of the chunk that stopped, if issued
-        if (mma_chunks) mbar_wait(&ctl->mma2, (mma_chunks - 1) & 1);
-      }
+  // a record's stage is refilled with the record NST chunks later once its
+  // MMAs are done (the state threads finished reading it before MMA2 started)
+  auto refill = [&](int c, int s) {
+    const int p = c + NST;
+    if (p < nchunks) {
+      mbar_arrive_expect_tx(&ctl->full[s], REC_BYTES);
+      bulk_g2s(smem + s * REC_STRIDE_SMEM, rec0 + p * rec_step, REC_BYTES, &ctl->full[s]);
+      ++issued;
     }
-  } else {
-    state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
-               final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err);
+  };
+  state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
+             final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
+             err, refill);
+  if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
+    // copies still in flight must land before the CTA releases its memory
+    for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)
+      mbar_wait(&ctl->full[p % NST], (p / NST) & 1);
   }
   tc_fence_before();
   __syncthreads();

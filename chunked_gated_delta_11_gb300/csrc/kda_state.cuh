@@ -40,7 +40,7 @@ template <int NST>
 struct StateCtl {
   uint64_t full[NST];
   uint64_t empty[NST];
-  uint64_t mma1, mma2, eready;
+  uint64_t mma1, mma2;
   uint32_t tmem;
   int abort;
 };
@@ -58,6 +58,21 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
     }
   }
   return true;
+}
+
+// AND of `pred` over the 128 state threads (named barrier 2).  Every decision
+// to stop goes through it, so no state thread is ever left at a barrier.
+__device__ __forceinline__ bool state_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 2, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ uint64_t kend_desc(uint32_t saddr) {
@@ -88,25 +103,23 @@ __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
   tmem_wait_st();
 }
 
-// MMA1, MMA2 and MMA3 of chunk c on the record at shared address `sb`
-// (issuing thread only).  Returns false if a wait gave up.
-template <int NST>
-__device__ __forceinline__ bool issue_chunk_mmas(StateCtl<NST>* ctl, int c, int s, uint32_t sb,
-                                                 uint32_t tb, int* err) {
-  const uint32_t id1 = make_idesc(2, 128, 32), id2 = make_idesc(1, 128, 128),
-                 id3 = make_idesc(1, 128, 16);
+// MMA1 of chunk c (16 tf32 steps into D1 of that chunk) on the record at
+// shared address sb.  Issuing thread only.
+__device__ __forceinline__ void issue_mma1(int c, uint32_t sb, uint32_t tb, uint64_t* bar) {
+  const uint32_t id1 = make_idesc(2, 128, 32);
   const uint32_t d1 = tb + d1_col(c);
-  if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) return false;
-  if (c > 0 && !wait_or_abort(&ctl->mma2, (c - 1) & 1, ctl, err)) return false;
-  tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
     mma_tf32_ts(d1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
   }
-  tc_commit(&ctl->mma1);
-  if (!wait_or_abort(&ctl->eready, c & 1, ctl, err)) return false;
-  tc_fence_after();
+  tc_commit(bar);
+}
+
+// MMA2 (state update) and MMA3 (output correction) of chunk c.  Issuing thread only.
+__device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uint64_t* bar) {
+  const uint32_t id2 = make_idesc(1, 128, 128), id3 = make_idesc(1, 128, 16);
+  const uint32_t d1 = tb + d1_col(c);
   const uint64_t kh = kend_desc(sb + OFF_KH), kl = kend_desc(sb + OFF_KL);
   mma_bf16_ts(tb + TM_S, tb + TM_A2H, kh, id2, 1u);
   mma_bf16_ts(tb + TM_S, tb + TM_A2L, kh, id2, 1u);
@@ -116,57 +129,60 @@ __device__ __forceinline__ bool issue_chunk_mmas(StateCtl<NST>* ctl, int c, int 
   mma_bf16_ts(d1 + 16, tb + TM_A2H, ah, id3, 1u);
   mma_bf16_ts(d1 + 16, tb + TM_A2L, ah, id3, 1u);
   mma_bf16_ts(d1 + 16, tb + TM_A2H, al, id3, 1u);
-  tc_commit(&ctl->mma2);
-  tc_commit(&ctl->empty[s]);
-  return true;
+  tc_commit(bar);
 }
 
-// The state threads' work for all chunks, then the final state.  `ring` is the
-// 1024-aligned record ring (stage stride REC_STRIDE_SMEM).
-template <int NST>
-__device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, const uint8_t* ring, int nchunks,
+// The state threads' work for all chunks, then the final state.  Thread v = 0
+// also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
+// REC_STRIDE_SMEM).  `stage_free(c, s)` runs on thread 0 once record c (in
+// stage s) is fully consumed; it refills or releases the stage.
+template <int NST, class StageFree>
+__device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out,
-                                           float* __restrict__ final_dst, int* err) {
+                                           float* __restrict__ final_dst, int* err,
+                                           StageFree&& stage_free) {
   bool ok = true;
+  int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
+  if (v == 0 && nchunks > 0) {
+    ok = wait_or_abort(&ctl->full[0], 0, ctl, err);
+    if (ok) {
+      tc_fence_after();
+      issue_mma1(0, smem_u32(ring), tb, &ctl->mma1);
+      ++n1;
+    }
+  }
   for (int c = 0; c < nchunks; ++c) {
     const int s = c % NST;
     const uint8_t* st = ring + s * REC_STRIDE_SMEM;
-    if (!wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err)) { ok = false; break; }
-    if (!wait_or_abort(&ctl->mma1, c & 1, ctl, err)) { ok = false; break; }
-    tc_fence_after();
-    // forget: S[v][:] *= dlast (MMA1 has finished reading S); two 32-column
-    // loads are in flight per wait
-    const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
+    if (ok) ok = wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err);
+    if (ok) ok = wait_or_abort(&ctl->mma1, c & 1, ctl, err);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      // forget: S[v][:] *= dlast (MMA1 has finished reading S), 32 columns at a time
+      const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
 #pragma unroll
-    for (int hq = 0; hq < 2; ++hq) {
-      uint32_t ra[32], rb[32];
-      tmem_ld32(tb + TM_S + lane_off + hq * 64, ra);
-      tmem_ld32(tb + TM_S + lane_off + hq * 64 + 32, rb);
-      tmem_wait_ld();
+      for (int qd = 0; qd < 4; ++qd) {
+        uint32_t r[32];
+        tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 da = dl4[hq * 16 + i4];
-        const float4 db = dl4[hq * 16 + 8 + i4];
-        ra[4 * i4 + 0] = __float_as_uint(__uint_as_float(ra[4 * i4 + 0]) * da.x);
-        ra[4 * i4 + 1] = __float_as_uint(__uint_as_float(ra[4 * i4 + 1]) * da.y);
-        ra[4 * i4 + 2] = __float_as_uint(__uint_as_float(ra[4 * i4 + 2]) * da.z);
-        ra[4 * i4 + 3] = __float_as_uint(__uint_as_float(ra[4 * i4 + 3]) * da.w);
-        rb[4 * i4 + 0] = __float_as_uint(__uint_as_float(rb[4 * i4 + 0]) * db.x);
-        rb[4 * i4 + 1] = __float_as_uint(__uint_as_float(rb[4 * i4 + 1]) * db.y);
-        rb[4 * i4 + 2] = __float_as_uint(__uint_as_float(rb[4 * i4 + 2]) * db.z);
-        rb[4 * i4 + 3] = __float_as_uint(__uint_as_float(rb[4 * i4 + 3]) * db.w);
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 dv = dl4[qd * 8 + i4];
+          r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
+          r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
+          r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
+          r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
+        }
+        tmem_st32(tb + TM_S + lane_off + qd * 32, r);
       }
-      tmem_st32(tb + TM_S + lane_off + hq * 64, ra);
-      tmem_st32(tb + TM_S + lane_off + hq * 64 + 32, rb);
-    }
-    uint32_t d1[16];
-    tmem_ld16(tb + d1_col(c) + lane_off, d1);
-    tmem_wait_ld();
-    // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v]
-    const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
-    {
+      uint32_t d1[16];
+      tmem_ld16(tb + d1_col(c) + lane_off, d1);
+      tmem_wait_ld();
+      // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
+      const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
       uint32_t pk[16];
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4) {
@@ -179,25 +195,52 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, const uint8_t* ri
         split_pair2(e2, e3, pk[2 * i4 + 1], pk[8 + 2 * i4 + 1]);
       }
       tmem_st16(tb + TM_A2H + lane_off, pk);
+      tmem_wait_st();
+      tc_fence_before();
     }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&ctl->eready);
-    mbar_arrive(&ctl->empty[s]);  // U and dlast are read; the MMAs hold the rest
-    // outputs: D1[v][16 + i] = o[i][v] once MMA2/MMA3 of this chunk are done
-    if (!wait_or_abort(&ctl->mma2, c & 1, ctl, err)) { ok = false; break; }
-    tc_fence_after();
-    uint32_t o[16];
-    tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
-    tmem_wait_ld();
-    const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
-    const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
-    __nv_bfloat16* orow = out + (t0 * H + h) * kDim + v;
+    // every state thread has written E^T and finished reading U and dlast
+    if (!state_all(ok)) { ok = false; break; }
+    if (v == 0) {
+      tc_fence_after();
+      issue_mma23(c, smem_u32(st), tb, &ctl->mma2);
+      ++n2;
+    }
+    ok = wait_or_abort(&ctl->mma2, c & 1, ctl, err);
+    if (v == 0 && ok) {
+      tc_fence_after();
+      stage_free(c, s);
+      if (c + 1 < nchunks) {
+        const int s1 = (c + 1) % NST;
+        ok = wait_or_abort(&ctl->full[s1], ((c + 1) / NST) & 1, ctl, err);
+        if (ok) {
+          tc_fence_after();
+          issue_mma1(c + 1, smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1);
+          ++n1;
+        }
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      // outputs: D1[v][16 + i] = o[i][v] (MMA1 of chunk c+1 writes the other D1)
+      tc_fence_after();
+      uint32_t o[16];
+      tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
+      tmem_wait_ld();
+      const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
+      const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
+      __nv_bfloat16* orow = out + (t0 * H + h) * kDim + v;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < nc) orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
+      for (int i = 0; i < 16; ++i)
+        if (i < nc)
+          orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
+    }
   }
-  if (ok && nchunks > 0 && !wait_or_abort(&ctl->mma2, (nchunks - 1) & 1, ctl, err)) ok = false;
+  ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
+  if (!ok && v == 0) {
+    // let MMAs still in flight finish before the CTA frees its tensor memory
+    if (n1 > 0) mbar_wait(&ctl->mma1, (n1 - 1) & 1);
+    if (n2 > 0) mbar_wait(&ctl->mma2, (n2 - 1) & 1);
+  }
   tc_fence_after();
   if (ok && final_dst) {
 #pragma unroll
