@@ -162,14 +162,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test, but a thread whose phase is not complete sleeps in hardware until
+// it completes or about `hint_ns` nanoseconds pass, instead of spinning on the
+// issue slots that the other warps of its SM partition need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Every wait in libkda is bounded: ~2^31 SM cycles (about a second) and then
 // the caller records an error and unwinds instead of hanging the GPU.
 constexpr long long kWaitLimitCycles = 1LL << 31;
+constexpr uint32_t kSleepHintNs = 20000;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
   return true;

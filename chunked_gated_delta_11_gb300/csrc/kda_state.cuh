@@ -49,7 +49,7 @@ template <class Ctl>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
