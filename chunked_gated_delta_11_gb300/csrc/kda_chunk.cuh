@@ -203,13 +203,16 @@ __device__ __forceinline__ void tri_entry(const float (*X)[20], const float (*YT
   Cm[i][j] = c;
   if (CT) CT[j][i] = c;
 }
-// Thread t of 128 computes entries e1 = kEntries[t] and, for t < 8, e2 =
-// kEntries[128 + t] (packed (i << 4) | j, loaded once per chunk).
+// Thread t of 128 computes entry e1 = kEntries[t] and, on lanes 0 and 1 of
+// each warp, e2 = kEntries[128 + 2 (t / 32) + lane] (packed (i << 4) | j,
+// loaded once per chunk), so the eight extra entries are spread over the warps.
+__device__ __forceinline__ bool has_second_entry(int t) { return (t & 31) < 2; }
+__device__ __forceinline__ int second_entry_index(int t) { return 128 + (t >> 5) * 2 + (t & 31); }
 __device__ __forceinline__ void tri_product(const float (*X)[20], const float (*YT)[20],
                                             const float (*B)[20], float (*Cm)[20],
                                             float (*CT)[20], int e1, int e2, int t) {
   tri_entry(X, YT, B, Cm, CT, e1 >> 4, e1 & 15);
-  if (t < 8) tri_entry(X, YT, B, Cm, CT, e2 >> 4, e2 & 15);
+  if (has_second_entry(t)) tri_entry(X, YT, B, Cm, CT, e2 >> 4, e2 & 15);
 }
 
 // Zero the inverse workspace once (its unwritten triangles must stay zero).
@@ -238,27 +241,36 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
   }
   chunk_sync();
 
-  // ---- per-token inverse norms (warp w: tokens 4w .. 4w+3) ----
+  // ---- per-token inverse norms (warp w: tokens 4w .. 4w+3), all eight sums
+  // reduced together so the shuffle latencies overlap ----
+  {
+    float sq[4], sk[4];
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = w * 4 + ii;
-    const int off = raw_piece(i, l >> 1) + (l & 1) * 8;
-    const uint2 qv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_Q, i) + off);
-    const uint2 kv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_K, i) + off);
-    const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
-    const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
-    const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
-    const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
-    float sq = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
-    float sk = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+    for (int ii = 0; ii < 4; ++ii) {
+      const int i = w * 4 + ii;
+      const int off = raw_piece(i, l >> 1) + (l & 1) * 8;
+      const uint2 qv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_Q, i) + off);
+      const uint2 kv = *reinterpret_cast<const uint2*>(raw_row(R, RAW_K, i) + off);
+      const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.x));
+      const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qv.y));
+      const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.x));
+      const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kv.y));
+      sq[ii] = q0.x * q0.x + q0.y * q0.y + q1.x * q1.x + q1.y * q1.y;
+      sk[ii] = k0.x * k0.x + k0.y * k0.y + k1.x * k1.x + k1.y * k1.y;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        sq[ii] += __shfl_xor_sync(0xffffffffu, sq[ii], o);
+        sk[ii] += __shfl_xor_sync(0xffffffffu, sk[ii], o);
+      }
     }
-    if (l == 0) {
-      S.rq[i] = rsqrtf(sq + eps);
-      S.rk[i] = rsqrtf(sk + eps);
+    if (l < 4) {
+      // the read scale is folded into the query norm: rq = scale / |q|
+      S.rq[w * 4 + l] =
+          scale * rsqrtf((l == 0 ? sq[0] : l == 1 ? sq[1] : l == 2 ? sq[2] : sq[3]) + eps);
+      S.rk[w * 4 + l] = rsqrtf((l == 0 ? sk[0] : l == 1 ? sk[1] : l == 2 ? sk[2] : sk[3]) + eps);
     }
   }
   chunk_sync();
@@ -283,20 +295,23 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       uint32_t qh[4], ql[4], kh[4], kl[4];
 #pragma unroll
       for (int i2 = 0; i2 < 4; ++i2) {
-        float Qd[2], Kd[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int i = half * 8 + i2 * 2 + u;
-          const int off = raw_piece(i, dp) + db;
-          p *= a[i];
-          const float qv = bf16_at(raw_row(R, RAW_Q, i) + off) * S.rq[i];
-          const float kv = bf16_at(raw_row(R, RAW_K, i) + off) * S.rk[i];
-          Qd[u] = scale * qv * p;
-          Kd[u] = kv * p;
-          *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd[u]);
-        }
-        split_pair2(Qd[0], Qd[1], qh[i2], ql[i2]);
-        split_pair2(Kd[0], Kd[1], kh[i2], kl[i2]);
+        const int i = half * 8 + i2 * 2;  // tokens i, i + 1 as one packed pair
+        const int o0 = raw_piece(i, dp) + db, o1 = raw_piece(i + 1, dp) + db;
+        float2 P;
+        p *= a[i];
+        P.x = p;
+        p *= a[i + 1];
+        P.y = p;
+        const float2 qr = make_float2(bf16_at(raw_row(R, RAW_Q, i) + o0),
+                                      bf16_at(raw_row(R, RAW_Q, i + 1) + o1));
+        const float2 kr = make_float2(bf16_at(raw_row(R, RAW_K, i) + o0),
+                                      bf16_at(raw_row(R, RAW_K, i + 1) + o1));
+        const float2 Qd = mul2(mul2(qr, make_float2(S.rq[i], S.rq[i + 1])), P);
+        const float2 Kd = mul2(mul2(kr, make_float2(S.rk[i], S.rk[i + 1])), P);
+        *reinterpret_cast<float*>(rec + b1_offset(16 + i, d)) = to_tf32(Qd.x);
+        *reinterpret_cast<float*>(rec + b1_offset(17 + i, d)) = to_tf32(Qd.y);
+        split_pair2(Qd.x, Qd.y, qh[i2], ql[i2]);
+        split_pair2(Kd.x, Kd.y, kh[i2], kl[i2]);
       }
       const int o = drv_off(d, half);
       *reinterpret_cast<uint4*>(S.qdh + o) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
@@ -313,17 +328,19 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       uint32_t eh[4], el[4], ih[4], il[4];
 #pragma unroll
       for (int i2 = 3; i2 >= 0; --i2) {
-        float Ke[2], Ki[2];
-#pragma unroll
-        for (int u = 1; u >= 0; --u) {
-          const int i = half * 8 + i2 * 2 + u;
-          const float kv = bf16_at(raw_row(R, RAW_K, i) + raw_piece(i, dp) + db) * S.rk[i];
-          Ke[u] = kv * sfx;
-          Ki[u] = Ke[u] * inv_dl;
-          sfx *= a[i];
-        }
-        split_pair2(Ke[0], Ke[1], eh[i2], el[i2]);
-        split_pair2(Ki[0], Ki[1], ih[i2], il[i2]);
+        const int i = half * 8 + i2 * 2;  // tokens i, i + 1 as one packed pair
+        float2 Q;
+        Q.y = sfx;
+        sfx *= a[i + 1];
+        Q.x = sfx;
+        sfx *= a[i];
+        const float2 kr =
+            make_float2(bf16_at(raw_row(R, RAW_K, i) + raw_piece(i, dp) + db),
+                        bf16_at(raw_row(R, RAW_K, i + 1) + raw_piece(i + 1, dp) + db));
+        const float2 Ke = mul2(mul2(kr, make_float2(S.rk[i], S.rk[i + 1])), Q);
+        const float2 Ki = mul2(Ke, make_float2(inv_dl, inv_dl));
+        split_pair2(Ke.x, Ke.y, eh[i2], el[i2]);
+        split_pair2(Ki.x, Ki.y, ih[i2], il[i2]);
       }
       const int o = drv_off(d, half);
       *reinterpret_cast<uint4*>(S.kih + o) = make_uint4(ih[0], ih[1], ih[2], ih[3]);
@@ -390,7 +407,7 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
 
   // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent steps ----
   {
-    const int e1 = kEntries.ij[t], e2 = t < 8 ? kEntries.ij[128 + t] : 0;
+    const int e1 = kEntries.ij[t], e2 = has_second_entry(t) ? kEntries.ij[second_entry_index(t)] : 0;
     tri_product(S.Rr, S.RT, nullptr, S.R2r, S.R2T, e1, e2, t);   // R^2
     chunk_sync();
     tri_product(S.P0, S.R2T, S.P0, S.P1, nullptr, e1, e2, t);    // P1 = (I-R)(I+R^2)
