@@ -116,13 +116,20 @@ def dist_init():
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Slowest rank's value (the step time every rank reports is the max)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (max_ms * 1e-3)
 
 
 def barrier(world):
@@ -321,7 +328,7 @@ def main():
         assert kda.kda_device_status() == 0
 
     tokens_per_step = T * world
-    value = tokens_per_step / (ms * 1e-3)
+    value = whole_job_rate(T, world, ms)
     units = N * H
     init_bytes = STATE_BYTES * units if inp["initial_state"] is not None else 0
     alg_bytes = ALG_BYTES_PER_TOKEN_HEAD * T * H + STATE_BYTES * units + init_bytes

@@ -226,20 +226,23 @@ __device__ __forceinline__ void clear_inverse_workspace(ChunkSmem& S, int t) {
 // issue_raw_loads (this call waits for them).  All 128 threads of the group
 // must call it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
 // beta_raw (any value for t >= nc).  `rec` is the record base (global or
-// shared).  `after_d` runs on all threads once the raw q, k and g tiles are no
-// longer needed (the fused kernel issues the next chunk's loads there).
-template <class Hook>
-__device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles& R,
+// shared).  `may_write()` runs on all threads before the first write to the
+// record and returns, uniformly, whether to go on (the fused kernel waits there
+// until the previous record in this stage is consumed); on false nothing is
+// written.  `after_d` runs on all threads in the middle of the build (the
+// fused kernel issues the next chunk's loads there).  Returns may_write().
+template <class MayWrite, class Hook>
+__device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, const RawTiles& R,
                                                    uint32_t beta_raw_bits, int nc, float scale,
                                                    float lb_log2e, float eps, uint8_t* rec,
-                                                   int t, Hook&& after_d) {
+                                                   int t, MayWrite&& may_write, Hook&& after_d) {
   const int w = t >> 5, l = t & 31;
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (t < 16) {
     const float br = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(beta_raw_bits)));
     S.beta[t] = (t < nc) ? sigmoid_fast(br) : 0.f;
   }
-  chunk_sync();
+  if (!may_write()) return false;  // includes a barrier of the 128 threads
 
   // ---- per-token inverse norms (warp w: tokens 4w .. 4w+3), all eight sums
   // reduced together so the shuffle latencies overlap ----
@@ -489,6 +492,7 @@ __device__ __forceinline__ void build_chunk_record(ChunkSmem& S, const RawTiles&
       U[(c + 1) * 16 + r0 + 8] = ua[nt][3];
     }
   }
+  return true;
 }
 
 // Locate record slot `slot`: the sequence n with slot0(n) <= slot < slot0(n+1)

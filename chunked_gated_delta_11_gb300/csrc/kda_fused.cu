@@ -65,6 +65,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     for (int s = 0; s < NST; ++s) {
       mbar_init(&ctl->full[s], 128);
       mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl->rawfree[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
     mbar_init(&ctl->mma2, 1);
@@ -112,11 +113,20 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       const int s = c % NST;
       uint32_t next_bits = 0u;
       bool stop = false;
+      // before writing record c into stage s: record c - NST there must be
+      // fully consumed (its MMAs read Kend, Aqk and Qdec)
+      auto may_write = [&]() -> bool {
+        bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
+        ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
+        return chunk_all(ok);
+      };
+      // mid-build: load chunk c+1's raw tiles into the W/U area of its stage as
+      // soon as the record there (c + 1 - NST) no longer needs W and U
       auto prefetch = [&] {
         if (c + 1 >= nchunks) return;
         const int s1 = (c + 1) % NST;
         bool ok = c + 1 < NST ||
-                  wait_or_abort(&ctl->empty[s1], (((c + 1) / NST) - 1) & 1, ctl, err);
+                  wait_or_abort(&ctl->rawfree[s1], (((c + 1) / NST) - 1) & 1, ctl, err);
         ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
         if (chunk_all(ok))
           next_bits = issue(c + 1, s1);
@@ -127,8 +137,9 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       int nc;
       chunk_geom(c, t0, nc);
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
-      build_chunk_record(CS, raw_tiles_in_record(rec), bbits, nc, scale, lb_log2e, eps, rec, tc,
-                         prefetch);
+      if (!build_chunk_record(CS, raw_tiles_in_record(rec), bbits, nc, scale, lb_log2e, eps, rec,
+                              tc, may_write, prefetch))
+        break;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&ctl->full[s]);
       if (stop) break;
@@ -137,10 +148,11 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
+    auto wu_free = [&](int, int s) { mbar_arrive(&ctl->rawfree[s]); };
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err, release);
+               err, wu_free, release);
   }
   tc_fence_before();
   __syncthreads();

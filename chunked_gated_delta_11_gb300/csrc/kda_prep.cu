@@ -43,7 +43,8 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const uint32_t bbits =
         (t < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + t) * H + h]) : 0u;
     build_chunk_record(P.chunk, R, bbits, nc, scale, lb_log2e, eps,
-                       ws + static_cast<int64_t>(item) * REC_BYTES, t, [] {});
+                       ws + static_cast<int64_t>(item) * REC_BYTES, t,
+                       [] { chunk_sync(); return true; }, [] {});
   }
 }
 

@@ -80,7 +80,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   };
   state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
              final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-             err, refill);
+             err, [](int, int) {}, refill);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory
     for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)

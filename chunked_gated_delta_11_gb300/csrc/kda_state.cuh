@@ -39,7 +39,8 @@ __device__ __forceinline__ uint32_t d1_col(int c) { return TM_D1 + 32u * static_
 template <int NST>
 struct StateCtl {
   uint64_t full[NST];
-  uint64_t empty[NST];
+  uint64_t empty[NST];    // record fully consumed (its MMAs are done)
+  uint64_t rawfree[NST];  // its W and U areas are consumed (MMA1 and the errors are done)
   uint64_t mma1, mma2;
   uint32_t tmem;
   int abort;
@@ -134,15 +135,16 @@ __device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uin
 
 // The state threads' work for all chunks, then the final state.  Thread v = 0
 // also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
-// REC_STRIDE_SMEM).  `stage_free(c, s)` runs on thread 0 once record c (in
-// stage s) is fully consumed; it refills or releases the stage.
-template <int NST, class StageFree>
+// REC_STRIDE_SMEM).  On thread 0, `wu_free(c, s)` runs once MMA1 of record c
+// and every read of its U and dlast are done (its W and U areas may be
+// reused), and `stage_free(c, s)` once all of its MMAs are done.
+template <int NST, class WUFree, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ final_dst, int* err,
-                                           StageFree&& stage_free) {
+                                           WUFree&& wu_free, StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   if (v == 0 && nchunks > 0) {
@@ -204,6 +206,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tc_fence_after();
       issue_mma23(c, smem_u32(st), tb, &ctl->mma2);
       ++n2;
+      wu_free(c, s);
     }
     ok = wait_or_abort(&ctl->mma2, c & 1, ctl, err);
     if (v == 0 && ok) {
