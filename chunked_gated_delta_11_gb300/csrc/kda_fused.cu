@@ -25,7 +25,8 @@ namespace kda {
 constexpr int F_NST = 2;
 constexpr int F_THREADS = 256;
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
-constexpr int F_CTL_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
+constexpr int F_OST_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
+constexpr int F_CTL_OFF = F_OST_OFF + 4096;
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
 
 // AND of `pred` over the 128 chunk threads (named barrier 1).
@@ -68,6 +69,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       mbar_init(&ctl->rawfree[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
+    mbar_init(&ctl->mma1b, 1);
     mbar_init(&ctl->mma2, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -152,7 +154,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err, wu_free, release);
+               err, smem + F_OST_OFF, wu_free, release);
   }
   tc_fence_before();
   __syncthreads();

@@ -13,8 +13,9 @@ namespace kda {
 
 constexpr int K2_NST = 3;
 constexpr int K2_THREADS = 128;
-constexpr int K2_SMEM =
-    K2_NST * REC_STRIDE_SMEM + 1024 + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 64;
+constexpr int K2_OST_OFF = K2_NST * REC_STRIDE_SMEM;
+constexpr int K2_CTL_OFF = K2_OST_OFF + 4096;
+constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 1024 + 64;
 
 __global__ void __launch_bounds__(K2_THREADS, 2)
 recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init,
@@ -24,7 +25,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   constexpr int NST = K2_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + NST * REC_STRIDE_SMEM);
+  auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + K2_CTL_OFF);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int unit = blockIdx.x;
   const int n = unit / H, h = unit - (unit / H) * H;
@@ -41,6 +42,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
+    mbar_init(&ctl->mma1b, 1);
     mbar_init(&ctl->mma2, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -80,7 +82,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   };
   state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
              final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-             err, [](int, int) {}, refill);
+             err, smem + K2_OST_OFF, [](int, int) {}, refill);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory
     for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)

@@ -41,7 +41,7 @@ struct StateCtl {
   uint64_t full[NST];
   uint64_t empty[NST];    // record fully consumed (its MMAs are done)
   uint64_t rawfree[NST];  // its W and U areas are consumed (MMA1 and the errors are done)
-  uint64_t mma1, mma2;
+  uint64_t mma1, mma1b, mma2;  // MMA1 k-steps over channels 0-63, then 64-127; MMA2/3
   uint32_t tmem;
   int abort;
 };
@@ -105,16 +105,20 @@ __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
 }
 
 // MMA1 of chunk c (16 tf32 steps into D1 of that chunk) on the record at
-// shared address sb.  Issuing thread only.
-__device__ __forceinline__ void issue_mma1(int c, uint32_t sb, uint32_t tb, uint64_t* bar) {
+// shared address sb, committed in two halves: `bar_a` completes once the steps
+// over key channels 0-63 are done (those state columns may then be rewritten),
+// `bar_b` once all are.  Issuing thread only.
+__device__ __forceinline__ void issue_mma1(int c, uint32_t sb, uint32_t tb, uint64_t* bar_a,
+                                           uint64_t* bar_b) {
   const uint32_t id1 = make_idesc(2, 128, 32);
   const uint32_t d1 = tb + d1_col(c);
 #pragma unroll
   for (int kk = 0; kk < 16; ++kk) {
     const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
     mma_tf32_ts(d1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+    if (kk == 7) tc_commit(bar_a);
   }
-  tc_commit(bar);
+  tc_commit(bar_b);
 }
 
 // MMA2 (state update) and MMA3 (output correction) of chunk c.  Issuing thread only.
@@ -137,21 +141,24 @@ __device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uin
 // also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
 // REC_STRIDE_SMEM).  On thread 0, `wu_free(c, s)` runs once MMA1 of record c
 // and every read of its U and dlast are done (its W and U areas may be
-// reused), and `stage_free(c, s)` once all of its MMAs are done.
+// reused), and `stage_free(c, s)` once all of its MMAs are done.  `ostage` is
+// 4 KB of shared memory (1 KB per state warp) used to turn each warp's 16 x 32
+// output tile into 16-byte stores.
 template <int NST, class WUFree, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ final_dst, int* err,
-                                           WUFree&& wu_free, StageFree&& stage_free) {
+                                           uint8_t* ostage, WUFree&& wu_free,
+                                           StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   if (v == 0 && nchunks > 0) {
     ok = wait_or_abort(&ctl->full[0], 0, ctl, err);
     if (ok) {
       tc_fence_after();
-      issue_mma1(0, smem_u32(ring), tb, &ctl->mma1);
+      issue_mma1(0, smem_u32(ring), tb, &ctl->mma1, &ctl->mma1b);
       ++n1;
     }
   }
@@ -163,10 +170,16 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      // forget: S[v][:] *= dlast (MMA1 has finished reading S), 32 columns at a time
+      // forget: S[v][:] *= dlast, 32 columns at a time; columns 0-63 while MMA1
+      // still reads columns 64-127, the rest once MMA1 is done
       const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
 #pragma unroll
       for (int qd = 0; qd < 4; ++qd) {
+        if (qd == 2) {
+          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma1b, c & 1, ctl, err));
+          if (!ok) break;
+          tc_fence_after();
+        }
         uint32_t r[32];
         tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
         tmem_wait_ld();
@@ -180,25 +193,27 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
         }
         tmem_st32(tb + TM_S + lane_off + qd * 32, r);
       }
-      uint32_t d1[16];
-      tmem_ld16(tb + d1_col(c) + lane_off, d1);
-      tmem_wait_ld();
-      // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
-      const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
-      uint32_t pk[16];
+      if (ok) {
+        uint32_t d1[16];
+        tmem_ld16(tb + d1_col(c) + lane_off, d1);
+        tmem_wait_ld();
+        // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
+        const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
+        uint32_t pk[16];
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 u = U4[i4];
-        const float e0 = u.x - __uint_as_float(d1[i4 * 4 + 0]);
-        const float e1 = u.y - __uint_as_float(d1[i4 * 4 + 1]);
-        const float e2 = u.z - __uint_as_float(d1[i4 * 4 + 2]);
-        const float e3 = u.w - __uint_as_float(d1[i4 * 4 + 3]);
-        split_pair2(e0, e1, pk[2 * i4], pk[8 + 2 * i4]);
-        split_pair2(e2, e3, pk[2 * i4 + 1], pk[8 + 2 * i4 + 1]);
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const float4 u = U4[i4];
+          const float e0 = u.x - __uint_as_float(d1[i4 * 4 + 0]);
+          const float e1 = u.y - __uint_as_float(d1[i4 * 4 + 1]);
+          const float e2 = u.z - __uint_as_float(d1[i4 * 4 + 2]);
+          const float e3 = u.w - __uint_as_float(d1[i4 * 4 + 3]);
+          split_pair2(e0, e1, pk[2 * i4], pk[8 + 2 * i4]);
+          split_pair2(e2, e3, pk[2 * i4 + 1], pk[8 + 2 * i4 + 1]);
+        }
+        tmem_st16(tb + TM_A2H + lane_off, pk);
+        tmem_wait_st();
+        tc_fence_before();
       }
-      tmem_st16(tb + TM_A2H + lane_off, pk);
-      tmem_wait_st();
-      tc_fence_before();
     }
     // every state thread has written E^T and finished reading U and dlast
     if (!state_all(ok)) { ok = false; break; }
@@ -217,7 +232,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
         ok = wait_or_abort(&ctl->full[s1], ((c + 1) / NST) & 1, ctl, err);
         if (ok) {
           tc_fence_after();
-          issue_mma1(c + 1, smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1);
+          issue_mma1(c + 1, smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1, &ctl->mma1b);
           ++n1;
         }
       }
@@ -231,17 +246,28 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tmem_wait_ld();
       const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
       const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      __nv_bfloat16* orow = out + (t0 * H + h) * kDim + v;
+      // warp tile [16 tokens][32 channels] bf16 through shared memory
+      const int w = v >> 5, l = v & 31;
+      uint8_t* ost = ostage + w * 1024;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<__nv_bfloat16*>(ost + i * 64 + l * 2) =
+            __float2bfloat16_rn(__uint_as_float(o[i]));
+      __syncwarp();
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int p = l + 32 * rep, i = p >> 2, sub = p & 3;
         if (i < nc)
-          orow[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
+          *reinterpret_cast<uint4*>(out + ((t0 + i) * H + h) * kDim + w * 32 + sub * 8) =
+              *reinterpret_cast<const uint4*>(ost + i * 64 + sub * 16);
+      }
+      __syncwarp();
     }
   }
   ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
   if (!ok && v == 0) {
     // let MMAs still in flight finish before the CTA frees its tensor memory
-    if (n1 > 0) mbar_wait(&ctl->mma1, (n1 - 1) & 1);
+    if (n1 > 0) mbar_wait(&ctl->mma1b, (n1 - 1) & 1);
     if (n2 > 0) mbar_wait(&ctl->mma2, (n2 - 1) & 1);
   }
   tc_fence_after();
