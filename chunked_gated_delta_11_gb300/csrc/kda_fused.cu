@@ -25,8 +25,8 @@ namespace kda {
 constexpr int F_NST = 2;
 constexpr int F_THREADS = 256;
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
-constexpr int F_OST_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
-constexpr int F_CTL_OFF = F_OST_OFF + 4096;
+constexpr int F_RAW_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
+constexpr int F_CTL_OFF = F_RAW_OFF + RAW_BYTES;
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
 
 // AND of `pred` over the 128 chunk threads (named barrier 1).
@@ -66,7 +66,6 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     for (int s = 0; s < NST; ++s) {
       mbar_init(&ctl->full[s], 128);
       mbar_init(&ctl->empty[s], 1);
-      mbar_init(&ctl->rawfree[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
     mbar_init(&ctl->mma1b, 1);
@@ -92,69 +91,63 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 
   if (w >= 4) {
     // ---------------- chunk threads ----------------
-    // The raw tiles of chunk c are loaded into stage c % 2 while chunk c - 1 is
-    // being built, so their latency hides behind that work.
+    // Raw tiles have their own buffer: q, k, g_raw of chunk c+1 load once the
+    // gate phase of chunk c is done with them, v of chunk c at the start of
+    // its own build, so their latency hides behind the rest of a build.
     const int tc = t - 128;
+    uint8_t* raw = smem + F_RAW_OFF;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
     auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
       t0 = bos + static_cast<int64_t>(c) * kChunk;
       nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
     };
-    auto issue = [&](int c, int s) -> uint32_t {
+    auto start = [&](int c) -> uint32_t {
       int64_t t0;
       int nc;
       chunk_geom(c, t0, nc);
       const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      issue_raw_loads(raw_tiles_in_record(smem + s * REC_STRIDE_SMEM), q + base, k + base,
-                      v + base, g + base, row_stride, nc, tc);
+      issue_qkg_loads(raw, q + base, k + base, g + base, row_stride, nc, tc);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
-    clear_inverse_workspace(CS, tc);
-    uint32_t bbits = nchunks > 0 ? issue(0, 0) : 0u;
+    clear_chunk_workspace(CS, tc);
+    uint32_t bbits = nchunks > 0 ? start(0) : 0u;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
+      int64_t t0;
+      int nc;
+      chunk_geom(c, t0, nc);
       uint32_t next_bits = 0u;
-      bool stop = false;
       // before writing record c into stage s: record c - NST there must be
-      // fully consumed (its MMAs read Kend, Aqk and Qdec)
+      // fully consumed (its MMAs read W, Qdec, Kend and Aqk)
       auto may_write = [&]() -> bool {
         bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
         ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
         return chunk_all(ok);
       };
-      // mid-build: load chunk c+1's raw tiles into the W/U area of its stage as
-      // soon as the record there (c + 1 - NST) no longer needs W and U
-      auto prefetch = [&] {
-        if (c + 1 >= nchunks) return;
-        const int s1 = (c + 1) % NST;
-        bool ok = c + 1 < NST ||
-                  wait_or_abort(&ctl->rawfree[s1], (((c + 1) / NST) - 1) & 1, ctl, err);
-        ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
-        if (chunk_all(ok))
-          next_bits = issue(c + 1, s1);
-        else
-          stop = true;
+      auto load_v = [&] {
+        issue_v_loads(raw, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, row_stride, nc,
+                      tc);
       };
-      int64_t t0;
-      int nc;
-      chunk_geom(c, t0, nc);
+      auto next_qkg = [&]() -> bool {
+        if (c + 1 >= nchunks) return false;
+        next_bits = start(c + 1);
+        return true;
+      };
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
-      if (!build_chunk_record(CS, raw_tiles_in_record(rec), bbits, nc, scale, lb_log2e, eps, rec,
-                              tc, may_write, prefetch))
+      if (!build_chunk_record(CS, raw, bbits, nc, scale, lb_log2e, eps, rec, tc, may_write,
+                              load_v, next_qkg))
         break;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&ctl->full[s]);
-      if (stop) break;
       bbits = next_bits;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
-    auto wu_free = [&](int, int s) { mbar_arrive(&ctl->rawfree[s]); };
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err, smem + F_OST_OFF, wu_free, release);
+               err, release);
   }
   tc_fence_before();
   __syncthreads();

@@ -10,7 +10,7 @@ namespace kda {
 
 struct PrepSmem {
   ChunkSmem chunk;
-  uint8_t raw[4 * 4096];  // q, k, v, g_raw tiles of the current chunk
+  uint8_t raw[RAW_BYTES];  // q, k, v, g_raw tiles
 };
 
 __global__ void __launch_bounds__(128, 4)
@@ -21,30 +21,59 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   uint8_t* __restrict__ ws, int64_t n_items) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PrepSmem& P = *reinterpret_cast<PrepSmem*>(smem_raw);
-  RawTiles R;
-#pragma unroll
-  for (int x = 0; x < 4; ++x) {
-    R.lo[x] = P.raw + x * 4096;
-    R.hi[x] = P.raw + x * 4096 + 2048;
-  }
   const int t = threadIdx.x;
   const int64_t row_stride = static_cast<int64_t>(H) * kDim;
-  clear_inverse_workspace(P.chunk, t);
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int64_t slot = item / H;
-    const int h = static_cast<int>(item - slot * H);
-    int n;
-    int64_t bos, eos, c;
-    if (!locate_slot(cu, T_total, N, slot, n, bos, eos, c)) continue;
-    const int64_t t0 = bos + c * kChunk;
-    const int nc = static_cast<int>(((eos - t0) < kChunk ? (eos - t0) : kChunk));
-    const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-    issue_raw_loads(R, q + base, k + base, v + base, g + base, row_stride, nc, t);
-    const uint32_t bbits =
-        (t < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + t) * H + h]) : 0u;
-    build_chunk_record(P.chunk, R, bbits, nc, scale, lb_log2e, eps,
-                       ws + static_cast<int64_t>(item) * REC_BYTES, t,
-                       [] { chunk_sync(); return true; }, [] {});
+  clear_chunk_workspace(P.chunk, t);
+
+  // the next used slot at or after `item` on this CTA's grid stride
+  struct Item {
+    int64_t item, base, t0;
+    int h, nc;
+  };
+  auto find = [&](int64_t item, Item& it) -> bool {
+    for (; item < n_items; item += gridDim.x) {
+      const int64_t slot = item / H;
+      const int h = static_cast<int>(item - slot * H);
+      int n;
+      int64_t bos, eos, c;
+      if (locate_slot(cu, T_total, N, slot, n, bos, eos, c)) {
+        it.item = item;
+        it.h = h;
+        it.t0 = bos + c * kChunk;
+        it.nc = static_cast<int>(((eos - it.t0) < kChunk ? (eos - it.t0) : kChunk));
+        it.base = it.t0 * row_stride + static_cast<int64_t>(h) * kDim;
+        return true;
+      }
+    }
+    return false;
+  };
+  auto start = [&](const Item& it) -> uint32_t {
+    issue_qkg_loads(P.raw, q + it.base, k + it.base, g + it.base, row_stride, it.nc, t);
+    return (t < it.nc) ? __bfloat16_as_ushort(beta_raw[(it.t0 + t) * H + it.h]) : 0u;
+  };
+
+  Item cur, nxt;
+  bool have = find(blockIdx.x, cur);
+  uint32_t bbits = have ? start(cur) : 0u;
+  while (have) {
+    bool have_next = false;
+    uint32_t next_bits = 0u;
+    build_chunk_record(
+        P.chunk, P.raw, bbits, cur.nc, scale, lb_log2e, eps,
+        ws + static_cast<int64_t>(cur.item) * REC_BYTES, t,
+        [] {
+          chunk_sync();
+          return true;
+        },
+        [&] { issue_v_loads(P.raw, v + cur.base, row_stride, cur.nc, t); },
+        [&] {
+          have_next = find(cur.item + gridDim.x, nxt);
+          if (have_next) next_bits = start(nxt);
+          return have_next;
+        });
+    cur = nxt;
+    have = have_next;
+    bbits = next_bits;
   }
 }
 

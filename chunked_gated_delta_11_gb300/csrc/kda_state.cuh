@@ -39,8 +39,7 @@ __device__ __forceinline__ uint32_t d1_col(int c) { return TM_D1 + 32u * static_
 template <int NST>
 struct StateCtl {
   uint64_t full[NST];
-  uint64_t empty[NST];    // record fully consumed (its MMAs are done)
-  uint64_t rawfree[NST];  // its W and U areas are consumed (MMA1 and the errors are done)
+  uint64_t empty[NST];  // record fully consumed (its MMAs are done)
   uint64_t mma1, mma1b, mma2;  // MMA1 k-steps over channels 0-63, then 64-127; MMA2/3
   uint32_t tmem;
   int abort;
@@ -139,18 +138,14 @@ __device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uin
 
 // The state threads' work for all chunks, then the final state.  Thread v = 0
 // also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
-// REC_STRIDE_SMEM).  On thread 0, `wu_free(c, s)` runs once MMA1 of record c
-// and every read of its U and dlast are done (its W and U areas may be
-// reused), and `stage_free(c, s)` once all of its MMAs are done.  `ostage` is
-// 4 KB of shared memory (1 KB per state warp) used to turn each warp's 16 x 32
-// output tile into 16-byte stores.
-template <int NST, class WUFree, class StageFree>
+// REC_STRIDE_SMEM).  On thread 0, `stage_free(c, s)` runs once all MMAs of
+// record c are done and every state thread has finished reading it.
+template <int NST, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ final_dst, int* err,
-                                           uint8_t* ostage, WUFree&& wu_free,
                                            StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
@@ -221,11 +216,17 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tc_fence_after();
       issue_mma23(c, smem_u32(st), tb, &ctl->mma2);
       ++n2;
-      wu_free(c, s);
     }
-    ok = wait_or_abort(&ctl->mma2, c & 1, ctl, err);
-    if (v == 0 && ok) {
+    ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma2, c & 1, ctl, err));
+    // outputs: D1[v][16 + i] = o[i][v], read while the tensor pipe is idle
+    // (MMA1 of chunk c+1 writes the other D1 buffer)
+    uint32_t o[16];
+    if (ok) {
       tc_fence_after();
+      tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
+      tmem_wait_ld();
+    }
+    if (v == 0 && ok) {
       stage_free(c, s);
       if (c + 1 < nchunks) {
         const int s1 = (c + 1) % NST;
@@ -239,29 +240,13 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      // outputs: D1[v][16 + i] = o[i][v] (MMA1 of chunk c+1 writes the other D1)
-      tc_fence_after();
-      uint32_t o[16];
-      tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
-      tmem_wait_ld();
+      // bf16 rows of 128 value channels: each warp store covers 64 contiguous bytes
       const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
       const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      // warp tile [16 tokens][32 channels] bf16 through shared memory
-      const int w = v >> 5, l = v & 31;
-      uint8_t* ost = ostage + w * 1024;
+      __nv_bfloat16* dst = out + (t0 * H + h) * kDim + v;
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<__nv_bfloat16*>(ost + i * 64 + l * 2) =
-            __float2bfloat16_rn(__uint_as_float(o[i]));
-      __syncwarp();
-#pragma unroll
-      for (int rep = 0; rep < 2; ++rep) {
-        const int p = l + 32 * rep, i = p >> 2, sub = p & 3;
-        if (i < nc)
-          *reinterpret_cast<uint4*>(out + ((t0 + i) * H + h) * kDim + w * 32 + sub * 8) =
-              *reinterpret_cast<const uint4*>(ost + i * 64 + sub * 16);
-      }
-      __syncwarp();
+        if (i < nc) dst[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
     }
   }
   ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&ctl->abort));

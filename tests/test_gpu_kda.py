@@ -140,7 +140,16 @@ def test_chunk_records_match_oracle_factors(lengths, H):
         r_ = np.concatenate(ref[key])
         mx = np.abs(g_ - r_).max() / np.abs(r_).max()
         fro = np.linalg.norm(g_ - r_) / np.linalg.norm(r_)
-        assert mx < 2e-3 and fro < 1e-3, f"{key}: max_rel {mx:.2e} fro {fro:.2e}"
+        tmax, tfro = RECORD_TOL.get(key, (2e-3, 1e-3))
+        assert mx < tmax and fro < tfro, f"{key}: max_rel {mx:.2e} fro {fro:.2e}"
+
+
+# W and Aqk come from products with bf16 operands and fp32 accumulation, the
+# chunk-kernel precision of FlashKDA ("FlashKDA v1: A Deep Dive", sec. 3): each
+# product term carries up to 2^-8 relative rounding, so they are held to the
+# output bounds (1e-2 of the largest entry, 5e-3 Frobenius).  U (split bf16
+# operands), Qdec and dlast (fp32) and Kend (bf16 high + low) stay at 2e-3 / 1e-3.
+RECORD_TOL = {"W": (1e-2, 5e-3), "Aqk": (1e-2, 5e-3)}
 
 
 # ---------------------------------------------------------------------------
