@@ -75,7 +75,7 @@ def load(build_if_missing: bool = False):
         lib.kda_device_status.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
-        lib.kda_selftest_tcgen05.argtypes = [P, P, ctypes.c_int, P, P]
+        lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]
         lib.kda_selftest_tcgen05.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -232,12 +232,11 @@ def kda_device_status(stream=None) -> int:
     return int(load().kda_device_status(_stream(stream)))
 
 
-def kda_selftest_tcgen05(kend_layout: int = 0, device="cuda"):
+def kda_selftest_tcgen05(device="cuda"):
     out1 = torch.zeros((128, 32), dtype=torch.float32, device=device)
     out2 = torch.zeros((128, 128), dtype=torch.float32, device=device)
     status = torch.zeros((1,), dtype=torch.int32, device=device)
-    rc = load().kda_selftest_tcgen05(_ptr(out1), _ptr(out2), int(kend_layout), _ptr(status),
-                                     _stream(None))
+    rc = load().kda_selftest_tcgen05(_ptr(out1), _ptr(out2), _ptr(status), _stream(None))
     if rc != 0:
         raise KdaError(rc, "kda_selftest_tcgen05")
     torch.cuda.synchronize()

@@ -26,8 +26,8 @@
 // accumulation, as FlashKDA's chunk kernel does ("FlashKDA v1: A Deep Dive",
 // sec. 3).  U keeps A diag(beta) as a bf16 high part plus remainder (two
 // products) because its rounding would go straight into the state.  The
-// inverse runs in fp32.  W and Qdec are stored as fp32 (the recurrence reads
-// their tf32 part), U as fp32, Kend and Aqk as bf16 high/low pairs.
+// inverse runs in fp32 (tf32 tensor-core products with high/low operand
+// splits).  The record holds fp32 values; the recurrence reads their tf32 part.
 //
 // Raw input tiles (q, k, v, g_raw: 16 rows of 128 bf16, 4 KB each, in that
 // order) live in a 16 KB shared buffer of the caller, rows of 256 bytes whose
@@ -155,59 +155,74 @@ __device__ __forceinline__ void issue_v_loads(uint8_t* raw, const __nv_bfloat16*
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Order of the 136 lower-triangle entries (i >= j) by decreasing i - j, so that
-// the threads of one warp get similar loop lengths in the triangular products.
-struct EntryTable {
-  uint8_t ij[136];
-};
-__host__ __device__ constexpr EntryTable make_entry_table() {
-  EntryTable t{};
-  int e = 0;
-  for (int dl = 15; dl >= 0; --dl)
-    for (int j = 0; j + dl < 16; ++j) t.ij[e++] = static_cast<uint8_t>(((j + dl) << 4) | j);
-  return t;
+// x = high + low, both tf32: the three-product split keeps ~21 mantissa bits
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_bits(x);
+  lo = tf32_bits(x - __uint_as_float(hi));
 }
-__constant__ EntryTable kEntries = make_entry_table();
+__device__ __forceinline__ void mma1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
-// Entry (i, j), i >= j, of B + X Y for 16 x 16 lower-triangular X, Y whose
-// never-written triangles hold zeros: a dense 16-term dot product of row i of
-// X with column j of Y (read as row j of Y^T), all loads issued up front.
-__device__ __forceinline__ float tri_dot(const float (*X)[20], const float (*YT)[20],
-                                         const float (*B)[20], int i, int j) {
-  const float4* xr = reinterpret_cast<const float4*>(X[i]);
-  const float4* yr = reinterpret_cast<const float4*>(YT[j]);
-  float4 x[4], y[4];
+// Columns 8 nt .. 8 nt + 7 of C = B + X Y for 16 x 16 fp32 matrices in shared
+// memory (B may be null; Y is given transposed), by one warp: two k-steps of
+// tf32 tensor-core products, each operand split into a tf32 high part and a
+// tf32 remainder (high*high + high*low + low*high), fp32 accumulation.
+// Lane (g = l / 4, q = l % 4) gets C[g][8nt+2q], C[g][8nt+2q+1],
+// C[g+8][8nt+2q], C[g+8][8nt+2q+1] in c[0..3].
+__device__ __forceinline__ void tile_product(const float (*X)[20], const float (*YT)[20],
+                                             const float (*B)[20], int nt, int l,
+                                             float (&c)[4]) {
+  const int g = l >> 2, q = l & 3, j = nt * 8 + 2 * q;
+  float acc[2][4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    x[q] = xr[q];
-    y[q] = yr[q];
-  }
-  float a0 = B ? B[i][j] : 0.f, a1 = 0.f;
+  for (int e = 0; e < 4; ++e) acc[1][e] = 0.f;
+  if (B) {
+    const float2 b0 = *reinterpret_cast<const float2*>(&B[g][j]);
+    const float2 b1 = *reinterpret_cast<const float2*>(&B[g + 8][j]);
+    acc[0][0] = b0.x;
+    acc[0][1] = b0.y;
+    acc[0][2] = b1.x;
+    acc[0][3] = b1.y;
+  } else {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    a0 = fmaf(x[q].x, y[q].x, a0);
-    a1 = fmaf(x[q].y, y[q].y, a1);
-    a0 = fmaf(x[q].z, y[q].z, a0);
-    a1 = fmaf(x[q].w, y[q].w, a1);
+    for (int e = 0; e < 4; ++e) acc[0][e] = 0.f;
   }
-  return a0 + a1;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const int k = kk * 8 + q;
+    const float av[4] = {X[g][k], X[g + 8][k], X[g][k + 4], X[g + 8][k + 4]};
+    const float bv[2] = {YT[nt * 8 + g][k], YT[nt * 8 + g][k + 4]};
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_tf32(av[e], ah[e], al[e]);
+    split_tf32(bv[0], bh[0], bl[0]);
+    split_tf32(bv[1], bh[1], bl[1]);
+    mma1688(acc[kk], al, bh[0], bh[1]);
+    mma1688(acc[kk], ah, bl[0], bl[1]);
+    mma1688(acc[kk], ah, bh[0], bh[1]);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e];
 }
-// Thread t of 128 computes entry e1 = kEntries[t] and, on lanes 0 and 1 of
-// each warp, e2 = kEntries[128 + 2 (t / 32) + lane] (packed (i << 4) | j,
-// loaded once per chunk), so the eight extra entries are spread over the warps.
-__device__ __forceinline__ bool has_second_entry(int t) { return (t & 31) < 2; }
-__device__ __forceinline__ int second_entry_index(int t) { return 128 + (t >> 5) * 2 + (t & 31); }
-// C = B + X Y (B may be null), written to Cm and, if CT, transposed to CT.
-__device__ __forceinline__ void tri_product(const float (*X)[20], const float (*YT)[20],
-                                            const float (*B)[20], float (*Cm)[20],
-                                            float (*CT)[20], int e1, int e2, int t) {
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    if (r == 1 && !has_second_entry(t)) break;
-    const int e = r ? e2 : e1, i = e >> 4, j = e & 15;
-    const float c = tri_dot(X, YT, B, i, j);
-    Cm[i][j] = c;
-    if (CT) CT[j][i] = c;
+// Store a tile_product result: rows of Cm and, if CT, the transpose.
+__device__ __forceinline__ void store_tile(float (*Cm)[20], float (*CT)[20], int nt, int l,
+                                           const float (&c)[4]) {
+  const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
+  if (Cm) {
+    *reinterpret_cast<float2*>(&Cm[g][j]) = make_float2(c[0], c[1]);
+    *reinterpret_cast<float2*>(&Cm[g + 8][j]) = make_float2(c[2], c[3]);
+  }
+  if (CT) {
+    CT[j][g] = c[0];
+    CT[j + 1][g] = c[1];
+    CT[j][g + 8] = c[2];
+    CT[j + 1][g + 8] = c[3];
   }
 }
 
@@ -316,7 +331,8 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
     const float rqv[8] = {rq0.x, rq0.y, rq0.z, rq0.w, rq1.x, rq1.y, rq1.z, rq1.w};
     const float rkv[8] = {rk0.x, rk0.y, rk0.z, rk0.w, rk1.x, rk1.y, rk1.z, rk1.w};
     // packed bf16 words, [token pair m] for channel d0 (x) and d0+1 (y)
-    uint32_t qx[4], qy[4], kx[4], ky[4], ix[4], iy[4], ehx[4], ehy[4], elx[4], ely[4];
+    uint32_t qx[4], qy[4], kx[4], ky[4], ix[4], iy[4];
+    float ex[8], ey[8];  // Kend of channels d0, d0 + 1
     float2 sfx = post;  // prod over the tokens after the one being processed
 #pragma unroll
     for (int m = 3; m >= 0; --m) {
@@ -343,8 +359,10 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
       ky[m] = pack_bf16(Kd[0].y, Kd[1].y);
       ix[m] = pack_bf16(Ki[0].x, Ki[1].x);
       iy[m] = pack_bf16(Ki[0].y, Ki[1].y);
-      split_pair2(Ke[0].x, Ke[1].x, ehx[m], elx[m]);
-      split_pair2(Ke[0].y, Ke[1].y, ehy[m], ely[m]);
+      ex[2 * m] = Ke[0].x;
+      ex[2 * m + 1] = Ke[1].x;
+      ey[2 * m] = Ke[0].y;
+      ey[2 * m + 1] = Ke[1].y;
     }
     const int ox = drv_off(d0, hf), oy = drv_off(d0 + 1, hf);
     *reinterpret_cast<uint4*>(S.qd + ox) = make_uint4(qx[0], qx[1], qx[2], qx[3]);
@@ -353,12 +371,12 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
     *reinterpret_cast<uint4*>(S.kd + oy) = make_uint4(ky[0], ky[1], ky[2], ky[3]);
     *reinterpret_cast<uint4*>(S.ki + ox) = make_uint4(ix[0], ix[1], ix[2], ix[3]);
     *reinterpret_cast<uint4*>(S.ki + oy) = make_uint4(iy[0], iy[1], iy[2], iy[3]);
-    const int kex = kend_offset(KDA_KEND_LAYOUT, d0, hf * 8);
-    const int key = kend_offset(KDA_KEND_LAYOUT, d0 + 1, hf * 8);
-    *reinterpret_cast<uint4*>(rec + OFF_KH + kex) = make_uint4(ehx[0], ehx[1], ehx[2], ehx[3]);
-    *reinterpret_cast<uint4*>(rec + OFF_KH + key) = make_uint4(ehy[0], ehy[1], ehy[2], ehy[3]);
-    *reinterpret_cast<uint4*>(rec + OFF_KL + kex) = make_uint4(elx[0], elx[1], elx[2], elx[3]);
-    *reinterpret_cast<uint4*>(rec + OFF_KL + key) = make_uint4(ely[0], ely[1], ely[2], ely[3]);
+    // Kend: this half's 8 tokens are one K=8 tile row, two 16-byte pieces
+    uint8_t* ke = rec + OFF_KEND;
+    *reinterpret_cast<float4*>(ke + kend_offset(d0, hf * 8)) = make_float4(ex[0], ex[1], ex[2], ex[3]);
+    *reinterpret_cast<float4*>(ke + kend_offset(d0, hf * 8 + 4)) = make_float4(ex[4], ex[5], ex[6], ex[7]);
+    *reinterpret_cast<float4*>(ke + kend_offset(d0 + 1, hf * 8)) = make_float4(ey[0], ey[1], ey[2], ey[3]);
+    *reinterpret_cast<float4*>(ke + kend_offset(d0 + 1, hf * 8 + 4)) = make_float4(ey[4], ey[5], ey[6], ey[7]);
   }
   chunk_sync();
   // q, k and g_raw of this chunk are no longer read
@@ -392,35 +410,52 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
           S.P0[i][j] = -r;
         }
       } else {
-        __nv_bfloat16 ah, al;
-        split_bf16(j <= i ? acc[e] : 0.f, ah, al);
-        *reinterpret_cast<__nv_bfloat16*>(rec + OFF_AQK + aqk_offset(i, j)) = ah;
-        *reinterpret_cast<__nv_bfloat16*>(rec + OFF_AQK + 512 + aqk_offset(i, j)) = al;
+        *reinterpret_cast<float*>(rec + OFF_AQK + aqk_offset(i, j)) = j <= i ? acc[e] : 0.f;
       }
     }
   }
   chunk_sync();
 
-  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent steps; the
-  // last one writes A diag(beta) as bf16 high / low ----
+  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent levels of
+  // tensor-core tile products (warp w: tile w & 1 of product w >> 1); the last
+  // level writes A diag(beta) as bf16 high / low ----
   {
-    const int e1 = kEntries.ij[t], e2 = has_second_entry(t) ? kEntries.ij[second_entry_index(t)] : 0;
-    tri_product(S.Rr, S.RT, nullptr, S.R2r, S.R2T, e1, e2, t);   // R^2
+    const int nt = w & 1;
+    float c[4];
+    if (w < 2) {  // R^2
+      tile_product(S.Rr, S.RT, nullptr, nt, l, c);
+      store_tile(S.R2r, S.R2T, nt, l, c);
+    }
     chunk_sync();
-    tri_product(S.P0, S.R2T, S.P0, S.P1, nullptr, e1, e2, t);    // P1 = (I-R)(I+R^2)
-    tri_product(S.R2r, S.R2T, nullptr, S.Rr, S.R4T, e1, e2, t);  // R^4 (rows into Rr)
+    if (w < 2) {  // P1 = (I-R)(I+R^2)
+      tile_product(S.P0, S.R2T, S.P0, nt, l, c);
+      store_tile(S.P1, nullptr, nt, l, c);
+    } else {      // R^4 (rows into Rr)
+      tile_product(S.R2r, S.R2T, nullptr, nt, l, c);
+      store_tile(S.Rr, S.R4T, nt, l, c);
+    }
     chunk_sync();
-    tri_product(S.P1, S.R4T, S.P1, S.P0, nullptr, e1, e2, t);    // P2 = P1 (I+R^4)
-    tri_product(S.Rr, S.R4T, nullptr, S.R2r, S.RT, e1, e2, t);   // R^8 (only R8^T kept)
+    if (w < 2) {  // P2 = P1 (I+R^4)
+      tile_product(S.P1, S.R4T, S.P1, nt, l, c);
+      store_tile(S.P0, nullptr, nt, l, c);
+    } else {      // R^8 (only its transpose is kept)
+      tile_product(S.Rr, S.R4T, nullptr, nt, l, c);
+      store_tile(nullptr, S.RT, nt, l, c);
+    }
     chunk_sync();
+    if (w < 2) {  // A = P2 (I+R^8), times diag(beta)
+      tile_product(S.P0, S.RT, S.P0, nt, l, c);
+      const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
+      const float b0 = S.beta[j], b1 = S.beta[j + 1];
+      const float ab[4] = {c[0] * b0, c[1] * b1, c[2] * b0, c[3] * b1};
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {                                // A = P2 (I+R^8)
-      if (r == 1 && !has_second_entry(t)) break;
-      const int e = r ? e2 : e1, i = e >> 4, j = e & 15;
-      __nv_bfloat16 hi, lo;
-      split_bf16(tri_dot(S.P0, S.RT, S.P0, i, j) * S.beta[j], hi, lo);
-      S.abh[i * AS + j] = hi;
-      S.abl[i * AS + j] = lo;
+      for (int e = 0; e < 4; ++e) {
+        const int i = g + (e >> 1) * 8, jj = j + (e & 1);
+        __nv_bfloat16 hi, lo;
+        split_bf16(ab[e], hi, lo);
+        S.abh[i * AS + jj] = hi;
+        S.abl[i * AS + jj] = lo;
+      }
     }
   }
   // this chunk's v tile (the older of at most two pending groups)

@@ -11,18 +11,18 @@
 //   S'   = S_c Diag(dlast) + E Kend    (state fast-forward, sec. 6.4)
 //
 // Byte layout of one record (REC_BYTES):
-//   [OFF_B1,  +16384)  [W ; Qdec], 32 rows x 128 key channels, fp32 rounded to
-//                      tf32, K-major with the 128-byte swizzle: 4 blocks of 32
-//                      channels, each 32 rows x 128 B; row n of block kb at
-//                      kb*4096 + n*128, its 16-byte piece c at (c ^ (n & 7))*16.
+//   [OFF_B1,  +16384)  [W ; Qdec], 32 rows x 128 key channels, fp32 (the
+//                      tensor core reads its tf32 part), K-major with the
+//                      128-byte swizzle: 4 blocks of 32 channels, each 32 rows
+//                      x 128 B; row n of block kb at kb*4096 + n*128, its
+//                      16-byte piece c at (c ^ (n & 7))*16.
 //                      Rows 0..15 are W, rows 16..31 are Qdec.
-//   [OFF_KH,  +4096)   Kend high part (bf16), MMA operand indexed [d][j]:
-//   [OFF_KL,  +4096)   Kend low part (bf16) = bf16(Kend - high); same layout.
+//   [OFF_KEND, +8192)  Kend fp32 [128 d][16 j] as two K=8 tiles (j 0-7, j 8-15,
+//                      4 KB each), K-major with the 32-byte swizzle: row d at
+//                      d*32, 16-byte piece p at (p ^ ((d >> 2) & 1))*16.
 //   [OFF_U,   +8192)   U^T fp32 [128 value channels][16 tokens].
-//   [OFF_AQK, +512)    Aqk high part (bf16) [16 rows i][16 j] (chi_ij for j <= i,
-//                      zero above), K-major with the 32-byte swizzle: row i at
-//                      i*32, 16-byte piece p at (p ^ ((i >> 2) & 1))*16.
-//   [OFF_AQK+512,+512) Aqk low part (bf16) = bf16(Aqk - high); same layout.
+//   [OFF_AQK, +1024)   Aqk fp32 [16 i][16 j] (chi_ij for j <= i, zero above) as
+//                      two K=8 tiles of 512 B, same 32-byte swizzle (row i).
 //   [OFF_DL,  +512)    dlast fp32 [128] = diagonal of D_{0:C-1}.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
@@ -37,21 +37,12 @@ constexpr int kChunk = 16;
 constexpr int kDim = 128;
 
 constexpr int OFF_B1 = 0;
-constexpr int OFF_KH = 16384;
-constexpr int OFF_KL = 20480;
+constexpr int OFF_KEND = 16384;
 constexpr int OFF_U = 24576;
 constexpr int OFF_AQK = 32768;
 constexpr int OFF_DL = 33792;
 constexpr int REC_BYTES = 34304;
 constexpr int REC_STRIDE_SMEM = 34816;  // 1024-aligned stage stride in smem
-
-// Layout of the Kend tiles (MMA2 B operand, 128 rows d x 16 tokens j, bf16,
-// K-major).  0: 32-byte swizzle (row d at d*32, 16-byte piece p at
-// (p ^ ((d >> 2) & 1))*16).  1: no swizzle, 8x16-byte core matrices with
-// the K-direction core stride 128 B and the row-group stride 256 B.
-#ifndef KDA_KEND_LAYOUT
-#define KDA_KEND_LAYOUT 0
-#endif
 
 __host__ __device__ constexpr int b1_offset(int n, int d) {
   // fp32 element (row n, channel d) of the [W ; Qdec] tile
@@ -59,16 +50,14 @@ __host__ __device__ constexpr int b1_offset(int n, int d) {
          ((d & 3) << 2);
 }
 
-__host__ __device__ constexpr int aqk_offset(int i, int j) {
-  // byte offset of bf16 element (i, j) inside one 512-byte Aqk tile
-  return i * 32 + ((((j >> 3) ^ (i >> 2)) & 1) << 4) + ((j & 7) << 1);
+// Byte offset of fp32 element (r, j), j < 16, in a pair of K=8 tiles with the
+// 32-byte swizzle (tile stride `tile`): the Kend tiles (r = d, tile 4096) and
+// the Aqk tiles (r = i, tile 512).
+__host__ __device__ constexpr int sw32_offset(int r, int j, int tile) {
+  return (j >> 3) * tile + r * 32 + (((((j & 7) >> 2) ^ (r >> 2)) & 1) << 4) + ((j & 3) << 2);
 }
-
-__host__ __device__ constexpr int kend_offset(int layout, int d, int j) {
-  // byte offset of bf16 element (d, j) inside one 4096-byte Kend tile
-  return layout == 0 ? d * 32 + ((((j >> 3) ^ (d >> 2)) & 1) << 4) + ((j & 7) << 1)
-                     : (d >> 3) * 256 + (j >> 3) * 128 + ((d & 7) << 4) + ((j & 7) << 1);
-}
+__host__ __device__ constexpr int kend_offset(int d, int j) { return sw32_offset(d, j, 4096); }
+__host__ __device__ constexpr int aqk_offset(int i, int j) { return sw32_offset(i, j, 512); }
 
 // ---------------------------------------------------------------------------
 // small PTX wrappers
@@ -107,11 +96,11 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
   return rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * x));
 }
 
-// fp32 -> tf32 (round to nearest, ties away), kept in an fp32 container
-__device__ __forceinline__ float to_tf32(float x) {
+// fp32 -> tf32 bits (round to nearest, ties away), in an fp32 container
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -129,26 +118,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return r;
 }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
-
-// (x0, x1) -> packed bf16 pair of high parts and packed pair of remainders
-__device__ __forceinline__ void split_pair2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const float2 d = sub2(make_float2(x0, x1), hf);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(d.x, d.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
@@ -261,17 +230,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D (tmem, fp32) (+)= A (tmem) * B (smem descriptor); A/B bf16, one K=16 step.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -24,10 +24,21 @@ namespace kda {
 
 constexpr int F_NST = 2;
 constexpr int F_THREADS = 256;
+// Registers per thread: the kernel is compiled for 128 (two CTAs of 256
+// threads per SM); after the prologue the state warpgroup takes 152 and the
+// chunk warpgroup 104 (setmaxnreg), 128 x 152 + 128 x 104 = 256 x 128, so the
+// increase is always covered by the decrease.  launch_fused checks the
+// compiled count before the first launch.
+constexpr int F_REGS = 128, F_STATE_REGS = 152, F_CHUNK_REGS = 104;
+static_assert(128 * F_STATE_REGS + 128 * F_CHUNK_REGS == F_THREADS * F_REGS,
+              "register split must add up to the launch allocation");
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
 constexpr int F_RAW_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
-constexpr int F_CTL_OFF = F_RAW_OFF + RAW_BYTES;
+constexpr int F_OST_OFF = F_RAW_OFF + RAW_BYTES;
+constexpr int F_CTL_OFF = F_OST_OFF + 4096;
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
+// two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+static_assert(2 * (F_SMEM + 1024) <= 228 * 1024, "fused kernel must fit two CTAs per SM");
 
 // AND of `pred` over the 128 chunk threads (named barrier 1).
 __device__ __forceinline__ bool chunk_all(bool pred) {
@@ -90,6 +101,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   tc_fence_after();
 
   if (w >= 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_CHUNK_REGS));
     // ---------------- chunk threads ----------------
     // Raw tiles have their own buffer: q, k, g_raw of chunk c+1 load once the
     // gate phase of chunk c is done with them, v of chunk c at the start of
@@ -143,11 +155,12 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_STATE_REGS));
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err, release);
+               err, smem + F_OST_OFF, release);
   }
   tc_fence_before();
   __syncthreads();
@@ -160,8 +173,12 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
                          void* out, float* final_state, int* err, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+    // the register split above is only safe if every thread starts with F_REGS
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != F_REGS) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }

@@ -13,7 +13,8 @@ namespace kda {
 
 constexpr int K2_NST = 3;
 constexpr int K2_THREADS = 128;
-constexpr int K2_CTL_OFF = K2_NST * REC_STRIDE_SMEM;
+constexpr int K2_OST_OFF = K2_NST * REC_STRIDE_SMEM;
+constexpr int K2_CTL_OFF = K2_OST_OFF + 4096;
 constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 1024 + 64;
 
 __global__ void __launch_bounds__(K2_THREADS, 2)
@@ -81,7 +82,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   };
   state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
              final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-             err, refill);
+             err, smem + K2_OST_OFF, refill);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory
     for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)

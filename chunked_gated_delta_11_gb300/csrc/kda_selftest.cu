@@ -5,12 +5,13 @@
 //   MMA1-like: D1[128 x 32]  = A1[128 x 128] (tf32, tensor memory)
 //                             * B1^T (fp32 [32 x 128] in the record's 128-byte
 //                               swizzled K-major layout), 16 K=8 steps.
-//   MMA2-like: D2[128 x 128] = D0 + A2[128 x 16] (bf16 pairs in tensor memory)
-//                             * B2^T (bf16 [128 x 16] in the Kend layout chosen
-//                               by `kend_layout`), one K=16 step, accumulating.
+//   MMA2-like: D2[128 x 128] = D0 + A2[128 x 16] (tf32, tensor memory)
+//                             * B2^T (fp32 [128 x 16] in the record's Kend
+//                               layout: two 32-byte-swizzled K=8 tiles), two
+//                               K=8 steps accumulating onto a preset D.
 //
-// Every smem address the descriptors can form stays inside the 20 KB tile
-// area whatever the layout, so a wrong convention gives wrong numbers only.
+// Every smem address the descriptors can form stays inside the 24 KB tile
+// area, so a wrong convention gives wrong numbers only.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -22,14 +23,14 @@ __host__ __device__ inline float st_b2(int d, int j) { return ((d * 5 + j * 11) 
 __host__ __device__ inline float st_d0(int m, int d) { return (m - d) * 0.0625f; }
 
 __global__ void __launch_bounds__(128, 1)
-selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int kend_layout,
+selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
                         int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* b1 = smem;                       // 16 KB, record OFF_B1 layout
-  uint8_t* b2 = smem + 16384;               // 4 KB, Kend layout
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 20480);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 20488);
+  uint8_t* b2 = smem + 16384;               // 8 KB, Kend layout
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 24576);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 24584);
   const int t = threadIdx.x, w = t >> 5;
 
   for (int e = t; e < 32 * 128; e += 128) {
@@ -38,8 +39,7 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int 
   }
   for (int e = t; e < 128 * 16; e += 128) {
     const int d = e >> 4, j = e & 15;
-    *reinterpret_cast<__nv_bfloat16*>(b2 + kend_offset(kend_layout, d, j)) =
-        __float2bfloat16_rn(st_b2(d, j));
+    *reinterpret_cast<float*>(b2 + kend_offset(d, j)) = st_b2(d, j);
   }
   if (t == 0) {
     mbar_init(bar, 1);
@@ -59,7 +59,7 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int 
   const uint32_t lane_off = static_cast<uint32_t>(w * 32) << 16;
   const int m = t;
 
-  // A1 row m (fp32), D0 row m, A2 row m (bf16 pairs, low half = even k)
+  // A1 row m, D0 row m, A2 row m (fp32)
   for (int q = 0; q < 4; ++q) {
     uint32_t r[32];
     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(st_a1(m, q * 32 + i));
@@ -69,8 +69,7 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int 
   }
   {
     uint32_t r[16];
-    for (int c = 0; c < 8; ++c) r[c] = pack_bf16(st_a2(m, 2 * c), st_a2(m, 2 * c + 1));
-    for (int c = 8; c < 16; ++c) r[c] = 0u;
+    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(st_a2(m, j));
     tmem_st16(A2 + lane_off, r);
   }
   tmem_wait_st();
@@ -85,10 +84,9 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int 
       const uint64_t bd = make_sdesc(b1a + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
       mma_tf32_ts(D1, A1 + kk * 8, bd, id1, kk > 0);
     }
-    const uint32_t id2 = make_idesc(1, 128, 128);
-    const uint64_t bd2 = kend_layout == 0 ? make_sdesc(smem_u32(b2), 16, 256, 6)
-                                          : make_sdesc(smem_u32(b2), 128, 256, 0);
-    mma_bf16_ts(D2, A2, bd2, id2, 1);
+    const uint32_t id2 = make_idesc(2, 128, 128);
+    for (int kk = 0; kk < 2; ++kk)
+      mma_tf32_ts(D2, A2 + kk * 8, make_sdesc(smem_u32(b2) + kk * 4096, 16, 256, 6), id2, 1);
     tc_commit(bar);
   }
   __syncwarp();
@@ -113,11 +111,10 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2, int 
 
 }  // namespace kda
 
-extern "C" int kda_selftest_tcgen05(float* out1, float* out2, int kend_layout, int* status,
-                                    void* stream) {
-  if (!out1 || !out2 || !status || (kend_layout != 0 && kend_layout != 1)) return 1;
-  const int smem = 20480 + 64 + 1024;
+extern "C" int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream) {
+  if (!out1 || !out2 || !status) return 1;
+  const int smem = 24576 + 64 + 1024;
   kda::selftest_tcgen05_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
-      out1, out2, kend_layout, status);
+      out1, out2, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

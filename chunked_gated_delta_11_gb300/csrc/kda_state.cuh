@@ -12,12 +12,12 @@
 //   state threads (thread v = row v):
 //        S[v][:] *= dlast                                  (forget, sec. 6.4)
 //        e[v][i] = U[i][v] - D1[v][i]                       (corrected errors)
-//        E^T -> tensor memory as bf16 high part + bf16 remainder
-//   MMA2 (tcgen05 kind::f16 bf16, M=128 N=128 K=16, three instructions):
-//        S += E^T_hi Kend_hi + E^T_lo Kend_hi + E^T_hi Kend_lo   (write, sec. 6.4)
-//   MMA3 (kind::f16 bf16, M=128 N=16 K=16, three instructions):
+//        E^T -> tensor memory (fp32 rounded to tf32)
+//   MMA2 (tcgen05 kind::tf32, M=128 N=128 K=16, two instructions):
+//        S += E^T Kend                                      (write, sec. 6.4)
+//   MMA3 (kind::tf32, M=128 N=16 K=16, two instructions):
 //        D1[v][16+i] += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v]     (read, sec. 6.5)
-//   state threads, while MMA1 of chunk c+1 runs: o -> bf16 -> out.
+//   state threads: o -> bf16 -> out.
 //
 // MMA1 takes the fp32 state as its A operand directly (the tensor core reads its
 // tf32 part), so no operand copy of S is kept.  D1 alternates between two
@@ -32,7 +32,7 @@
 
 namespace kda {
 
-constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_A2H = 192, TM_A2L = 200, TM_COLS = 256;
+constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_E = 192, TM_COLS = 256;
 // D1 of chunk c: columns TM_D1 + 32 * (c & 1) .. + 31
 __device__ __forceinline__ uint32_t d1_col(int c) { return TM_D1 + 32u * static_cast<uint32_t>(c & 1); }
 
@@ -75,13 +75,8 @@ __device__ __forceinline__ bool state_all(bool pred) {
   return r != 0;
 }
 
-__device__ __forceinline__ uint64_t kend_desc(uint32_t saddr) {
-#if KDA_KEND_LAYOUT == 0
-  return make_sdesc(saddr, 16, 256, 6);
-#else
-  return make_sdesc(saddr, 128, 256, 0);
-#endif
-}
+// descriptor of a K=8 tf32 tile with the 32-byte swizzle (rows of 32 bytes)
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) { return make_sdesc(saddr, 16, 256, 6); }
 
 // Initial state (or zeros) -> tensor memory.  State threads only (t < 128).
 __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
@@ -120,19 +115,17 @@ __device__ __forceinline__ void issue_mma1(int c, uint32_t sb, uint32_t tb, uint
   tc_commit(bar_b);
 }
 
-// MMA2 (state update) and MMA3 (output correction) of chunk c.  Issuing thread only.
+// MMA2 (state update) and MMA3 (output correction) of chunk c, two K=8 tf32
+// steps each.  Issuing thread only.
 __device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uint64_t* bar) {
-  const uint32_t id2 = make_idesc(1, 128, 128), id3 = make_idesc(1, 128, 16);
+  const uint32_t id2 = make_idesc(2, 128, 128), id3 = make_idesc(2, 128, 16);
   const uint32_t d1 = tb + d1_col(c);
-  const uint64_t kh = kend_desc(sb + OFF_KH), kl = kend_desc(sb + OFF_KL);
-  mma_bf16_ts(tb + TM_S, tb + TM_A2H, kh, id2, 1u);
-  mma_bf16_ts(tb + TM_S, tb + TM_A2L, kh, id2, 1u);
-  mma_bf16_ts(tb + TM_S, tb + TM_A2H, kl, id2, 1u);
-  const uint64_t ah = make_sdesc(sb + OFF_AQK, 16, 256, 6),
-                 al = make_sdesc(sb + OFF_AQK + 512, 16, 256, 6);
-  mma_bf16_ts(d1 + 16, tb + TM_A2H, ah, id3, 1u);
-  mma_bf16_ts(d1 + 16, tb + TM_A2L, ah, id3, 1u);
-  mma_bf16_ts(d1 + 16, tb + TM_A2H, al, id3, 1u);
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+    mma_tf32_ts(tb + TM_S, tb + TM_E + kk * 8, sw32_desc(sb + OFF_KEND + kk * 4096), id2, 1u);
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+    mma_tf32_ts(d1 + 16, tb + TM_E + kk * 8, sw32_desc(sb + OFF_AQK + kk * 512), id3, 1u);
   tc_commit(bar);
 }
 
@@ -140,13 +133,15 @@ __device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uin
 // also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
 // REC_STRIDE_SMEM).  On thread 0, `stage_free(c, s)` runs once all MMAs of
 // record c are done and every state thread has finished reading it.
+// `ostage` is 4 KB of shared memory (1 KB per state warp) that turns each
+// warp's 16 x 32 output tile into 16-byte stores.
 template <int NST, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out,
                                            float* __restrict__ final_dst, int* err,
-                                           StageFree&& stage_free) {
+                                           uint8_t* ostage, StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   if (v == 0 && nchunks > 0) {
@@ -198,14 +193,12 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4) {
           const float4 u = U4[i4];
-          const float e0 = u.x - __uint_as_float(d1[i4 * 4 + 0]);
-          const float e1 = u.y - __uint_as_float(d1[i4 * 4 + 1]);
-          const float e2 = u.z - __uint_as_float(d1[i4 * 4 + 2]);
-          const float e3 = u.w - __uint_as_float(d1[i4 * 4 + 3]);
-          split_pair2(e0, e1, pk[2 * i4], pk[8 + 2 * i4]);
-          split_pair2(e2, e3, pk[2 * i4 + 1], pk[8 + 2 * i4 + 1]);
+          pk[i4 * 4 + 0] = tf32_bits(u.x - __uint_as_float(d1[i4 * 4 + 0]));
+          pk[i4 * 4 + 1] = tf32_bits(u.y - __uint_as_float(d1[i4 * 4 + 1]));
+          pk[i4 * 4 + 2] = tf32_bits(u.z - __uint_as_float(d1[i4 * 4 + 2]));
+          pk[i4 * 4 + 3] = tf32_bits(u.w - __uint_as_float(d1[i4 * 4 + 3]));
         }
-        tmem_st16(tb + TM_A2H + lane_off, pk);
+        tmem_st16(tb + TM_E + lane_off, pk);
         tmem_wait_st();
         tc_fence_before();
       }
@@ -240,13 +233,30 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
-      // bf16 rows of 128 value channels: each warp store covers 64 contiguous bytes
+      // warp tile [16 tokens][32 channels] bf16 through shared memory, then
+      // 16-byte stores (each row of the tile is 64 contiguous bytes of `out`)
       const int64_t t0 = bos + static_cast<int64_t>(c) * kChunk;
       const int nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      __nv_bfloat16* dst = out + (t0 * H + h) * kDim + v;
+      const int w = v >> 5, l = v & 31;
+      uint8_t* ost = ostage + w * 1024;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (i < nc) dst[static_cast<int64_t>(i) * H * kDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
+      for (int i = 0; i < 16; i += 2) {
+        // tokens i, i+1 of channel v: two bf16 in one 4-byte store would
+        // stride rows, so keep one bf16 per store (conflict-free, 64 B rows)
+        *reinterpret_cast<__nv_bfloat16*>(ost + i * 64 + l * 2) =
+            __float2bfloat16_rn(__uint_as_float(o[i]));
+        *reinterpret_cast<__nv_bfloat16*>(ost + (i + 1) * 64 + l * 2) =
+            __float2bfloat16_rn(__uint_as_float(o[i + 1]));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int p = l + 32 * rep, i = p >> 2, sub = p & 3;
+        if (i < nc)
+          *reinterpret_cast<uint4*>(out + ((t0 + i) * H + h) * kDim + w * 32 + sub * 8) =
+              *reinterpret_cast<const uint4*>(ost + i * 64 + sub * 16);
+      }
+      __syncwarp();
     }
   }
   ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&ctl->abort));

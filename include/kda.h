@@ -128,9 +128,10 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const vo
  *   ((floor(bos_n / 16) + n + c) * H + h) * 34304
  * with bos_n the first token of sequence n, and holds, for the chunk's tokens
  * i < 16 (rows past the sequence end are zero), in this order:
- *   [W ; Qdec] fp32 (tf32-rounded) 32 x 128, 128-byte-swizzled K-major tiles;
- *   Kend as two bf16 tiles (high part, remainder), 128 x 16;
- *   U^T fp32 [128][16];  Aqk fp32 [16][16];  dlast fp32 [128];
+ *   [W ; Qdec] fp32 32 x 128, 128-byte-swizzled K-major tiles;
+ *   Kend fp32 [128][16], two 32-byte-swizzled K=8 tiles;
+ *   U^T fp32 [128][16];  Aqk fp32 [16][16], two 32-byte-swizzled K=8 tiles;
+ *   dlast fp32 [128];
  * where (sec. 6.1-6.6 of "You Could Have Come Up with Kimi Delta Attention")
  *   Qdec_i = scale q^_i D_{0:i},  Kend_i = k^_i D_{i+1:last},
  *   Akk = (I + R)^-1 with R_ij = beta_i <k^_j|D_{j+1:i}|k^_i> (j < i),
@@ -162,13 +163,13 @@ const char* kda_status_string(kda_status status);
 
 /* Diagnostic: one-CTA check of the tensor-core operand conventions used by
  * the recurrence kernel (tf32 MMA with A in tensor memory and a 128-byte
- * swizzled B tile; bf16 MMA with A in tensor memory and the Kend tile layout
- * `kend_layout` (0 or 1) accumulating into a preset D).  Writes
+ * swizzled B tile; tf32 MMA with A in tensor memory and the record's
+ * 32-byte-swizzled Kend tiles, accumulating into a preset D).  Writes
  * out1 fp32 [128][32] and out2 fp32 [128][128] (device), and 5 to *status
  * (device int) if its wait ran out.  Returns 0, 1 for bad arguments, 4 on a
  * launch error.  The expected values are closed-form small dyadic numbers
  * (see the kernel source), exact in fp32. */
-int kda_selftest_tcgen05(float* out1, float* out2, int kend_layout, int* status, void* stream);
+int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream);
 
 #ifdef __cplusplus
 }

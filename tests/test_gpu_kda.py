@@ -15,7 +15,6 @@ from kda_testlib import assert_close, compare_units, f64, oracle_case
 
 pytestmark = pytest.mark.gpu
 
-KEND_LAYOUT = 0  # the layout compiled into the recurrence kernel (KDA_KEND_LAYOUT)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,9 +61,8 @@ def _selftest_expected():
     return A1 @ B1.T, D0 + A2 @ B2.T
 
 
-@pytest.mark.parametrize("layout", [KEND_LAYOUT])
-def test_tcgen05_operand_conventions(layout):
-    out1, out2, status = kda.kda_selftest_tcgen05(layout)
+def test_tcgen05_operand_conventions():
+    out1, out2, status = kda.kda_selftest_tcgen05()
     assert status == 0
     e1, e2 = _selftest_expected()
     np.testing.assert_array_equal(out1.cpu().numpy(), e1.astype(np.float32))
@@ -78,10 +76,8 @@ def _b1_offset(n, d):
     return (d >> 5) * 4096 + n * 128 + ((((d & 31) >> 2) ^ (n & 7)) << 4) + ((d & 3) << 2)
 
 
-def _kend_offset(d, j):
-    if KEND_LAYOUT == 0:
-        return d * 32 + ((((j >> 3) ^ (d >> 2)) & 1) << 4) + ((j & 7) << 1)
-    return (d >> 3) * 256 + (j >> 3) * 128 + ((d & 7) << 4) + ((j & 7) << 1)
+def _sw32_offset(r, j, tile):
+    return (j >> 3) * tile + r * 32 + (((((j & 7) >> 2) ^ (r >> 2)) & 1) << 4) + ((j & 3) << 2)
 
 
 def decode_record(rec):
@@ -89,24 +85,13 @@ def decode_record(rec):
     nn, dd = np.meshgrid(np.arange(32), np.arange(128), indexing="ij")
     b1 = rec[:16384].view(np.float32)[(_b1_offset(nn, dd)) // 4]
     jj, dd2 = np.meshgrid(np.arange(16), np.arange(128), indexing="ij")
-    off = _kend_offset(dd2, jj)
-
-    def bf16_at(base):
-        raw = rec[base:base + 4096].view(np.uint16)[off // 2].astype(np.uint32) << 16
-        return raw.view(np.float32).astype(np.float64)
-
-    kend = bf16_at(16384) + bf16_at(20480)
+    kend = rec[16384:24576].view(np.float32)[_sw32_offset(dd2, jj, 4096) // 4]
     U = rec[24576:32768].view(np.float32).reshape(128, 16).T
     ii, jj2 = np.meshgrid(np.arange(16), np.arange(16), indexing="ij")
-    aoff = ii * 32 + ((((jj2 >> 3) ^ (ii >> 2)) & 1) << 4) + ((jj2 & 7) << 1)
-
-    def aqk_at(base):
-        raw = rec[base:base + 512].view(np.uint16)[aoff // 2].astype(np.uint32) << 16
-        return raw.view(np.float32).astype(np.float64)
-
-    Aqk = aqk_at(32768) + aqk_at(33280)
+    Aqk = rec[32768:33792].view(np.float32)[_sw32_offset(ii, jj2, 512) // 4]
     dl = rec[33792:34304].view(np.float32)
-    return {"W": b1[:16], "Qdec": b1[16:], "Kend": kend, "U": U, "Aqk": Aqk, "dlast": dl}
+    return {"W": b1[:16], "Qdec": b1[16:], "Kend": kend.astype(np.float64), "U": U,
+            "Aqk": Aqk.astype(np.float64), "dlast": dl}
 
 
 @pytest.mark.parametrize("lengths,H", [([64], 1), ([45], 2), ([7, 0, 33, 16], 2)])
@@ -148,7 +133,7 @@ def test_chunk_records_match_oracle_factors(lengths, H):
 # chunk-kernel precision of FlashKDA ("FlashKDA v1: A Deep Dive", sec. 3): each
 # product term carries up to 2^-8 relative rounding, so they are held to the
 # output bounds (1e-2 of the largest entry, 5e-3 Frobenius).  U (split bf16
-# operands), Qdec and dlast (fp32) and Kend (bf16 high + low) stay at 2e-3 / 1e-3.
+# operands), Qdec, Kend and dlast (fp32) stay at 2e-3 / 1e-3.
 RECORD_TOL = {"W": (1e-2, 5e-3), "Aqk": (1e-2, 5e-3)}
 
 
