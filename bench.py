@@ -4,9 +4,9 @@
 Default workload: B = 8 sequences x T = 8192 tokens, H = 32 heads, D = 128,
 bf16, lower_bound = -5, zero initial state (seeded synthetic inputs; see
 chunked_gated_delta_11_gb300/synth.py).  A step is one whole forward pass
-over that batch (default: kda_fwd, chunk kernel then recurrence kernel;
---path fused: kda_fwd_fused, one kernel), inputs resident in HBM.  Inputs
-(2.1 GB) are larger than the 129 MB L2, so no flush runs between steps.
+over that batch (default: kda_fwd_fused, one kernel; --path split: kda_fwd,
+chunk kernel then recurrence kernel), inputs resident in HBM.  Inputs (2.1 GB)
+are larger than the 129 MB L2, so no flush runs between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -215,7 +215,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b8")
-    ap.add_argument("--path", choices=["fused", "split"], default="split",
+    ap.add_argument("--path", choices=["fused", "split"], default="fused",
                     help="fused: kda_fwd_fused (one kernel); split: kda_fwd (K1 + K2)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=0,

@@ -28,7 +28,7 @@ __all__ = [
 
 CHUNK = 16
 HEAD_DIM = 128
-REC_BYTES = 34304
+REC_BYTES = 26112
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
           3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_LAUNCH", 5: "KDA_ERR_TIMEOUT"}
@@ -234,7 +234,7 @@ def kda_device_status(stream=None) -> int:
 
 def kda_selftest_tcgen05(device="cuda"):
     out1 = torch.zeros((128, 32), dtype=torch.float32, device=device)
-    out2 = torch.zeros((128, 128), dtype=torch.float32, device=device)
+    out2 = torch.zeros((128, 144), dtype=torch.float32, device=device)
     status = torch.zeros((1,), dtype=torch.int32, device=device)
     rc = load().kda_selftest_tcgen05(_ptr(out1), _ptr(out2), _ptr(status), _stream(None))
     if rc != 0:

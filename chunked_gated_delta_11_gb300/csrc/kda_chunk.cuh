@@ -27,7 +27,9 @@
 // sec. 3).  U keeps A diag(beta) as a bf16 high part plus remainder (two
 // products) because its rounding would go straight into the state.  The
 // inverse runs in fp32 (tf32 tensor-core products with high/low operand
-// splits).  The record holds fp32 values; the recurrence reads their tf32 part.
+// splits).  The record holds Qdec and W as bf16 (the recurrence's first MMA
+// reads a bf16 snapshot of the state, as FlashKDA's bf16 state does) and Kend,
+// Aqk, U, dlast as fp32 (the tf32 MMAs read their tf32 part).
 //
 // Raw input tiles (q, k, v, g_raw: 16 rows of 128 bf16, 4 KB each, in that
 // order) live in a 16 KB shared buffer of the caller, rows of 256 bytes whose
@@ -351,7 +353,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
         Kd[o] = mul2(kr, P);
         Ke[o] = mul2(kr, Q);
         Ki[o] = mul2(Ke[o], inv_dl);
-        *reinterpret_cast<float2*>(rec + b1_offset(16 + i, d0)) = Qd[o];
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(i, d0)) = pack_bf16(Qd[o].x, Qd[o].y);
       }
       qx[m] = pack_bf16(Qd[0].x, Qd[1].x);
       qy[m] = pack_bf16(Qd[0].y, Qd[1].y);
@@ -372,11 +374,10 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
     *reinterpret_cast<uint4*>(S.ki + ox) = make_uint4(ix[0], ix[1], ix[2], ix[3]);
     *reinterpret_cast<uint4*>(S.ki + oy) = make_uint4(iy[0], iy[1], iy[2], iy[3]);
     // Kend: this half's 8 tokens are one K=8 tile row, two 16-byte pieces
-    uint8_t* ke = rec + OFF_KEND;
-    *reinterpret_cast<float4*>(ke + kend_offset(d0, hf * 8)) = make_float4(ex[0], ex[1], ex[2], ex[3]);
-    *reinterpret_cast<float4*>(ke + kend_offset(d0, hf * 8 + 4)) = make_float4(ex[4], ex[5], ex[6], ex[7]);
-    *reinterpret_cast<float4*>(ke + kend_offset(d0 + 1, hf * 8)) = make_float4(ey[0], ey[1], ey[2], ey[3]);
-    *reinterpret_cast<float4*>(ke + kend_offset(d0 + 1, hf * 8 + 4)) = make_float4(ey[4], ey[5], ey[6], ey[7]);
+    *reinterpret_cast<float4*>(rec + kend_offset(d0, hf * 8)) = make_float4(ex[0], ex[1], ex[2], ex[3]);
+    *reinterpret_cast<float4*>(rec + kend_offset(d0, hf * 8 + 4)) = make_float4(ex[4], ex[5], ex[6], ex[7]);
+    *reinterpret_cast<float4*>(rec + kend_offset(d0 + 1, hf * 8)) = make_float4(ey[0], ey[1], ey[2], ey[3]);
+    *reinterpret_cast<float4*>(rec + kend_offset(d0 + 1, hf * 8 + 4)) = make_float4(ey[4], ey[5], ey[6], ey[7]);
   }
   chunk_sync();
   // q, k and g_raw of this chunk are no longer read
@@ -410,7 +411,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
           S.P0[i][j] = -r;
         }
       } else {
-        *reinterpret_cast<float*>(rec + OFF_AQK + aqk_offset(i, j)) = j <= i ? acc[e] : 0.f;
+        *reinterpret_cast<float*>(rec + aqk_offset(i, j)) = j <= i ? acc[e] : 0.f;
       }
     }
   }
@@ -489,8 +490,8 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
         mma16816(uacc, ah, bv[2 * half], bv[2 * half + 1]);
         mma16816(uacc, al, bv[2 * half], bv[2 * half + 1]);
         const int c = n0 + half * 8 + (l & 3) * 2;
-        *reinterpret_cast<float2*>(rec + b1_offset(r0, c)) = make_float2(wacc[0], wacc[1]);
-        *reinterpret_cast<float2*>(rec + b1_offset(r0 + 8, c)) = make_float2(wacc[2], wacc[3]);
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + r0, c)) = pack_bf16(wacc[0], wacc[1]);
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + r0, c)) = pack_bf16(wacc[2], wacc[3]);
         U[c * 16 + r0] = uacc[0];
         U[(c + 1) * 16 + r0] = uacc[1];
         U[c * 16 + r0 + 8] = uacc[2];

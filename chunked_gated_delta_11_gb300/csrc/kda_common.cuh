@@ -11,19 +11,19 @@
 //   S'   = S_c Diag(dlast) + E Kend    (state fast-forward, sec. 6.4)
 //
 // Byte layout of one record (REC_BYTES):
-//   [OFF_B1,  +16384)  [W ; Qdec], 32 rows x 128 key channels, fp32 (the
-//                      tensor core reads its tf32 part), K-major with the
-//                      128-byte swizzle: 4 blocks of 32 channels, each 32 rows
-//                      x 128 B; row n of block kb at kb*4096 + n*128, its
-//                      16-byte piece c at (c ^ (n & 7))*16.
-//                      Rows 0..15 are W, rows 16..31 are Qdec.
-//   [OFF_KEND, +8192)  Kend fp32 [128 d][16 j] as two K=8 tiles (j 0-7, j 8-15,
-//                      4 KB each), K-major with the 32-byte swizzle: row d at
-//                      d*32, 16-byte piece p at (p ^ ((d >> 2) & 1))*16.
-//   [OFF_U,   +8192)   U^T fp32 [128 value channels][16 tokens].
-//   [OFF_AQK, +1024)   Aqk fp32 [16 i][16 j] (chi_ij for j <= i, zero above) as
-//                      two K=8 tiles of 512 B, same 32-byte swizzle (row i).
-//   [OFF_DL,  +512)    dlast fp32 [128] = diagonal of D_{0:C-1}.
+//   [OFF_B1, +8192)    [Qdec ; W], 32 rows x 128 key channels, bf16, K-major
+//                      with the 128-byte swizzle: 2 blocks of 64 channels, each
+//                      32 rows x 128 B; row n of block kb at kb*4096 + n*128,
+//                      its 16-byte piece c at (c ^ (n & 7))*16.
+//                      Rows 0..15 are Qdec, rows 16..31 are W.
+//   [OFF_KA, +9216)    [Kend ; Aqk] fp32 (the tensor core reads its tf32
+//                      part), 144 rows r x 16 tokens j as two K=8 tiles (j 0-7,
+//                      j 8-15) of 4608 B, K-major with the 32-byte swizzle: row
+//                      r at r*32, 16-byte piece p at (p ^ ((r >> 2) & 1))*16.
+//                      Rows 0..127 are Kend[j][d] (r = d), rows 128..143 are
+//                      Aqk[i][j] (r = 128 + i; chi_ij for j <= i, zero above).
+//   [OFF_U,  +8192)    U^T fp32 [128 value channels][16 tokens].
+//   [OFF_DL, +512)     dlast fp32 [128] = diagonal of D_{0:C-1}.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
 
@@ -37,27 +37,26 @@ constexpr int kChunk = 16;
 constexpr int kDim = 128;
 
 constexpr int OFF_B1 = 0;
-constexpr int OFF_KEND = 16384;
-constexpr int OFF_U = 24576;
-constexpr int OFF_AQK = 32768;
-constexpr int OFF_DL = 33792;
-constexpr int REC_BYTES = 34304;
-constexpr int REC_STRIDE_SMEM = 34816;  // 1024-aligned stage stride in smem
+constexpr int OFF_KA = 8192;
+constexpr int KA_TILE = 4608;  // one K=8 tile of [Kend ; Aqk]: 144 rows x 32 B
+constexpr int OFF_U = OFF_KA + 2 * KA_TILE;
+constexpr int OFF_DL = OFF_U + 8192;
+constexpr int REC_BYTES = OFF_DL + 512;  // 26112
+constexpr int REC_STRIDE_SMEM = 26624;   // 1024-aligned stage stride in smem
+static_assert(REC_BYTES == 26112 && REC_STRIDE_SMEM >= REC_BYTES, "record layout");
 
 __host__ __device__ constexpr int b1_offset(int n, int d) {
-  // fp32 element (row n, channel d) of the [W ; Qdec] tile
-  return OFF_B1 + (d >> 5) * 4096 + n * 128 + ((((d & 31) >> 2) ^ (n & 7)) << 4) +
-         ((d & 3) << 2);
+  // byte offset of bf16 element (row n, channel d) of the [Qdec ; W] tile
+  return OFF_B1 + (d >> 6) * 4096 + n * 128 + ((((d & 63) >> 3) ^ (n & 7)) << 4) + ((d & 7) << 1);
 }
 
-// Byte offset of fp32 element (r, j), j < 16, in a pair of K=8 tiles with the
-// 32-byte swizzle (tile stride `tile`): the Kend tiles (r = d, tile 4096) and
-// the Aqk tiles (r = i, tile 512).
-__host__ __device__ constexpr int sw32_offset(int r, int j, int tile) {
-  return (j >> 3) * tile + r * 32 + (((((j & 7) >> 2) ^ (r >> 2)) & 1) << 4) + ((j & 3) << 2);
+// Byte offset of fp32 element (row r, token j) of the [Kend ; Aqk] tiles.
+__host__ __device__ constexpr int ka_offset(int r, int j) {
+  return OFF_KA + (j >> 3) * KA_TILE + r * 32 + (((((j & 7) >> 2) ^ (r >> 2)) & 1) << 4) +
+         ((j & 3) << 2);
 }
-__host__ __device__ constexpr int kend_offset(int d, int j) { return sw32_offset(d, j, 4096); }
-__host__ __device__ constexpr int aqk_offset(int i, int j) { return sw32_offset(i, j, 512); }
+__host__ __device__ constexpr int kend_offset(int d, int j) { return ka_offset(d, j); }
+__host__ __device__ constexpr int aqk_offset(int i, int j) { return ka_offset(128 + i, j); }
 
 // ---------------------------------------------------------------------------
 // small PTX wrappers
@@ -230,6 +229,17 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (tmem, fp32) (+)= A (tmem) * B (smem descriptor); A/B bf16, one K=16 step.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -79,7 +79,6 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
-    mbar_init(&ctl->mma1b, 1);
     mbar_init(&ctl->mma2, 1);
     ctl->abort = 0;
     fence_mbar_init();

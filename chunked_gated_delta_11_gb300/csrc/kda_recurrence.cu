@@ -5,17 +5,18 @@
 //
 // 128 threads, the state threads (tensor-memory lanes 0-127, state row v =
 // thread id).  Thread 0 also streams the records written by the chunk kernel
-// from HBM into a 3-stage shared-memory ring (one cp.async.bulk per record,
+// from HBM into a 4-stage shared-memory ring (one cp.async.bulk per record,
 // refilled as soon as a record's MMAs have finished) and issues every MMA.
 #include "kda_state.cuh"
 
 namespace kda {
 
-constexpr int K2_NST = 3;
+constexpr int K2_NST = 4;
 constexpr int K2_THREADS = 128;
 constexpr int K2_OST_OFF = K2_NST * REC_STRIDE_SMEM;
 constexpr int K2_CTL_OFF = K2_OST_OFF + 4096;
 constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 1024 + 64;
+static_assert(2 * (K2_SMEM + 1024) <= 228 * 1024, "recurrence kernel must fit two CTAs per SM");
 
 __global__ void __launch_bounds__(K2_THREADS, 2)
 recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init,
@@ -42,7 +43,6 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
-    mbar_init(&ctl->mma1b, 1);
     mbar_init(&ctl->mma2, 1);
     ctl->abort = 0;
     fence_mbar_init();

@@ -1,16 +1,16 @@
 // kda_selftest.cu -- one-CTA check of the tcgen05 operand conventions that the
-// recurrence kernel relies on, with values that are exact in tf32 / bf16 so
-// the fp32 results can be compared bit for bit on the host:
+// recurrence relies on, with values that are exact in bf16 / tf32 so the fp32
+// results can be compared bit for bit on the host.  Shared memory is laid out
+// as one chunk record (kda_common.cuh):
 //
-//   MMA1-like: D1[128 x 32]  = A1[128 x 128] (tf32, tensor memory)
-//                             * B1^T (fp32 [32 x 128] in the record's 128-byte
-//                               swizzled K-major layout), 16 K=8 steps.
-//   MMA2-like: D2[128 x 128] = D0 + A2[128 x 16] (tf32, tensor memory)
-//                             * B2^T (fp32 [128 x 16] in the record's Kend
-//                               layout: two 32-byte-swizzled K=8 tiles), two
-//                               K=8 steps accumulating onto a preset D.
+//   MMA1-like: D1[128 x 32]  = A1[128 x 128] (bf16 pairs in tensor memory)
+//                             * B1^T (bf16 [32 x 128] in the record's [Qdec ; W]
+//                               layout), 8 K=16 steps.
+//   MMA2-like: D2[128 x 144] = D0 + A2[128 x 16] (tf32, tensor memory)
+//                             * B2^T (fp32 [144 x 16] in the record's
+//                               [Kend ; Aqk] layout), 2 K=8 steps, accumulating.
 //
-// Every smem address the descriptors can form stays inside the 24 KB tile
+// Every smem address the descriptors can form stays inside the 17 KB record
 // area, so a wrong convention gives wrong numbers only.
 #include "kda_common.cuh"
 
@@ -26,20 +26,18 @@ __global__ void __launch_bounds__(128, 1)
 selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
                         int* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* b1 = smem;                       // 16 KB, record OFF_B1 layout
-  uint8_t* b2 = smem + 16384;               // 8 KB, Kend layout
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 24576);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 24584);
+  uint8_t* rec = align1024(smem_raw);       // one record: B1 then [Kend ; Aqk]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(rec + OFF_U);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rec + OFF_U + 8);
   const int t = threadIdx.x, w = t >> 5;
 
-  for (int e = t; e < 32 * 128; e += 128) {
-    const int n = e >> 7, d = e & 127;
-    *reinterpret_cast<float*>(b1 + b1_offset(n, d)) = st_b1(n, d);
+  for (int e = t; e < 32 * 64; e += 128) {
+    const int n = e >> 6, d = (e & 63) * 2;
+    *reinterpret_cast<uint32_t*>(rec + b1_offset(n, d)) = pack_bf16(st_b1(n, d), st_b1(n, d + 1));
   }
-  for (int e = t; e < 128 * 16; e += 128) {
-    const int d = e >> 4, j = e & 15;
-    *reinterpret_cast<float*>(b2 + kend_offset(d, j)) = st_b2(d, j);
+  for (int e = t; e < 144 * 16; e += 128) {
+    const int r = e >> 4, j = e & 15;
+    *reinterpret_cast<float*>(rec + ka_offset(r, j)) = st_b2(r, j);
   }
   if (t == 0) {
     mbar_init(bar, 1);
@@ -55,17 +53,29 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  const uint32_t A1 = tbase, D2 = tbase + 128, D1 = tbase + 256, A2 = tbase + 288;
+  const uint32_t A1 = tbase, D2 = tbase + 64, D1 = tbase + 256, A2 = tbase + 288;
   const uint32_t lane_off = static_cast<uint32_t>(w * 32) << 16;
   const int m = t;
 
-  // A1 row m, D0 row m, A2 row m (fp32)
-  for (int q = 0; q < 4; ++q) {
+  // A1 row m as bf16 pairs (low half = even k), D0 row m, A2 row m (fp32)
+  for (int q = 0; q < 2; ++q) {
     uint32_t r[32];
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(st_a1(m, q * 32 + i));
+    for (int i = 0; i < 32; ++i) {
+      const int k = (q * 32 + i) * 2;
+      r[i] = pack_bf16(st_a1(m, k), st_a1(m, k + 1));
+    }
     tmem_st32(A1 + lane_off + q * 32, r);
+  }
+  for (int q = 0; q < 5; ++q) {
+    uint32_t r[32];
     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(st_d0(m, q * 32 + i));
-    tmem_st32(D2 + lane_off + q * 32, r);
+    if (q < 4) {
+      tmem_st32(D2 + lane_off + q * 32, r);
+    } else {
+      uint32_t r16[16];
+      for (int i = 0; i < 16; ++i) r16[i] = r[i];
+      tmem_st16(D2 + lane_off + 128, r16);
+    }
   }
   {
     uint32_t r[16];
@@ -78,15 +88,15 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
   tc_fence_after();
 
   if (t == 0) {
-    const uint32_t id1 = make_idesc(2, 128, 32);
-    const uint32_t b1a = smem_u32(b1);
-    for (int kk = 0; kk < 16; ++kk) {
-      const uint64_t bd = make_sdesc(b1a + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
-      mma_tf32_ts(D1, A1 + kk * 8, bd, id1, kk > 0);
+    const uint32_t sb = smem_u32(rec);
+    const uint32_t id1 = make_idesc(1, 128, 32);
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
+      mma_bf16_ts(D1, A1 + kk * 8, bd, id1, kk > 0);
     }
-    const uint32_t id2 = make_idesc(2, 128, 128);
+    const uint32_t id2 = make_idesc(2, 128, 144);
     for (int kk = 0; kk < 2; ++kk)
-      mma_tf32_ts(D2, A2 + kk * 8, make_sdesc(smem_u32(b2) + kk * 4096, 16, 256, 6), id2, 1);
+      mma_tf32_ts(D2, A2 + kk * 8, make_sdesc(sb + OFF_KA + kk * KA_TILE, 16, 256, 6), id2, 1);
     tc_commit(bar);
   }
   __syncwarp();
@@ -101,8 +111,12 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
     for (int q = 0; q < 4; ++q) {
       tmem_ld32(D2 + lane_off + q * 32, r);
       tmem_wait_ld();
-      for (int i = 0; i < 32; ++i) out2[m * 128 + q * 32 + i] = __uint_as_float(r[i]);
+      for (int i = 0; i < 32; ++i) out2[m * 144 + q * 32 + i] = __uint_as_float(r[i]);
     }
+    uint32_t r16[16];
+    tmem_ld16(D2 + lane_off + 128, r16);
+    tmem_wait_ld();
+    for (int i = 0; i < 16; ++i) out2[m * 144 + 128 + i] = __uint_as_float(r16[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -113,7 +127,7 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
 
 extern "C" int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream) {
   if (!out1 || !out2 || !status) return 1;
-  const int smem = 24576 + 64 + 1024;
+  const int smem = kda::OFF_U + 64 + 1024;
   kda::selftest_tcgen05_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
       out1, out2, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;

@@ -4,43 +4,45 @@
 // kernel (records built in shared memory by the same CTA).
 //
 // One CTA owns one (sequence, head) unit.  Its 128 x 128 fp32 state S lives in
-// tensor memory, row v in lane v.  For each chunk record c (kda_common.cuh):
+// tensor memory, row v in lane v, next to a bf16 snapshot Sb of it.  For each
+// chunk record c (layout in kda_common.cuh), with S = S_c Diag(dlast_c)
+// already applied and Sb = bf16(S_c):
 //
-//   MMA1 (tcgen05 kind::tf32, M=128 N=32 K=128, issued by one thread):
-//        D1[v][n] = sum_d S[v][d] B1[n][d],  B1 = [W ; Qdec]
-//        -> D1[v][i] = (W S^T)[i][v],  D1[v][16+i] = (Qdec S^T)[i][v]
+//   MMA1 (tcgen05 kind::f16, bf16, M=128 N=32 K=128, 8 instructions):
+//        D1[v][n] = sum_d Sb[v][d] B1[n][d],  B1 = [Qdec ; W]
+//        -> D1[v][i] = (Qdec S_c^T)[i][v],  D1[v][16+i] = (W S_c^T)[i][v]
 //   state threads (thread v = row v):
-//        S[v][:] *= dlast                                  (forget, sec. 6.4)
-//        e[v][i] = U[i][v] - D1[v][i]                       (corrected errors)
-//        E^T -> tensor memory (fp32 rounded to tf32)
-//   MMA2 (tcgen05 kind::tf32, M=128 N=128 K=16, two instructions):
-//        S += E^T Kend                                      (write, sec. 6.4)
-//   MMA3 (kind::tf32, M=128 N=16 K=16, two instructions):
-//        D1[v][16+i] += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v]     (read, sec. 6.5)
-//   state threads: o -> bf16 -> out.
+//        e[v][i] = U[i][v] - D1[v][16+i]    (corrected errors, sec. 6.3)
+//        E^T -> tensor memory, fp32 rounded to tf32
+//   MMA2 (kind::tf32, M=128 N=144 K=16, 2 instructions), D = [S | D1 cols 0-15]:
+//        S[v][d]    += sum_j E^T[v][j] Kend[j][d]          (write, sec. 6.4)
+//        D1[v][i]   += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v] (read, sec. 6.5)
+//   state threads: o read out; then, once record c+1 is there,
+//        Sb = bf16(S) (= bf16(S_{c+1})),  S *= dlast_{c+1}   (forget, sec. 6.4)
+//   while MMA1 of chunk c+1 runs: o -> bf16 -> out.
 //
-// MMA1 takes the fp32 state as its A operand directly (the tensor core reads its
-// tf32 part), so no operand copy of S is kept.  D1 alternates between two
-// tensor-memory buffers so that chunk c's outputs can be read while MMA1 of
-// chunk c+1 writes the other one.  Barriers per CTA (mbarriers): full[s]
-// (record s ready), empty[s] (record s consumed: 128 state threads + one MMA
-// commit), mma1/mma2 (MMA completion), eready (128 state threads wrote E^T).
-// Every wait is bounded; a timeout sets the CTA's abort flag and the error word.
+// The tensor core spends tens of cycles per MMA instruction whatever its size
+// at these shapes, so the chain uses few, wide instructions: bf16 for MMA1
+// (K=16 per instruction, half the count of tf32) and one N=144 tf32 MMA for
+// the state update and the output correction together.  Barriers per CTA
+// (mbarriers): full[s] (record s ready), empty[s] (record s consumed), mma1 and
+// mma2 (MMA completion).  Every wait is bounded; a timeout sets the CTA's abort
+// flag and the error word.
 #pragma once
 
 #include "kda_common.cuh"
 
 namespace kda {
 
-constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_E = 192, TM_COLS = 256;
-// D1 of chunk c: columns TM_D1 + 32 * (c & 1) .. + 31
-__device__ __forceinline__ uint32_t d1_col(int c) { return TM_D1 + 32u * static_cast<uint32_t>(c & 1); }
+// tensor-memory columns: S (fp32), D1 = [O | W S^T] (fp32), E^T (tf32), Sb (bf16 pairs)
+constexpr uint32_t TM_S = 0, TM_D1 = 128, TM_E = 160, TM_SB = 176, TM_COLS = 256;
+static_assert(TM_SB + 64 <= TM_COLS, "tensor-memory map");
 
 template <int NST>
 struct StateCtl {
   uint64_t full[NST];
   uint64_t empty[NST];  // record fully consumed (its MMAs are done)
-  uint64_t mma1, mma1b, mma2;  // MMA1 k-steps over channels 0-63, then 64-127; MMA2/3
+  uint64_t mma1, mma2;
   uint32_t tmem;
   int abort;
 };
@@ -75,9 +77,6 @@ __device__ __forceinline__ bool state_all(bool pred) {
   return r != 0;
 }
 
-// descriptor of a K=8 tf32 tile with the 32-byte swizzle (rows of 32 bytes)
-__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) { return make_sdesc(saddr, 16, 256, 6); }
-
 // Initial state (or zeros) -> tensor memory.  State threads only (t < 128).
 __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
                                            const float* __restrict__ src) {
@@ -98,34 +97,53 @@ __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
   tmem_wait_st();
 }
 
-// MMA1 of chunk c (16 tf32 steps into D1 of that chunk) on the record at
-// shared address sb, committed in two halves: `bar_a` completes once the steps
-// over key channels 0-63 are done (those state columns may then be rewritten),
-// `bar_b` once all are.  Issuing thread only.
-__device__ __forceinline__ void issue_mma1(int c, uint32_t sb, uint32_t tb, uint64_t* bar_a,
-                                           uint64_t* bar_b) {
-  const uint32_t id1 = make_idesc(2, 128, 32);
-  const uint32_t d1 = tb + d1_col(c);
+// Snapshot and forget: Sb = bf16(S), then S *= dlast (dlast of the next
+// chunk, fp32 [128] in shared memory).  Thread v's row, 32 columns at a time.
+__device__ __forceinline__ void snapshot_and_decay(uint32_t tb, uint32_t lane_off,
+                                                   const float* dlast) {
+  const float4* dl4 = reinterpret_cast<const float4*>(dlast);
 #pragma unroll
-  for (int kk = 0; kk < 16; ++kk) {
-    const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
-    mma_tf32_ts(d1, tb + TM_S + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
-    if (kk == 7) tc_commit(bar_a);
+  for (int qd = 0; qd < 4; ++qd) {
+    uint32_t r[32], b[16];
+    tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      b[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    tmem_st16(tb + TM_SB + lane_off + qd * 16, b);
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+      const float4 dv = dl4[qd * 8 + i4];
+      r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
+      r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
+      r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
+      r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
+    }
+    tmem_st32(tb + TM_S + lane_off + qd * 32, r);
   }
-  tc_commit(bar_b);
+  tmem_wait_st();
 }
 
-// MMA2 (state update) and MMA3 (output correction) of chunk c, two K=8 tf32
-// steps each.  Issuing thread only.
-__device__ __forceinline__ void issue_mma23(int c, uint32_t sb, uint32_t tb, uint64_t* bar) {
-  const uint32_t id2 = make_idesc(2, 128, 128), id3 = make_idesc(2, 128, 16);
-  const uint32_t d1 = tb + d1_col(c);
+// MMA1 on the record at shared address sb: 8 bf16 K=16 steps into D1.
+// Issuing thread only.
+__device__ __forceinline__ void issue_mma1(uint32_t sb, uint32_t tb, uint64_t* bar) {
+  const uint32_t id1 = make_idesc(1, 128, 32);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
+    mma_bf16_ts(tb + TM_D1, tb + TM_SB + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+  }
+  tc_commit(bar);
+}
+
+// MMA2: [S | O] += E^T [Kend ; Aqk]^T, two tf32 K=8 steps with N = 144.
+// Issuing thread only.
+__device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* bar) {
+  const uint32_t id2 = make_idesc(2, 128, 144);
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk)
-    mma_tf32_ts(tb + TM_S, tb + TM_E + kk * 8, sw32_desc(sb + OFF_KEND + kk * 4096), id2, 1u);
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk)
-    mma_tf32_ts(d1 + 16, tb + TM_E + kk * 8, sw32_desc(sb + OFF_AQK + kk * 512), id3, 1u);
+    mma_tf32_ts(tb + TM_S, tb + TM_E + kk * 8, make_sdesc(sb + OFF_KA + kk * KA_TILE, 16, 256, 6),
+                id2, 1u);
   tc_commit(bar);
 }
 
@@ -144,94 +162,76 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
                                            uint8_t* ostage, StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
-  if (v == 0 && nchunks > 0) {
-    ok = wait_or_abort(&ctl->full[0], 0, ctl, err);
+  // chunk 0: snapshot the initial state and apply chunk 0's decay
+  if (nchunks > 0) {
+    ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->full[0], 0, ctl, err));
     if (ok) {
+      snapshot_and_decay(tb, lane_off, reinterpret_cast<const float*>(ring + OFF_DL));
+      tc_fence_before();
+    }
+    ok = state_all(ok);
+    if (ok && v == 0) {
       tc_fence_after();
-      issue_mma1(0, smem_u32(ring), tb, &ctl->mma1, &ctl->mma1b);
+      issue_mma1(smem_u32(ring), tb, &ctl->mma1);
       ++n1;
     }
   }
-  for (int c = 0; c < nchunks; ++c) {
+  for (int c = 0; c < nchunks && ok; ++c) {
     const int s = c % NST;
     const uint8_t* st = ring + s * REC_STRIDE_SMEM;
-    if (ok) ok = wait_or_abort(&ctl->full[s], (c / NST) & 1, ctl, err);
-    if (ok) ok = wait_or_abort(&ctl->mma1, c & 1, ctl, err);
-    ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma1, c & 1, ctl, err));
     if (ok) {
+      // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
       tc_fence_after();
-      // forget: S[v][:] *= dlast, 32 columns at a time; columns 0-63 while MMA1
-      // still reads columns 64-127, the rest once MMA1 is done
-      const float4* dl4 = reinterpret_cast<const float4*>(st + OFF_DL);
+      uint32_t d1[16];
+      tmem_ld16(tb + TM_D1 + 16 + lane_off, d1);
+      tmem_wait_ld();
+      const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
+      uint32_t pk[16];
 #pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        if (qd == 2) {
-          ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma1b, c & 1, ctl, err));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        uint32_t r[32];
-        tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 dv = dl4[qd * 8 + i4];
-          r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
-          r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
-          r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
-          r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
-        }
-        tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 u = U4[i4];
+        pk[i4 * 4 + 0] = tf32_bits(u.x - __uint_as_float(d1[i4 * 4 + 0]));
+        pk[i4 * 4 + 1] = tf32_bits(u.y - __uint_as_float(d1[i4 * 4 + 1]));
+        pk[i4 * 4 + 2] = tf32_bits(u.z - __uint_as_float(d1[i4 * 4 + 2]));
+        pk[i4 * 4 + 3] = tf32_bits(u.w - __uint_as_float(d1[i4 * 4 + 3]));
       }
-      if (ok) {
-        uint32_t d1[16];
-        tmem_ld16(tb + d1_col(c) + lane_off, d1);
-        tmem_wait_ld();
-        // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
-        const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          const float4 u = U4[i4];
-          pk[i4 * 4 + 0] = tf32_bits(u.x - __uint_as_float(d1[i4 * 4 + 0]));
-          pk[i4 * 4 + 1] = tf32_bits(u.y - __uint_as_float(d1[i4 * 4 + 1]));
-          pk[i4 * 4 + 2] = tf32_bits(u.z - __uint_as_float(d1[i4 * 4 + 2]));
-          pk[i4 * 4 + 3] = tf32_bits(u.w - __uint_as_float(d1[i4 * 4 + 3]));
-        }
-        tmem_st16(tb + TM_E + lane_off, pk);
-        tmem_wait_st();
-        tc_fence_before();
-      }
+      tmem_st16(tb + TM_E + lane_off, pk);
+      tmem_wait_st();
+      tc_fence_before();
     }
-    // every state thread has written E^T and finished reading U and dlast
+    // every state thread has written E^T and finished reading U
     if (!state_all(ok)) { ok = false; break; }
     if (v == 0) {
       tc_fence_after();
-      issue_mma23(c, smem_u32(st), tb, &ctl->mma2);
+      issue_mma2(smem_u32(st), tb, &ctl->mma2);
       ++n2;
     }
     ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma2, c & 1, ctl, err));
-    // outputs: D1[v][16 + i] = o[i][v], read while the tensor pipe is idle
-    // (MMA1 of chunk c+1 writes the other D1 buffer)
     uint32_t o[16];
     if (ok) {
       tc_fence_after();
-      tmem_ld16(tb + d1_col(c) + 16 + lane_off, o);
+      tmem_ld16(tb + TM_D1 + lane_off, o);
       tmem_wait_ld();
     }
-    if (v == 0 && ok) {
-      stage_free(c, s);
-      if (c + 1 < nchunks) {
-        const int s1 = (c + 1) % NST;
-        ok = wait_or_abort(&ctl->full[s1], ((c + 1) / NST) & 1, ctl, err);
-        if (ok) {
-          tc_fence_after();
-          issue_mma1(c + 1, smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1, &ctl->mma1b);
-          ++n1;
-        }
+    if (ok && v == 0) stage_free(c, s);
+    if (c + 1 < nchunks) {
+      // snapshot S_{c+1} for MMA1 of chunk c+1 and apply that chunk's decay
+      const int s1 = (c + 1) % NST;
+      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->full[s1], ((c + 1) / NST) & 1, ctl, err));
+      if (ok) {
+        snapshot_and_decay(tb, lane_off,
+                           reinterpret_cast<const float*>(ring + s1 * REC_STRIDE_SMEM + OFF_DL));
+        tc_fence_before();
+      }
+      // also: every thread has read this chunk's outputs out of D1
+      ok = state_all(ok);
+      if (ok && v == 0) {
+        tc_fence_after();
+        issue_mma1(smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1);
+        ++n1;
       }
     }
-    ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       // warp tile [16 tokens][32 channels] bf16 through shared memory, then
       // 16-byte stores (each row of the tile is 64 contiguous bytes of `out`)
@@ -240,14 +240,9 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       const int w = v >> 5, l = v & 31;
       uint8_t* ost = ostage + w * 1024;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        // tokens i, i+1 of channel v: two bf16 in one 4-byte store would
-        // stride rows, so keep one bf16 per store (conflict-free, 64 B rows)
+      for (int i = 0; i < 16; ++i)
         *reinterpret_cast<__nv_bfloat16*>(ost + i * 64 + l * 2) =
             __float2bfloat16_rn(__uint_as_float(o[i]));
-        *reinterpret_cast<__nv_bfloat16*>(ost + (i + 1) * 64 + l * 2) =
-            __float2bfloat16_rn(__uint_as_float(o[i + 1]));
-      }
       __syncwarp();
 #pragma unroll
       for (int rep = 0; rep < 2; ++rep) {
@@ -259,10 +254,10 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       __syncwarp();
     }
   }
-  ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
+  ok = state_all(ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
   if (!ok && v == 0) {
     // let MMAs still in flight finish before the CTA frees its tensor memory
-    if (n1 > 0) mbar_wait(&ctl->mma1b, (n1 - 1) & 1);
+    if (n1 > 0) mbar_wait(&ctl->mma1, (n1 - 1) & 1);
     if (n2 > 0) mbar_wait(&ctl->mma2, (n2 - 1) & 1);
   }
   tc_fence_after();

@@ -63,7 +63,7 @@ typedef enum kda_status {
 #define KDA_HEAD_DIM 128
 
 /* Bytes of device workspace kda_fwd / kda_chunk_prep / kda_chunk_recurrence
- * need for these sizes: one chunk record (34304 bytes) per (chunk slot, head),
+ * need for these sizes: one chunk record (26112 bytes) per (chunk slot, head),
  * with T_total / 16 + N + 1 chunk slots, enough for any split of T_total
  * tokens into N sequences.  Returns 0 for invalid sizes. */
 size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D);
@@ -125,13 +125,12 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const vo
 /* K1 alone: the token-parallel chunk kernel.  Writes one record per (chunk,
  * head) into `workspace` (same size rule as kda_fwd; must not be NULL).  For
  * chunk c (0-based) of sequence n and head h the record starts at byte
- *   ((floor(bos_n / 16) + n + c) * H + h) * 34304
+ *   ((floor(bos_n / 16) + n + c) * H + h) * 26112
  * with bos_n the first token of sequence n, and holds, for the chunk's tokens
  * i < 16 (rows past the sequence end are zero), in this order:
- *   [W ; Qdec] fp32 32 x 128, 128-byte-swizzled K-major tiles;
- *   Kend fp32 [128][16], two 32-byte-swizzled K=8 tiles;
- *   U^T fp32 [128][16];  Aqk fp32 [16][16], two 32-byte-swizzled K=8 tiles;
- *   dlast fp32 [128];
+ *   [Qdec ; W] bf16 32 x 128, 128-byte-swizzled K-major tiles;
+ *   [Kend ; Aqk] fp32 144 x 16 (Kend^T rows 0-127, Aqk rows 128-143), two
+ *   32-byte-swizzled K=8 tiles;  U^T fp32 [128][16];  dlast fp32 [128];
  * where (sec. 6.1-6.6 of "You Could Have Come Up with Kimi Delta Attention")
  *   Qdec_i = scale q^_i D_{0:i},  Kend_i = k^_i D_{i+1:last},
  *   Akk = (I + R)^-1 with R_ij = beta_i <k^_j|D_{j+1:i}|k^_i> (j < i),
@@ -162,10 +161,11 @@ kda_status kda_device_status(void* stream);
 const char* kda_status_string(kda_status status);
 
 /* Diagnostic: one-CTA check of the tensor-core operand conventions used by
- * the recurrence kernel (tf32 MMA with A in tensor memory and a 128-byte
- * swizzled B tile; tf32 MMA with A in tensor memory and the record's
- * 32-byte-swizzled Kend tiles, accumulating into a preset D).  Writes
- * out1 fp32 [128][32] and out2 fp32 [128][128] (device), and 5 to *status
+ * the recurrence kernel (bf16 MMA with A in tensor memory and the record's
+ * 128-byte-swizzled [Qdec ; W] tile; tf32 MMA with N = 144, A in tensor memory
+ * and the record's 32-byte-swizzled [Kend ; Aqk] tiles, accumulating into a
+ * preset D).  Writes out1 fp32 [128][32] and out2 fp32 [128][144] (device),
+ * and 5 to *status
  * (device int) if its wait ran out.  Returns 0, 1 for bad arguments, 4 on a
  * launch error.  The expected values are closed-form small dyadic numbers
  * (see the kernel source), exact in fp32. */
