@@ -9,9 +9,11 @@ and independent of the CUDA sources:
   precision, "FlashKDA v1: A Deep Dive", sec. 3);
 - U = A diag(beta) V with A diag(beta) as a bf16 high part plus remainder;
 - the Neumann-product inverse in fp32;
-- recurrence products on tf32 operands with fp32 accumulation: MMA1 reads the
-  fp32 state and the stored [W; Qdec] as tf32 (truncated), MMA2/MMA3 take E
-  rounded to tf32 and Kend / Aqk truncated;
+- the first recurrence product on bf16 operands (a bf16 snapshot of the fp32
+  state times [Qdec; W] stored as bf16, as FlashKDA's bf16 state), fp32
+  accumulation;
+- the state update and output correction on tf32 operands (E rounded to tf32,
+  Kend and Aqk truncated), fp32 accumulation, the state itself kept in fp32;
 - out rounded to bf16.
 
 If this model drifts past the tolerance, a precision choice of the kernels is
@@ -95,7 +97,7 @@ def model_forward(inp):
             W = mm(Ab_hi, bf16(Kd))
             U = mm(Ab_hi, vv) + mm(bf16(Ab - Ab_hi), vv)
             Aqk = np.tril(Mqk)
-            D1 = mm(tf32_trunc(S), tf32_trunc(np.concatenate([W, Qd], 1)).transpose(0, 2, 1))
+            D1 = mm(bf16(S), bf16(np.concatenate([W, Qd], 1)).transpose(0, 2, 1))
             E = tf32_nearest(U - D1[:, :, :16].transpose(0, 2, 1))
             O = D1[:, :, 16:].transpose(0, 2, 1) + mm(tf32_trunc(Aqk), E)
             S = S * dl[:, None, :] + mm(E.transpose(0, 2, 1), tf32_trunc(Ke))
