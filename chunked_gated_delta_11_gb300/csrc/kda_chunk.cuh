@@ -26,8 +26,9 @@
 // accumulation, as FlashKDA's chunk kernel does ("FlashKDA v1: A Deep Dive",
 // sec. 3).  U keeps A diag(beta) as a bf16 high part plus remainder (two
 // products) because its rounding would go straight into the state.  The
-// inverse runs in fp32 (tf32 tensor-core products with high/low operand
-// splits).  The record holds Qdec and W as bf16 (the recurrence's first MMA
+// inverse runs as bf16 tensor-core products of high/low operand splits (about
+// 16 significant bits per operand) with fp32 accumulation and fp32 additive
+// terms.  The record holds Qdec and W as bf16 (the recurrence's first MMA
 // reads a bf16 snapshot of the state, as FlashKDA's bf16 state does) and Kend,
 // Aqk, U, dlast as fp32 (the tf32 MMAs read their tf32 part).
 //
@@ -55,15 +56,15 @@ struct ChunkSmem {
   uint8_t kd[4096];  // Kdec
   uint8_t ki[4096];  // Kinv
   uint8_t qd[4096];  // Qdec
-  // inverse workspace, rows of 20 floats (16-byte aligned, conflict-free):
-  // row-major copies (X role) and transposed copies (Y role) of the factors
-  float Rr[16][20];   // R, later R^4 (rows)
-  float RT[16][20];   // R^T, later (R^8)^T
-  float R2r[16][20];  // R^2 (rows)
-  float R2T[16][20];  // (R^2)^T
-  float R4T[16][20];  // (R^4)^T
-  float P0[16][20];   // I - R, later P2 = (I-R)(I+R^2)(I+R^4)
-  float P1[16][20];   // P1 = (I-R)(I+R^2)
+  // inverse workspace: 16 x 16 matrices as bf16 high/low tiles (rows of AS
+  // elements, the ldmatrix operands) and, for the additive terms, fp32 copies
+  // (rows of 20 floats)
+  __nv_bfloat16 Rh[16 * AS], Rl[16 * AS];    // R, later R^8
+  __nv_bfloat16 R2h[16 * AS], R2l[16 * AS];  // R^2
+  __nv_bfloat16 R4h[16 * AS], R4l[16 * AS];  // R^4
+  __nv_bfloat16 P0h[16 * AS], P0l[16 * AS];  // I - R, later P2 = (I-R)(I+R^2)(I+R^4)
+  __nv_bfloat16 P1h[16 * AS], P1l[16 * AS];  // P1 = (I-R)(I+R^2)
+  float P0f[16][20], P1f[16][20];
   __nv_bfloat16 abh[16 * AS];  // A diag(beta), high
   __nv_bfloat16 abl[16 * AS];  // A diag(beta), low
   float rq[16], rk[16], beta[16];
@@ -157,87 +158,66 @@ __device__ __forceinline__ void issue_v_loads(uint8_t* raw, const __nv_bfloat16*
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// x = high + low, both tf32: the three-product split keeps ~21 mantissa bits
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_bits(x);
-  lo = tf32_bits(x - __uint_as_float(hi));
-}
-__device__ __forceinline__ void mma1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Columns 8 nt .. 8 nt + 7 of C = B + X Y for 16 x 16 fp32 matrices in shared
-// memory (B may be null; Y is given transposed), by one warp: two k-steps of
-// tf32 tensor-core products, each operand split into a tf32 high part and a
-// tf32 remainder (high*high + high*low + low*high), fp32 accumulation.
+// Columns 8 nt .. 8 nt + 7 of C = B + X Y for 16 x 16 matrices held as bf16
+// high/low tiles (rows of AS elements; B, if not null, fp32 rows of 20), by
+// one warp: one K=16 step of bf16 tensor-core products high*high + high*low +
+// low*high (about 16 significant bits per operand), fp32 accumulation.
 // Lane (g = l / 4, q = l % 4) gets C[g][8nt+2q], C[g][8nt+2q+1],
 // C[g+8][8nt+2q], C[g+8][8nt+2q+1] in c[0..3].
-__device__ __forceinline__ void tile_product(const float (*X)[20], const float (*YT)[20],
-                                             const float (*B)[20], int nt, int l,
-                                             float (&c)[4]) {
-  const int g = l >> 2, q = l & 3, j = nt * 8 + 2 * q;
-  float acc[2][4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) acc[1][e] = 0.f;
+__device__ __forceinline__ void tile_product(const __nv_bfloat16* Xh, const __nv_bfloat16* Xl,
+                                             const __nv_bfloat16* Yh, const __nv_bfloat16* Yl,
+                                             const float (*B)[20], int nt, int l, float (&c)[4]) {
+  const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
+  const int aoff = (l & 15) * AS + (l >> 4) * 8;                   // X row-major: A
+  const int boff = ((l & 7) + ((l >> 3) & 1) * 8) * AS + nt * 8;   // Y [k][n]: B, transposed load
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  ldsm_x4(ah, Xh + aoff);
+  ldsm_x4(al, Xl + aoff);
+  ldsm_x2_t(bh, Yh + boff);
+  ldsm_x2_t(bl, Yl + boff);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
   if (B) {
     const float2 b0 = *reinterpret_cast<const float2*>(&B[g][j]);
     const float2 b1 = *reinterpret_cast<const float2*>(&B[g + 8][j]);
-    acc[0][0] = b0.x;
-    acc[0][1] = b0.y;
-    acc[0][2] = b1.x;
-    acc[0][3] = b1.y;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[0][e] = 0.f;
+    acc[0] = b0.x;
+    acc[1] = b0.y;
+    acc[2] = b1.x;
+    acc[3] = b1.y;
   }
+  mma16816(acc2, al, bh[0], bh[1]);
+  mma16816(acc2, ah, bl[0], bl[1]);
+  mma16816(acc, ah, bh[0], bh[1]);
 #pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-    const int k = kk * 8 + q;
-    const float av[4] = {X[g][k], X[g + 8][k], X[g][k + 4], X[g + 8][k + 4]};
-    const float bv[2] = {YT[nt * 8 + g][k], YT[nt * 8 + g][k + 4]};
-    uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) split_tf32(av[e], ah[e], al[e]);
-    split_tf32(bv[0], bh[0], bl[0]);
-    split_tf32(bv[1], bh[1], bl[1]);
-    mma1688(acc[kk], al, bh[0], bh[1]);
-    mma1688(acc[kk], ah, bl[0], bl[1]);
-    mma1688(acc[kk], ah, bh[0], bh[1]);
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e];
+  for (int e = 0; e < 4; ++e) c[e] = acc[e] + acc2[e];
 }
-// Store a tile_product result: rows of Cm and, if CT, the transpose.
-__device__ __forceinline__ void store_tile(float (*Cm)[20], float (*CT)[20], int nt, int l,
-                                           const float (&c)[4]) {
+// Store a tile_product result as bf16 high/low tiles and, if Cf, fp32.
+__device__ __forceinline__ void store_tile(__nv_bfloat16* Ch, __nv_bfloat16* Cl, float (*Cf)[20],
+                                           int nt, int l, const float (&c)[4]) {
   const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
-  if (Cm) {
-    *reinterpret_cast<float2*>(&Cm[g][j]) = make_float2(c[0], c[1]);
-    *reinterpret_cast<float2*>(&Cm[g + 8][j]) = make_float2(c[2], c[3]);
-  }
-  if (CT) {
-    CT[j][g] = c[0];
-    CT[j + 1][g] = c[1];
-    CT[j][g + 8] = c[2];
-    CT[j + 1][g + 8] = c[3];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float x0 = c[2 * r], x1 = c[2 * r + 1];
+    const int row = g + r * 8;
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    *reinterpret_cast<__nv_bfloat162*>(Ch + row * AS + j) = h;
+    *reinterpret_cast<__nv_bfloat162*>(Cl + row * AS + j) = lo;
+    if (Cf) *reinterpret_cast<float2*>(&Cf[row][j]) = make_float2(x0, x1);
   }
 }
 
 // Zero the inverse workspace and the A diag(beta) tiles once (their unwritten
 // triangles must stay zero) and set the unit diagonal of I - R.
 __device__ __forceinline__ void clear_chunk_workspace(ChunkSmem& S, int t) {
-  float* p = &S.Rr[0][0];
-  const int n = static_cast<int>(7 * 16 * 20);
-  for (int e = t; e < n; e += 128) p[e] = 0.f;
-  uint16_t* b = reinterpret_cast<uint16_t*>(S.abh);
-  for (int e = t; e < 2 * 16 * AS; e += 128) b[e] = 0;
+  uint32_t* p = reinterpret_cast<uint32_t*>(S.Rh);
+  const int n = static_cast<int>((reinterpret_cast<uint8_t*>(S.rq) - reinterpret_cast<uint8_t*>(S.Rh)) / 4);
+  for (int e = t; e < n; e += 128) p[e] = 0u;
   named_bar(1, 128);
-  if (t < 16) S.P0[t][t] = 1.f;
+  if (t < 16) {
+    S.P0h[t * AS + t] = __float2bfloat16_rn(1.f);
+    S.P0f[t][t] = 1.f;
+  }
 }
 
 // Build the record of one chunk whose q, k, g_raw tiles were issued with
@@ -406,9 +386,13 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
       if (mat == 0) {
         if (j < i) {
           const float r = S.beta[i] * acc[e];
-          S.Rr[i][j] = r;
-          S.RT[j][i] = r;
-          S.P0[i][j] = -r;
+          __nv_bfloat16 hi, lo;
+          split_bf16(r, hi, lo);
+          S.Rh[i * AS + j] = hi;
+          S.Rl[i * AS + j] = lo;
+          S.P0h[i * AS + j] = __hneg(hi);
+          S.P0l[i * AS + j] = __hneg(lo);
+          S.P0f[i][j] = -r;
         }
       } else {
         *reinterpret_cast<float*>(rec + aqk_offset(i, j)) = j <= i ? acc[e] : 0.f;
@@ -424,28 +408,28 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
     const int nt = w & 1;
     float c[4];
     if (w < 2) {  // R^2
-      tile_product(S.Rr, S.RT, nullptr, nt, l, c);
-      store_tile(S.R2r, S.R2T, nt, l, c);
+      tile_product(S.Rh, S.Rl, S.Rh, S.Rl, nullptr, nt, l, c);
+      store_tile(S.R2h, S.R2l, nullptr, nt, l, c);
     }
     chunk_sync();
     if (w < 2) {  // P1 = (I-R)(I+R^2)
-      tile_product(S.P0, S.R2T, S.P0, nt, l, c);
-      store_tile(S.P1, nullptr, nt, l, c);
-    } else {      // R^4 (rows into Rr)
-      tile_product(S.R2r, S.R2T, nullptr, nt, l, c);
-      store_tile(S.Rr, S.R4T, nt, l, c);
+      tile_product(S.P0h, S.P0l, S.R2h, S.R2l, S.P0f, nt, l, c);
+      store_tile(S.P1h, S.P1l, S.P1f, nt, l, c);
+    } else {      // R^4
+      tile_product(S.R2h, S.R2l, S.R2h, S.R2l, nullptr, nt, l, c);
+      store_tile(S.R4h, S.R4l, nullptr, nt, l, c);
     }
     chunk_sync();
-    if (w < 2) {  // P2 = P1 (I+R^4)
-      tile_product(S.P1, S.R4T, S.P1, nt, l, c);
-      store_tile(S.P0, nullptr, nt, l, c);
-    } else {      // R^8 (only its transpose is kept)
-      tile_product(S.Rr, S.R4T, nullptr, nt, l, c);
-      store_tile(nullptr, S.RT, nt, l, c);
+    if (w < 2) {  // P2 = P1 (I+R^4), into the I - R slots
+      tile_product(S.P1h, S.P1l, S.R4h, S.R4l, S.P1f, nt, l, c);
+      store_tile(S.P0h, S.P0l, S.P0f, nt, l, c);
+    } else {      // R^8, into the R slots
+      tile_product(S.R4h, S.R4l, S.R4h, S.R4l, nullptr, nt, l, c);
+      store_tile(S.Rh, S.Rl, nullptr, nt, l, c);
     }
     chunk_sync();
     if (w < 2) {  // A = P2 (I+R^8), times diag(beta)
-      tile_product(S.P0, S.RT, S.P0, nt, l, c);
+      tile_product(S.P0h, S.P0l, S.Rh, S.Rl, S.P0f, nt, l, c);
       const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
       const float b0 = S.beta[j], b1 = S.beta[j + 1];
       const float ab[4] = {c[0] * b0, c[1] * b1, c[2] * b0, c[3] * b1};

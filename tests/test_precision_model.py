@@ -8,7 +8,8 @@ and independent of the CUDA sources:
   Kdec with bf16 operands and fp32 accumulation (FlashKDA's chunk-kernel
   precision, "FlashKDA v1: A Deep Dive", sec. 3);
 - U = A diag(beta) V with A diag(beta) as a bf16 high part plus remainder;
-- the Neumann-product inverse in fp32;
+- the Neumann-product inverse as bf16 products of high/low operand splits
+  (high*high + high*low + low*high), fp32 accumulation;
 - the first recurrence product on bf16 operands (a bf16 snapshot of the fp32
   state times [Qdec; W] stored as bf16, as FlashKDA's bf16 state), fp32
   accumulation;
@@ -46,6 +47,14 @@ def tf32_trunc(x):
 
 def mm(a, b):
     return (a.astype(np.float64) @ b.astype(np.float64)).astype(f32)
+
+
+def mm3(a, b):
+    """a @ b from bf16 high/low splits of both operands, low*low dropped."""
+    ah, bh = bf16(a), bf16(b)
+    al, bl = bf16(a - ah), bf16(b - bh)
+    return (ah.astype(np.float64) @ bh + ah.astype(np.float64) @ bl
+            + al.astype(np.float64) @ bh).astype(f32)
 
 
 def model_forward(inp):
@@ -88,10 +97,12 @@ def model_forward(inp):
             Mqk = mm(bf16(Qd), bf16(Ki).transpose(0, 2, 1))
             R = np.tril(beta[:, :, None] * Mkk, -1)
             I = np.eye(16, dtype=f32)
-            R2 = mm(R, R)
-            R4 = mm(R2, R2)
-            R8 = mm(R4, R4)
-            A = mm(mm(mm(I - R, I + R2), I + R4), I + R8)
+            R2 = mm3(R, R)
+            R4 = mm3(R2, R2)
+            R8 = mm3(R4, R4)
+            P1 = (I - R) + mm3(I - R, R2)
+            P2 = P1 + mm3(P1, R4)
+            A = P2 + mm3(P2, R8)
             Ab = A * beta[:, None, :]
             Ab_hi = bf16(Ab)
             W = mm(Ab_hi, bf16(Kd))
