@@ -245,21 +245,81 @@ def kda_selftest_tcgen05(device="cuda"):
 
 def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
                      cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
-                     stream=None, fused=True):
-    """Forward pass on host (CPU, ideally pinned) tensors: copies the inputs to the
-    device, runs kda_fwd_fused (or kda_fwd with fused=False) and copies `out` and
-    the final state back into host tensors (allocated pinned if not given).
-    Returns (out, final_state)."""
+                     stream=None, fused=True, groups=8):
+    """Forward pass on host (CPU, ideally pinned) tensors; returns (out, final_state)
+    as host tensors (allocated pinned if not given), ready once `stream` is.
+
+    The sequences are split into up to `groups` contiguous groups.  Group p's
+    inputs go host->device on a copy stream; its forward pass (kda_fwd_fused, or
+    kda_fwd with fused=False) runs on a stream of its own once they have arrived,
+    so it overlaps the copies of the later groups; its outputs go device->host on
+    a third stream, overlapping the remaining input copies (the link carries
+    both directions at once).  `stream` (default: the current stream) orders the
+    whole call: nothing starts before work already queued on it, and it waits
+    for the last copy."""
     stream = torch.cuda.current_stream(device) if stream is None else stream
     fwd = kda_fwd_fused if fused else kda_fwd
-    with torch.cuda.stream(stream):
-        dev = [None if x is None else x.to(device, non_blocking=True)
-               for x in (q, k, v, g_raw, beta_raw, initial_state, cu_seqlens)]
-        o_d, s_d = fwd(*dev[:5], scale, lower_bound, dev[5], dev[6], N=N, stream=stream)
-        if out is None:
-            out = torch.empty(o_d.shape, dtype=o_d.dtype, pin_memory=True)
-        if final_state is None:
-            final_state = torch.empty(s_d.shape, dtype=s_d.dtype, pin_memory=True)
-        out.copy_(o_d, non_blocking=True)
-        final_state.copy_(s_d, non_blocking=True)
+    T_total, H, D, N = _geometry(q, None, N) if cu_seqlens is None else (
+        q.shape[0], q.shape[1], q.shape[2], cu_seqlens.shape[0] - 1)
+    if cu_seqlens is not None:
+        bounds = [int(x) for x in cu_seqlens.tolist()]
+    else:
+        if T_total % max(N, 1):
+            raise ValueError("T_total must be a multiple of N without cu_seqlens")
+        L = T_total // max(N, 1)
+        bounds = [n * L for n in range(N + 1)]
+    if out is None:
+        out = torch.empty((T_total, H, D), dtype=torch.bfloat16, pin_memory=True)
+    if final_state is None:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, pin_memory=True)
+    dev = {name: torch.empty(t.shape, dtype=t.dtype, device=device)
+           for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw))}
+    init_d = None if initial_state is None else torch.empty(initial_state.shape,
+                                                            dtype=initial_state.dtype,
+                                                            device=device)
+    out_d = torch.empty((T_total, H, D), dtype=torch.bfloat16, device=device)
+    fs_d = torch.empty((N, H, D, D), dtype=torch.float32, device=device)
+    G = max(1, min(int(groups), N))
+    edges = [round(i * N / G) for i in range(G + 1)]
+    copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    work = [torch.cuda.Stream(device) for _ in range(G)]
+    start = torch.cuda.Event()
+    start.record(stream)
+    copy_in.wait_event(start)
+    copy_out.wait_event(start)
+    for gi in range(G):
+        n0, n1 = edges[gi], edges[gi + 1]
+        t0, t1 = bounds[n0], bounds[n1]
+        with torch.cuda.stream(copy_in):
+            for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw)):
+                dev[name][t0:t1].copy_(t[t0:t1], non_blocking=True)
+            if init_d is not None:
+                init_d[n0:n1].copy_(initial_state[n0:n1], non_blocking=True)
+            cu_g = None
+            if cu_seqlens is not None:
+                cu_g = torch.tensor([b - t0 for b in bounds[n0:n1 + 1]], dtype=torch.int32,
+                                    pin_memory=True).to(device, non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(copy_in)
+        work[gi].wait_event(arrived)
+        with torch.cuda.stream(work[gi]):
+            if cu_g is not None:
+                cu_g.record_stream(work[gi])
+            fwd(dev["q"][t0:t1], dev["k"][t0:t1], dev["v"][t0:t1], dev["g_raw"][t0:t1],
+                dev["beta_raw"][t0:t1], scale, lower_bound,
+                None if init_d is None else init_d[n0:n1], cu_g, N=n1 - n0,
+                out=out_d[t0:t1], final_state=fs_d[n0:n1], stream=work[gi])
+            done = torch.cuda.Event()
+            done.record(work[gi])
+        copy_out.wait_event(done)
+        with torch.cuda.stream(copy_out):
+            out[t0:t1].copy_(out_d[t0:t1], non_blocking=True)
+            final_state[n0:n1].copy_(fs_d[n0:n1], non_blocking=True)
+    finished = torch.cuda.Event()
+    finished.record(copy_out)
+    stream.wait_event(finished)
+    # the device buffers stay alive until the streams that use them are done
+    for t in list(dev.values()) + [out_d, fs_d] + ([init_d] if init_d is not None else []):
+        for st in [copy_in, copy_out] + work:
+            t.record_stream(st)
     return out, final_state

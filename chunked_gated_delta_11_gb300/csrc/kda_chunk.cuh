@@ -32,12 +32,13 @@
 // reads a bf16 snapshot of the state, as FlashKDA's bf16 state does) and Kend,
 // Aqk, U, dlast as fp32 (the tf32 MMAs read their tf32 part).
 //
-// Raw input tiles (q, k, v, g_raw: 16 rows of 128 bf16, 4 KB each, in that
-// order) live in a 16 KB shared buffer of the caller, rows of 256 bytes whose
-// 16-byte pieces are XOR-swizzled by (row & 7).  They arrive as two cp.async
-// groups: q, k and g_raw of chunk c (issued during the build of the previous
-// chunk, once its gate phase is done with them) and v of chunk c (issued at the
-// start of its own build, once the previous U products are done with it).
+// Raw input tiles (16 rows of 128 bf16, 4 KB each) live in shared buffers of
+// the caller: q, k, g_raw of a chunk in one 12 KB buffer (in that order), v in
+// a 4 KB one; rows of 256 bytes whose 16-byte pieces are XOR-swizzled by
+// (row & 7).  They arrive as two cp.async groups: q, k, g_raw (issued during an
+// earlier build, once that build's gate phase is done with its own buffer) and
+// v (issued at the start of the chunk's own build, once the previous U
+// products are done with the v buffer).
 #pragma once
 
 #include "kda_common.cuh"
@@ -46,8 +47,9 @@ namespace kda {
 
 constexpr int AS = 24;  // bf16 row stride of the 16 x 16 A diag(beta) tiles (48 B)
 
-enum { RAW_Q = 0, RAW_K = 1, RAW_V = 2, RAW_G = 3 };
-constexpr int RAW_BYTES = 4 * 4096;
+enum { RAW_Q = 0, RAW_K = 1, RAW_G = 2 };
+constexpr int QKG_BYTES = 3 * 4096;  // one chunk's q, k, g_raw tiles
+constexpr int V_BYTES = 4096;        // one chunk's v tile
 
 // Per-group scratch.  Derived operand tiles are bf16, stored transposed,
 // [128 channels][16 tokens] (32 B per channel), 16-byte halves swizzled by
@@ -151,10 +153,10 @@ __device__ __forceinline__ void issue_qkg_loads(uint8_t* raw, const __nv_bfloat1
   load_tile(raw, RAW_G, g, row_stride, nc, t);
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// v of one chunk: the second group
-__device__ __forceinline__ void issue_v_loads(uint8_t* raw, const __nv_bfloat16* v,
+// v of one chunk into a v buffer: the second group
+__device__ __forceinline__ void issue_v_loads(uint8_t* vt, const __nv_bfloat16* v,
                                               int64_t row_stride, int nc, int t) {
-  load_tile(raw, RAW_V, v, row_stride, nc, t);
+  load_tile(vt, 0, v, row_stride, nc, t);
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
@@ -220,9 +222,11 @@ __device__ __forceinline__ void clear_chunk_workspace(ChunkSmem& S, int t) {
   }
 }
 
-// Build the record of one chunk whose q, k, g_raw tiles were issued with
-// issue_qkg_loads (this call waits for them).  All 128 threads of the group
-// must call it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
+// Build the record of one chunk whose q, k, g_raw tiles were issued into `raw`
+// with issue_qkg_loads (this call waits for them; `newer_qkg` says whether the
+// q, k, g_raw group of a later chunk was issued after them, and may still be
+// pending).  Its v tile goes to `vt`.  All 128 threads of the group must call
+// it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
 // beta_raw (any value for t >= nc).  `rec` is the record base (global or
 // shared).  Hooks, each run by all 128 threads:
 //   may_write()  before the first write to the record; returns, uniformly,
@@ -230,17 +234,22 @@ __device__ __forceinline__ void clear_chunk_workspace(ChunkSmem& S, int t) {
 //                previous record of this stage is consumed).  Includes a
 //                barrier of the group.  On false nothing is written.
 //   load_v()     right after may_write: issue this chunk's v tile (issue_v_loads).
-//   next_qkg()   once the gate phase is done with q, k, g_raw: issue the next
-//                chunk's q, k, g_raw tiles; returns whether it issued them.
+//   next_qkg()   once the gate phase is done with `raw`: issue a later chunk's
+//                q, k, g_raw tiles (into `raw` or another buffer); returns
+//                whether it issued them.
 // Returns may_write().
 template <class MayWrite, class LoadV, class NextQKG>
-__device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
-                                                   uint32_t beta_raw_bits, int nc, float scale,
+__device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, uint8_t* vt,
+                                                   bool newer_qkg, uint32_t beta_raw_bits,
+                                                   int nc, float scale,
                                                    float lb_log2e, float eps, uint8_t* rec, int t,
                                                    MayWrite&& may_write, LoadV&& load_v,
                                                    NextQKG&& next_qkg) {
   const int w = t >> 5, l = t & 31;
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (newer_qkg)
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (t < 16) {
     const float br = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(beta_raw_bits)));
     S.beta[t] = (t < nc) ? sigmoid_fast(br) : 0.f;
@@ -253,31 +262,21 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
   const int gpc = p >> 2, gsub = (p & 3) * 4;  // 16-byte piece and byte inside it
 
   // ---- phase 1: squared norms (tensor cores) and retention factors ----
+  // warp w: Gram tile G[i][j] = sum_d X[i][d] X[j][d] of X = q (w < 2) or k,
+  // columns j = 8 (w & 1) .. +7; only its diagonal is kept.  Two accumulator
+  // chains (even / odd k-steps); the gate math below fills their latency.
+  const int nx = (w >> 1) ? RAW_K : RAW_Q, ntn = w & 1;
+  float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   {
-    // warp w: Gram tile G[i][j] = sum_d X[i][d] X[j][d] of X = q (w < 2) or k,
-    // columns j = 8 (w & 1) .. +7; only its diagonal is kept
-    const int x = (w >> 1) ? RAW_K : RAW_Q, nt = w & 1;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int mi = l >> 3;
     const int arow = (l & 7) + (mi & 1) * 8;
-    const int brow = nt * 8 + (l & 7);
+    const int brow = ntn * 8 + (l & 7);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t a[4], b[2];
-      ldsm_x4(a, raw_row(raw, x, arow) + raw_piece(arow, 2 * kk + (mi >> 1)));
-      ldsm_x2(b, raw_row(raw, x, brow) + raw_piece(brow, 2 * kk + (mi & 1)));
-      mma16816(acc, a, b[0], b[1]);
-    }
-    // diagonal: lane (g = l >> 2, c = l & 3) holds columns 2c, 2c+1 of rows g
-    // (acc 0, 1) and g + 8 (acc 2, 3) of the tile
-    const int g = l >> 2, e = g - 2 * (l & 3);
-    if (e == 0 || e == 1) {
-      const float s2 = nt ? (e ? acc[3] : acc[2]) : (e ? acc[1] : acc[0]);
-      const int i = nt * 8 + g;
-      if (x == RAW_Q)
-        S.rq[i] = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
-      else
-        S.rk[i] = rsqrtf(s2 + eps);
+      ldsm_x4(a, raw_row(raw, nx, arow) + raw_piece(arow, 2 * kk + (mi >> 1)));
+      ldsm_x2(b, raw_row(raw, nx, brow) + raw_piece(brow, 2 * kk + (mi & 1)));
+      mma16816(gacc[kk & 1], a, b[0], b[1]);
     }
   }
   // retention factors of this thread's 8 tokens, two channels each, and their
@@ -295,6 +294,20 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
       Pl[ii] = ii ? mul2(Pl[ii - 1], a[ii]) : a[ii];
     }
     S.hx[hf][p] = Pl[7];
+  }
+  {
+    // diagonal: lane (g = l >> 2, c = l & 3) holds columns 2c, 2c+1 of rows g
+    // (acc 0, 1) and g + 8 (acc 2, 3) of the tile
+    const int g = l >> 2, e = g - 2 * (l & 3);
+    if (e == 0 || e == 1) {
+      const float s2 = ntn ? (e ? gacc[0][3] + gacc[1][3] : gacc[0][2] + gacc[1][2])
+                           : (e ? gacc[0][1] + gacc[1][1] : gacc[0][0] + gacc[1][0]);
+      const int i = ntn * 8 + g;
+      if (nx == RAW_Q)
+        S.rq[i] = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
+      else
+        S.rk[i] = rsqrtf(s2 + eps);
+    }
   }
   chunk_sync();
 
@@ -368,7 +381,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
   {
     const int mat = w >> 1, nt = w & 1;
     const uint8_t* A = mat ? S.qd : S.kd;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // even / odd k-steps
     const int mi = l >> 3;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -377,8 +390,11 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
       uint32_t ar[4], br[2];
       ldsm_x4_t(ar, A + drv_off(arow, mi & 1));
       ldsm_x2_t(br, S.ki + drv_off(brow, nt));
-      mma16816(acc, ar, br[0], br[1]);
+      mma16816(acc2[kk & 1], ar, br[0], br[1]);
     }
+    float acc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = acc2[0][e] + acc2[1][e];
     const int r0 = l >> 2, c0 = nt * 8 + (l & 3) * 2;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -466,7 +482,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw,
       ldsm_x4(bk, S.kd + drv_off(n0 + (l & 7) + (mi >> 1) * 8, mi & 1));
       // raw V [j][d] is B in [k][n] order: transposed ldmatrix
       const int vrow = (l & 7) + (mi & 1) * 8;
-      ldsm_x4_t(bv, raw_row(raw, RAW_V, vrow) + raw_piece(vrow, (n0 >> 3) + (mi >> 1)));
+      ldsm_x4_t(bv, raw_row(vt, 0, vrow) + raw_piece(vrow, (n0 >> 3) + (mi >> 1)));
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float wacc[4] = {0.f, 0.f, 0.f, 0.f}, uacc[4] = {0.f, 0.f, 0.f, 0.f};

@@ -10,8 +10,8 @@
 //              2-stage ring while the state threads work on record c
 //                                                             kda_chunk.cuh
 // The chunk threads write the records with ordinary shared-memory stores; each
-// of them fences those stores against the tensor core's (async-proxy) reads
-// and then arrives on full[s].
+// of them fences those stores against the tensor core's (async-proxy) reads,
+// and each chunk warp then arrives once on full[s].
 //
 // FlashKDA measured its fused prototype as slower than the two-kernel split
 // ("FlashKDA v1: A Deep Dive", sec. 2) because the token-parallel work waited
@@ -34,7 +34,8 @@ static_assert(128 * F_STATE_REGS + 128 * F_CHUNK_REGS == F_THREADS * F_REGS,
               "register split must add up to the launch allocation");
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
 constexpr int F_RAW_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
-constexpr int F_OST_OFF = F_RAW_OFF + RAW_BYTES;
+constexpr int F_V_OFF = F_RAW_OFF + 2 * QKG_BYTES;  // q, k, g_raw double-buffered
+constexpr int F_OST_OFF = F_V_OFF + V_BYTES;
 constexpr int F_CTL_OFF = F_OST_OFF + 4096;
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
@@ -75,7 +76,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
 
   if (t == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&ctl->full[s], 128);
+      mbar_init(&ctl->full[s], 4);  // one arrival per chunk warp
       mbar_init(&ctl->empty[s], 1);
     }
     mbar_init(&ctl->mma1, 1);
@@ -102,11 +103,13 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   if (w >= 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_CHUNK_REGS));
     // ---------------- chunk threads ----------------
-    // Raw tiles have their own buffer: q, k, g_raw of chunk c+1 load once the
-    // gate phase of chunk c is done with them, v of chunk c at the start of
-    // its own build, so their latency hides behind the rest of a build.
+    // q, k, g_raw tiles are double-buffered: those of chunk c+2 load into
+    // chunk c's buffer as soon as chunk c's gate phase is done with them, so
+    // they have a whole build to arrive; v of chunk c loads at the start of
+    // its own build.
     const int tc = t - 128;
-    uint8_t* raw = smem + F_RAW_OFF;
+    auto rawbuf = [&](int c) { return smem + F_RAW_OFF + (c & 1) * QKG_BYTES; };
+    uint8_t* vt = smem + F_V_OFF;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
     auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
       t0 = bos + static_cast<int64_t>(c) * kChunk;
@@ -117,11 +120,13 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       int nc;
       chunk_geom(c, t0, nc);
       const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      issue_qkg_loads(raw, q + base, k + base, g + base, row_stride, nc, tc);
+      issue_qkg_loads(rawbuf(c), q + base, k + base, g + base, row_stride, nc, tc);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
     clear_chunk_workspace(CS, tc);
-    uint32_t bbits = nchunks > 0 ? start(0) : 0u;
+    uint32_t bbits[2] = {0u, 0u};  // beta_raw bits of chunks c and c+1
+    if (nchunks > 0) bbits[0] = start(0);
+    if (nchunks > 1) bbits[1] = start(1);
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
       int64_t t0;
@@ -129,28 +134,31 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       chunk_geom(c, t0, nc);
       uint32_t next_bits = 0u;
       // before writing record c into stage s: record c - NST there must be
-      // fully consumed (its MMAs read W, Qdec, Kend and Aqk)
+      // fully consumed (its MMAs read [Qdec ; W] and [Kend ; Aqk])
       auto may_write = [&]() -> bool {
         bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
         ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
         return chunk_all(ok);
       };
       auto load_v = [&] {
-        issue_v_loads(raw, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, row_stride, nc,
+        issue_v_loads(vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, row_stride, nc,
                       tc);
       };
       auto next_qkg = [&]() -> bool {
-        if (c + 1 >= nchunks) return false;
-        next_bits = start(c + 1);
+        if (c + 2 >= nchunks) return false;
+        next_bits = start(c + 2);
         return true;
       };
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
-      if (!build_chunk_record(CS, raw, bbits, nc, scale, lb_log2e, eps, rec, tc, may_write,
-                              load_v, next_qkg))
+      if (!build_chunk_record(CS, rawbuf(c), vt, c + 1 < nchunks, bbits[0], nc, scale,
+                              lb_log2e, eps, rec, tc, may_write, load_v, next_qkg))
         break;
+      // every thread's record stores -> async proxy, then one arrival per warp
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&ctl->full[s]);
-      bbits = next_bits;
+      __syncwarp();
+      if ((tc & 31) == 0) mbar_arrive(&ctl->full[s]);
+      bbits[0] = bbits[1];
+      bbits[1] = next_bits;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {

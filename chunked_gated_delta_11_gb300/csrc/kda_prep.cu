@@ -10,7 +10,8 @@ namespace kda {
 
 struct PrepSmem {
   ChunkSmem chunk;
-  uint8_t raw[RAW_BYTES];  // q, k, v, g_raw tiles
+  uint8_t raw[QKG_BYTES];  // q, k, g_raw tiles
+  uint8_t vt[V_BYTES];     // v tile
 };
 
 __global__ void __launch_bounds__(128, 4)
@@ -59,13 +60,13 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     bool have_next = false;
     uint32_t next_bits = 0u;
     build_chunk_record(
-        P.chunk, P.raw, bbits, cur.nc, scale, lb_log2e, eps,
+        P.chunk, P.raw, P.vt, false, bbits, cur.nc, scale, lb_log2e, eps,
         ws + static_cast<int64_t>(cur.item) * REC_BYTES, t,
         [] {
           chunk_sync();
           return true;
         },
-        [&] { issue_v_loads(P.raw, v + cur.base, row_stride, cur.nc, t); },
+        [&] { issue_v_loads(P.vt, v + cur.base, row_stride, cur.nc, t); },
         [&] {
           have_next = find(cur.item + gridDim.x, nxt);
           if (have_next) next_bits = start(nxt);

@@ -277,6 +277,24 @@ def test_host_buffer_entry_point():
     assert_close(f64(fs), rs, "final_state")
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_host_buffer_entry_point_grouped(path):
+    # packed sequences (one empty), initial states, three groups of sequences
+    inp = synth.make_inputs(0, 2, lengths=[33, 0, 100, 17, 64, 5], seed=21, init_std=0.02)
+    host = {key: (inp[key].pin_memory() if inp[key] is not None else None)
+            for key in ("q", "k", "v", "g_raw", "beta_raw", "initial_state")}
+    out, fs = kda.kda_forward_host(host["q"], host["k"], host["v"], host["g_raw"],
+                                   host["beta_raw"], inp["scale"], inp["lower_bound"],
+                                   host["initial_state"], inp["cu_seqlens"], groups=3,
+                                   fused=path == "fused")
+    torch.cuda.synchronize()
+    od, sd = run(to_dev(inp), path)
+    assert torch.equal(out, od.cpu()) and torch.equal(fs, sd.cpu())
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "grouped host out")
+    assert_close(f64(fs), rs, "grouped host final_state")
+
+
 def test_fused_agrees_with_split_on_b8():
     inp = synth.workload_inputs("b8", device="cuda")
     o1, s1 = run(inp, "split")
