@@ -128,35 +128,52 @@ __device__ __forceinline__ float2 bf2_at(const uint8_t* p) {
 // larger CTA can run other warps beside them).
 __device__ __forceinline__ void chunk_sync() { named_bar(1, 128); }
 
-// 16-byte cp.async loads of raw tile x of one chunk (rows past nc are zeroed
-// with plain stores).  src points at token t0, head h (row stride
-// `row_stride` elements).
-__device__ __forceinline__ void load_tile(uint8_t* raw, int x, const __nv_bfloat16* src,
-                                          int64_t row_stride, int nc, int t) {
-#pragma unroll
-  for (int rep = 0; rep < 2; ++rep) {
-    const int p = t + rep * 128;
-    const int row = p >> 4, c = p & 15;
-    uint8_t* d = raw_row(raw, x, row) + raw_piece(row, c);
-    if (row < nc)
-      cp_async16(d, src + row * row_stride + c * 8);
-    else
-      *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+// The raw-tile loads of one thread, set up once: thread t copies 16-byte piece
+// (t & 15) of rows (t >> 4) and (t >> 4) + 8 of every tile with cp.async; rows
+// past a chunk's end get `fill` (two bf16 per word) by plain stores instead.
+struct TileLoader {
+  uint32_t soff;     // shared offset of the piece in row (t >> 4) (row + 8: + 2048)
+  int64_t goff;      // element offset of the piece from the chunk's first token
+  int64_t rstride8;  // elements between a row and the row 8 further
+  int row;
+  __device__ __forceinline__ TileLoader(int t, int64_t row_stride) {
+    row = t >> 4;
+    const int c = t & 15;
+    soff = static_cast<uint32_t>(row * 256 + ((c ^ (row & 7)) << 4));
+    goff = row * row_stride + c * 8;
+    rstride8 = row_stride * 8;
   }
-}
-// q, k and g_raw of one chunk: the first cp.async group of its raw tiles
-__device__ __forceinline__ void issue_qkg_loads(uint8_t* raw, const __nv_bfloat16* q,
-                                                const __nv_bfloat16* k, const __nv_bfloat16* g,
-                                                int64_t row_stride, int nc, int t) {
-  load_tile(raw, RAW_Q, q, row_stride, nc, t);
-  load_tile(raw, RAW_K, k, row_stride, nc, t);
-  load_tile(raw, RAW_G, g, row_stride, nc, t);
+  // tile: shared base of one 16-row tile; src: the chunk's first token, head h
+  __device__ __forceinline__ void load(uint8_t* tile, const __nv_bfloat16* src, int nc,
+                                       uint32_t fill) const {
+    uint8_t* d = tile + soff;
+    const __nv_bfloat16* s0 = src + goff;
+    if (row < nc)
+      cp_async16(d, s0);
+    else
+      *reinterpret_cast<uint4*>(d) = make_uint4(fill, fill, fill, fill);
+    if (row + 8 < nc)
+      cp_async16(d + 2048, s0 + rstride8);
+    else
+      *reinterpret_cast<uint4*>(d + 2048) = make_uint4(fill, fill, fill, fill);
+  }
+};
+// q, k and g_raw of one chunk (pointers at its first token, head h): the first
+// cp.async group of its raw tiles
+__device__ __forceinline__ void issue_qkg_loads(const TileLoader& L, uint8_t* raw,
+                                                const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                                const __nv_bfloat16* g, int nc) {
+  L.load(raw + RAW_Q * 4096, q, nc, 0u);
+  L.load(raw + RAW_K * 4096, k, nc, 0u);
+  // g_raw rows past the end hold -inf: sigma(-inf) = 0 gives a = 2^0 = 1 exactly,
+  // so those tokens neither decay nor change the running products
+  L.load(raw + RAW_G * 4096, g, nc, 0xFF80FF80u);
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 // v of one chunk into a v buffer: the second group
-__device__ __forceinline__ void issue_v_loads(uint8_t* vt, const __nv_bfloat16* v,
-                                              int64_t row_stride, int nc, int t) {
-  load_tile(vt, 0, v, row_stride, nc, t);
+__device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
+                                              const __nv_bfloat16* v, int nc) {
+  L.load(vt, v, nc, 0u);
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
@@ -228,7 +245,8 @@ __device__ __forceinline__ void clear_chunk_workspace(ChunkSmem& S, int t) {
 // pending).  Its v tile goes to `vt`.  All 128 threads of the group must call
 // it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
 // beta_raw (any value for t >= nc).  `rec` is the record base (global or
-// shared).  Hooks, each run by all 128 threads:
+// shared memory).  Hooks, each run by
+// all 128 threads:
 //   may_write()  before the first write to the record; returns, uniformly,
 //                whether to go on (the fused kernel waits there until the
 //                previous record of this stage is consumed).  Includes a
@@ -287,11 +305,14 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
       const int i = hf * 8 + ii;
-      const float2 gv = bf2_at(raw_row(raw, RAW_G, i) + raw_piece(i, gpc) + gsub);
-      const bool live = i < nc;
-      a[ii].x = live ? ex2_approx(fmaf(hl, tanh_approx(0.5f * gv.x), hl)) : 1.f;
-      a[ii].y = live ? ex2_approx(fmaf(hl, tanh_approx(0.5f * gv.y), hl)) : 1.f;
-      Pl[ii] = ii ? mul2(Pl[ii - 1], a[ii]) : a[ii];
+      const float2 gh = __fmul2_rn(bf2_at(raw_row(raw, RAW_G, i) + raw_piece(i, gpc) + gsub),
+                                   make_float2(0.5f, 0.5f));
+      const float2 e = __ffma2_rn(make_float2(hl, hl),
+                                  make_float2(tanh_approx(gh.x), tanh_approx(gh.y)),
+                                  make_float2(hl, hl));
+      a[ii].x = ex2_approx(e.x);
+      a[ii].y = ex2_approx(e.y);
+      Pl[ii] = ii ? __fmul2_rn(Pl[ii - 1], a[ii]) : a[ii];
     }
     S.hx[hf][p] = Pl[7];
   }
@@ -314,7 +335,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   // ---- phase 2: decayed factors -> record (Qdec, Kend, dlast) and tiles ----
   {
     const float2 h0 = S.hx[0][p], h1 = S.hx[1][p];
-    const float2 dl = mul2(h0, h1);
+    const float2 dl = __fmul2_rn(h0, h1);
     const float2 pre = hf ? h0 : make_float2(1.f, 1.f);   // prod over tokens before the half
     const float2 post = hf ? make_float2(1.f, 1.f) : h1;  // prod over tokens after the half
     const float2 inv_dl = make_float2(rcp_approx(dl.x), rcp_approx(dl.y));
@@ -336,16 +357,16 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
       for (int o = 1; o >= 0; --o) {
         const int ii = 2 * m + o, i = hf * 8 + ii;
         const float2 Q = sfx;
-        sfx = mul2(sfx, a[ii]);
-        const float2 P = mul2(pre, Pl[ii]);
+        sfx = __fmul2_rn(sfx, a[ii]);
+        const float2 P = __fmul2_rn(pre, Pl[ii]);
         const int off = raw_piece(i, gpc) + gsub;
         const float2 qv = bf2_at(raw_row(raw, RAW_Q, i) + off);
         const float2 kv = bf2_at(raw_row(raw, RAW_K, i) + off);
-        Qd[o] = mul2(mul2(qv, make_float2(rqv[ii], rqv[ii])), P);
-        const float2 kr = mul2(kv, make_float2(rkv[ii], rkv[ii]));
-        Kd[o] = mul2(kr, P);
-        Ke[o] = mul2(kr, Q);
-        Ki[o] = mul2(Ke[o], inv_dl);
+        Qd[o] = __fmul2_rn(__fmul2_rn(qv, make_float2(rqv[ii], rqv[ii])), P);
+        const float2 kr = __fmul2_rn(kv, make_float2(rkv[ii], rkv[ii]));
+        Kd[o] = __fmul2_rn(kr, P);
+        Ke[o] = __fmul2_rn(kr, Q);
+        Ki[o] = __fmul2_rn(Ke[o], inv_dl);
         *reinterpret_cast<uint32_t*>(rec + b1_offset(i, d0)) = pack_bf16(Qd[o].x, Qd[o].y);
       }
       qx[m] = pack_bf16(Qd[0].x, Qd[1].x);
@@ -468,34 +489,44 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
 
   // ---- W = A diag(beta) Kdec, U = A diag(beta) V (warp w: channels 32w..32w+31) ----
   {
-    uint32_t ah[4], al[4];
-    const int aoff = (l & 15) * AS + (l >> 4) * 8;
-    ldsm_x4(ah, S.abh + aoff);
-    ldsm_x4(al, S.abl + aoff);
-    const int mi = l >> 3, r0 = l >> 2;
-    float* U = reinterpret_cast<float*>(rec + OFF_U);
+    const int mi = l >> 3, g = l >> 2, q2 = (l & 3) * 2;
+    // W [i][c]: A = (A diag beta)_hi [i][j], B = Kdec^T tile [c][j] ([n][k] order)
+    uint32_t ah[4];
+    ldsm_x4(ah, S.abh + (l & 15) * AS + (l >> 4) * 8);
 #pragma unroll
     for (int pair = 0; pair < 2; ++pair) {
       const int n0 = w * 32 + pair * 16;
-      // Kdec^T tile [d][j] is B in [n][k] order: plain ldmatrix
-      uint32_t bk[4], bv[4];
+      uint32_t bk[4];
       ldsm_x4(bk, S.kd + drv_off(n0 + (l & 7) + (mi >> 1) * 8, mi & 1));
-      // raw V [j][d] is B in [k][n] order: transposed ldmatrix
-      const int vrow = (l & 7) + (mi & 1) * 8;
-      ldsm_x4_t(bv, raw_row(vt, 0, vrow) + raw_piece(vrow, (n0 >> 3) + (mi >> 1)));
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        float wacc[4] = {0.f, 0.f, 0.f, 0.f}, uacc[4] = {0.f, 0.f, 0.f, 0.f};
+        float wacc[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816(wacc, ah, bk[2 * half], bk[2 * half + 1]);
-        mma16816(uacc, ah, bv[2 * half], bv[2 * half + 1]);
-        mma16816(uacc, al, bv[2 * half], bv[2 * half + 1]);
-        const int c = n0 + half * 8 + (l & 3) * 2;
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + r0, c)) = pack_bf16(wacc[0], wacc[1]);
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + r0, c)) = pack_bf16(wacc[2], wacc[3]);
-        U[c * 16 + r0] = uacc[0];
-        U[(c + 1) * 16 + r0] = uacc[1];
-        U[c * 16 + r0 + 8] = uacc[2];
-        U[(c + 1) * 16 + r0 + 8] = uacc[3];
+        const int c = n0 + half * 8 + q2;
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + g, c)) = pack_bf16(wacc[0], wacc[1]);
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + g, c)) = pack_bf16(wacc[2], wacc[3]);
+      }
+    }
+    // U^T [c][i] = V^T (A diag beta)^T: A = V^T from the raw v tile (transposed
+    // load), B = (A diag beta) rows [i][j] ([n][k] order), high and low parts;
+    // each lane then holds two consecutive tokens of one channel
+    uint32_t bh[4], bl[4];
+    const int boff = ((l & 7) + (l >> 4) * 8) * AS + ((l >> 3) & 1) * 8;
+    ldsm_x4(bh, S.abh + boff);
+    ldsm_x4(bl, S.abl + boff);
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int m0 = w * 32 + mt * 16;
+      const int j = (l & 7) + (mi >> 1) * 8;
+      uint32_t av[4];
+      ldsm_x4_t(av, raw_row(vt, 0, j) + raw_piece(j, (m0 >> 3) + (mi & 1)));
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float u[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(u, av, bh[2 * nt], bh[2 * nt + 1]);
+        mma16816(u, av, bl[2 * nt], bl[2 * nt + 1]);
+        *reinterpret_cast<float2*>(rec + u_offset(m0 + g, nt * 8 + q2)) = make_float2(u[0], u[1]);
+        *reinterpret_cast<float2*>(rec + u_offset(m0 + g + 8, nt * 8 + q2)) = make_float2(u[2], u[3]);
       }
     }
   }

@@ -22,7 +22,9 @@
 //                      r at r*32, 16-byte piece p at (p ^ ((r >> 2) & 1))*16.
 //                      Rows 0..127 are Kend[j][d] (r = d), rows 128..143 are
 //                      Aqk[i][j] (r = 128 + i; chi_ij for j <= i, zero above).
-//   [OFF_U,  +8192)    U^T fp32 [128 value channels][16 tokens].
+//   [OFF_U,  +8192)    U^T fp32 [128 value channels c][16 tokens i], 64 B per
+//                      row c; its four 16-byte pieces (4 tokens each) in the
+//                      order p ^ (2 * ((c >> 1) & 1)).
 //   [OFF_DL, +512)     dlast fp32 [128] = diagonal of D_{0:C-1}.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
@@ -56,6 +58,10 @@ __host__ __device__ constexpr int ka_offset(int r, int j) {
          ((j & 3) << 2);
 }
 __host__ __device__ constexpr int kend_offset(int d, int j) { return ka_offset(d, j); }
+// Byte offset of U^T element (value channel c, token i).
+__host__ __device__ constexpr int u_offset(int c, int i) {
+  return OFF_U + c * 64 + ((((i >> 2) ^ (((c >> 1) & 1) << 1))) << 4) + ((i & 3) << 2);
+}
 __host__ __device__ constexpr int aqk_offset(int i, int j) { return ka_offset(128 + i, j); }
 
 // ---------------------------------------------------------------------------
@@ -107,16 +113,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Packed two-lane fp32 arithmetic (one instruction for both halves).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

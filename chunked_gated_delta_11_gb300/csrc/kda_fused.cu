@@ -111,6 +111,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     auto rawbuf = [&](int c) { return smem + F_RAW_OFF + (c & 1) * QKG_BYTES; };
     uint8_t* vt = smem + F_V_OFF;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+    const TileLoader loader(tc, row_stride);
     auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
       t0 = bos + static_cast<int64_t>(c) * kChunk;
       nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
@@ -120,7 +121,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       int nc;
       chunk_geom(c, t0, nc);
       const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      issue_qkg_loads(rawbuf(c), q + base, k + base, g + base, row_stride, nc, tc);
+      issue_qkg_loads(loader, rawbuf(c), q + base, k + base, g + base, nc);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
     clear_chunk_workspace(CS, tc);
@@ -141,8 +142,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
         return chunk_all(ok);
       };
       auto load_v = [&] {
-        issue_v_loads(vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, row_stride, nc,
-                      tc);
+        issue_v_loads(loader, vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, nc);
       };
       auto next_qkg = [&]() -> bool {
         if (c + 2 >= nchunks) return false;

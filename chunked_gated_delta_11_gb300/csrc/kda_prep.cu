@@ -24,6 +24,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   PrepSmem& P = *reinterpret_cast<PrepSmem*>(smem_raw);
   const int t = threadIdx.x;
   const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+  const TileLoader loader(t, row_stride);
   clear_chunk_workspace(P.chunk, t);
 
   // the next used slot at or after `item` on this CTA's grid stride
@@ -49,7 +50,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     return false;
   };
   auto start = [&](const Item& it) -> uint32_t {
-    issue_qkg_loads(P.raw, q + it.base, k + it.base, g + it.base, row_stride, it.nc, t);
+    issue_qkg_loads(loader, P.raw, q + it.base, k + it.base, g + it.base, it.nc);
     return (t < it.nc) ? __bfloat16_as_ushort(beta_raw[(it.t0 + t) * H + it.h]) : 0u;
   };
 
@@ -66,7 +67,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
           chunk_sync();
           return true;
         },
-        [&] { issue_v_loads(P.vt, v + cur.base, row_stride, cur.nc, t); },
+        [&] { issue_v_loads(loader, P.vt, v + cur.base, cur.nc); },
         [&] {
           have_next = find(cur.item + gridDim.x, nxt);
           if (have_next) next_bits = start(nxt);

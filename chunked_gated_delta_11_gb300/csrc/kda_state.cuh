@@ -13,7 +13,7 @@
 //        -> D1[v][i] = (Qdec S_c^T)[i][v],  D1[v][16+i] = (W S_c^T)[i][v]
 //   state threads (thread v = row v):
 //        e[v][i] = U[i][v] - D1[v][16+i]    (corrected errors, sec. 6.3)
-//        E^T -> tensor memory, fp32 rounded to tf32
+//        E^T -> tensor memory (fp32; the MMA reads its tf32 part)
 //   MMA2 (kind::tf32, M=128 N=144 K=16, 2 instructions), D = [S | D1 cols 0-15]:
 //        S[v][d]    += sum_j E^T[v][j] Kend[j][d]          (write, sec. 6.4)
 //        D1[v][i]   += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v] (read, sec. 6.5)
@@ -114,10 +114,14 @@ __device__ __forceinline__ void snapshot_and_decay(uint32_t tb, uint32_t lane_of
 #pragma unroll
     for (int i4 = 0; i4 < 8; ++i4) {
       const float4 dv = dl4[qd * 8 + i4];
-      r[4 * i4 + 0] = __float_as_uint(__uint_as_float(r[4 * i4 + 0]) * dv.x);
-      r[4 * i4 + 1] = __float_as_uint(__uint_as_float(r[4 * i4 + 1]) * dv.y);
-      r[4 * i4 + 2] = __float_as_uint(__uint_as_float(r[4 * i4 + 2]) * dv.z);
-      r[4 * i4 + 3] = __float_as_uint(__uint_as_float(r[4 * i4 + 3]) * dv.w);
+      const float2 a = __fmul2_rn(make_float2(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1])),
+                                  make_float2(dv.x, dv.y));
+      const float2 b = __fmul2_rn(make_float2(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3])),
+                                  make_float2(dv.z, dv.w));
+      r[4 * i4 + 0] = __float_as_uint(a.x);
+      r[4 * i4 + 1] = __float_as_uint(a.y);
+      r[4 * i4 + 2] = __float_as_uint(b.x);
+      r[4 * i4 + 3] = __float_as_uint(b.y);
     }
     tmem_st32(tb + TM_S + lane_off + qd * 32, r);
   }
@@ -187,14 +191,21 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tmem_ld16(tb + TM_D1 + 16 + lane_off, d1);
       tmem_wait_ld();
       const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
+      const int usw = ((v >> 1) & 1) << 1;  // piece order of row v (u_offset)
       uint32_t pk[16];
+      // (the tensor core reads the tf32 part of these fp32 values)
+      const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 u = U4[i4];
-        pk[i4 * 4 + 0] = tf32_bits(u.x - __uint_as_float(d1[i4 * 4 + 0]));
-        pk[i4 * 4 + 1] = tf32_bits(u.y - __uint_as_float(d1[i4 * 4 + 1]));
-        pk[i4 * 4 + 2] = tf32_bits(u.z - __uint_as_float(d1[i4 * 4 + 2]));
-        pk[i4 * 4 + 3] = tf32_bits(u.w - __uint_as_float(d1[i4 * 4 + 3]));
+        const float4 u = U4[i4 ^ usw];
+        const float2 e0 = __ffma2_rn(make_float2(__uint_as_float(d1[i4 * 4]), __uint_as_float(d1[i4 * 4 + 1])),
+                                     m1, make_float2(u.x, u.y));
+        const float2 e1 = __ffma2_rn(make_float2(__uint_as_float(d1[i4 * 4 + 2]), __uint_as_float(d1[i4 * 4 + 3])),
+                                     m1, make_float2(u.z, u.w));
+        pk[i4 * 4 + 0] = __float_as_uint(e0.x);
+        pk[i4 * 4 + 1] = __float_as_uint(e0.y);
+        pk[i4 * 4 + 2] = __float_as_uint(e1.x);
+        pk[i4 * 4 + 3] = __float_as_uint(e1.y);
       }
       tmem_st16(tb + TM_E + lane_off, pk);
       tmem_wait_st();

@@ -87,7 +87,9 @@ def decode_record(rec):
     b1 = (rec.view(np.uint16)[_b1_offset(nn, dd) // 2].astype(np.uint32) << 16).view(np.float32)
     jj, rr = np.meshgrid(np.arange(16), np.arange(144), indexing="ij")
     ka = rec.view(np.float32)[_ka_offset(rr, jj) // 4]          # [j][r]
-    U = rec[17408:25600].view(np.float32).reshape(128, 16).T
+    cc, ii_ = np.meshgrid(np.arange(128), np.arange(16), indexing="ij")
+    uoff = 17408 + cc * 64 + ((((ii_ >> 2) ^ (((cc >> 1) & 1) << 1))) << 4) + ((ii_ & 3) << 2)
+    U = rec.view(np.float32)[uoff // 4].T
     dl = rec[25600:26112].view(np.float32)
     return {"Qdec": b1[:16].astype(np.float64), "W": b1[16:].astype(np.float64),
             "Kend": ka[:, :128].astype(np.float64), "Aqk": ka[:, 128:].T.astype(np.float64),

@@ -13,8 +13,8 @@ and independent of the CUDA sources:
 - the first recurrence product on bf16 operands (a bf16 snapshot of the fp32
   state times [Qdec; W] stored as bf16, as FlashKDA's bf16 state), fp32
   accumulation;
-- the state update and output correction on tf32 operands (E rounded to tf32,
-  Kend and Aqk truncated), fp32 accumulation, the state itself kept in fp32;
+- the state update and output correction on tf32 operands (E, Kend and Aqk
+  truncated to tf32), fp32 accumulation, the state itself kept in fp32;
 - out rounded to bf16.
 
 If this model drifts past the tolerance, a precision choice of the kernels is
@@ -34,11 +34,6 @@ TOL_MAX, TOL_FRO = 1e-2, 5e-3   # max-abs / max|ref| and relative Frobenius
 def bf16(x):
     b = np.asarray(x, dtype=f32).view(np.uint32).astype(np.uint64)
     return (((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16).astype(np.uint32).view(f32)
-
-
-def tf32_nearest(x):
-    b = np.asarray(x, dtype=f32).view(np.uint32).astype(np.uint64)
-    return (((b + 0x1000) >> 13) << 13).astype(np.uint32).view(f32)
 
 
 def tf32_trunc(x):
@@ -109,7 +104,7 @@ def model_forward(inp):
             U = mm(Ab_hi, vv) + mm(bf16(Ab - Ab_hi), vv)
             Aqk = np.tril(Mqk)
             D1 = mm(bf16(S), bf16(np.concatenate([W, Qd], 1)).transpose(0, 2, 1))
-            E = tf32_nearest(U - D1[:, :, :16].transpose(0, 2, 1))
+            E = tf32_trunc(U - D1[:, :, :16].transpose(0, 2, 1))
             O = D1[:, :, 16:].transpose(0, 2, 1) + mm(tf32_trunc(Aqk), E)
             S = S * dl[:, None, :] + mm(E.transpose(0, 2, 1), tf32_trunc(Ke))
             out[sl] = bf16(O[:, :nc]).transpose(1, 0, 2)
