@@ -58,15 +58,7 @@ struct ChunkSmem {
   uint8_t kd[4096];  // Kdec
   uint8_t ki[4096];  // Kinv
   uint8_t qd[4096];  // Qdec
-  // inverse workspace: 16 x 16 matrices as bf16 high/low tiles (rows of AS
-  // elements, the ldmatrix operands) and, for the additive terms, fp32 copies
-  // (rows of 20 floats)
-  __nv_bfloat16 Rh[16 * AS], Rl[16 * AS];    // R, later R^8
-  __nv_bfloat16 R2h[16 * AS], R2l[16 * AS];  // R^2
-  __nv_bfloat16 R4h[16 * AS], R4l[16 * AS];  // R^4
-  __nv_bfloat16 P0h[16 * AS], P0l[16 * AS];  // I - R, later P2 = (I-R)(I+R^2)(I+R^4)
-  __nv_bfloat16 P1h[16 * AS], P1l[16 * AS];  // P1 = (I-R)(I+R^2)
-  float P0f[16][20], P1f[16][20];
+  float Rf[16][20];  // R = strictly-lower(diag(beta) Mkk), fp32, rows of 20 floats
   __nv_bfloat16 abh[16 * AS];  // A diag(beta), high
   __nv_bfloat16 abl[16 * AS];  // A diag(beta), low
   float rq[16], rk[16], beta[16];
@@ -177,66 +169,73 @@ __device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Columns 8 nt .. 8 nt + 7 of C = B + X Y for 16 x 16 matrices held as bf16
-// high/low tiles (rows of AS elements; B, if not null, fp32 rows of 20), by
-// one warp: one K=16 step of bf16 tensor-core products high*high + high*low +
-// low*high (about 16 significant bits per operand), fp32 accumulation.
-// Lane (g = l / 4, q = l % 4) gets C[g][8nt+2q], C[g][8nt+2q+1],
-// C[g+8][8nt+2q], C[g+8][8nt+2q+1] in c[0..3].
-__device__ __forceinline__ void tile_product(const __nv_bfloat16* Xh, const __nv_bfloat16* Xl,
-                                             const __nv_bfloat16* Yh, const __nv_bfloat16* Yl,
-                                             const float (*B)[20], int nt, int l, float (&c)[4]) {
-  const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
-  const int aoff = (l & 15) * AS + (l >> 4) * 8;                   // X row-major: A
-  const int boff = ((l & 7) + ((l >> 3) & 1) * 8) * AS + nt * 8;   // Y [k][n]: B, transposed load
-  uint32_t ah[4], al[4], bh[2], bl[2];
-  ldsm_x4(ah, Xh + aoff);
-  ldsm_x4(al, Xl + aoff);
-  ldsm_x2_t(bh, Yh + boff);
-  ldsm_x2_t(bl, Yl + boff);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-  if (B) {
-    const float2 b0 = *reinterpret_cast<const float2*>(&B[g][j]);
-    const float2 b1 = *reinterpret_cast<const float2*>(&B[g + 8][j]);
-    acc[0] = b0.x;
-    acc[1] = b0.y;
-    acc[2] = b1.x;
-    acc[3] = b1.y;
-  }
-  mma16816(acc2, al, bh[0], bh[1]);
-  mma16816(acc2, ah, bl[0], bl[1]);
-  mma16816(acc, ah, bh[0], bh[1]);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) c[e] = acc[e] + acc2[e];
+// ---- 16 x 16 matrix products inside one warp (the triangular inverse) ----
+// A 16 x 16 fp32 matrix M lives in the accumulator layout of two m16n8 tiles:
+// lane (g = l / 4, q = l % 4) holds m[nt][e] = M[g + 8 (e >> 1)][8 nt + 2q + (e & 1)].
+// Packed to bf16 pairs, those registers are exactly the A-operand fragment of
+// an m16n8k16 product (a0 = m[0][0..1], a1 = m[0][2..3], a2 = m[1][0..1],
+// a3 = m[1][2..3]); the B-operand fragments of M are the 8 x 8 transposes of
+// the same four blocks (movmatrix).  Every operand is split into a bf16 high
+// part and remainder and each product takes high*high + high*low + low*high
+// (about 16 significant bits per operand) with fp32 accumulation.
+struct Mat16 {
+  float m[2][4];
+};
+struct OpA {
+  uint32_t hi[4], lo[4];
+};
+struct OpB {
+  uint32_t hi[4], lo[4];  // n-tile nt: {x[2 nt], x[2 nt + 1]}
+};
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
-// Store a tile_product result as bf16 high/low tiles and, if Cf, fp32.
-__device__ __forceinline__ void store_tile(__nv_bfloat16* Ch, __nv_bfloat16* Cl, float (*Cf)[20],
-                                           int nt, int l, const float (&c)[4]) {
-  const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
+__device__ __forceinline__ OpA as_a(const Mat16& M) {
+  OpA A;
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const float x0 = c[2 * r], x1 = c[2 * r + 1];
-    const int row = g + r * 8;
+  for (int r = 0; r < 4; ++r) {
+    const float x0 = M.m[r >> 1][(r & 1) * 2], x1 = M.m[r >> 1][(r & 1) * 2 + 1];
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     const float2 hf = __bfloat1622float2(h);
     const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    *reinterpret_cast<__nv_bfloat162*>(Ch + row * AS + j) = h;
-    *reinterpret_cast<__nv_bfloat162*>(Cl + row * AS + j) = lo;
-    if (Cf) *reinterpret_cast<float2*>(&Cf[row][j]) = make_float2(x0, x1);
+    A.hi[r] = *reinterpret_cast<const uint32_t*>(&h);
+    A.lo[r] = *reinterpret_cast<const uint32_t*>(&lo);
   }
+  return A;
+}
+__device__ __forceinline__ OpB as_b(const OpA& A) {
+  OpB B;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    B.hi[r] = movmatrix_t(A.hi[r]);
+    B.lo[r] = movmatrix_t(A.lo[r]);
+  }
+  return B;
+}
+// C = Init + X Y (Init may be null)
+__device__ __forceinline__ Mat16 mat_mul(const OpA& X, const OpB& Y, const Mat16* Init) {
+  Mat16 C;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float acc[4], acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = Init ? Init->m[nt][e] : 0.f;
+    mma16816(acc2, X.lo, Y.hi[2 * nt], Y.hi[2 * nt + 1]);
+    mma16816(acc2, X.hi, Y.lo[2 * nt], Y.lo[2 * nt + 1]);
+    mma16816(acc, X.hi, Y.hi[2 * nt], Y.hi[2 * nt + 1]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) C.m[nt][e] = acc[e] + acc2[e];
+  }
+  return C;
 }
 
-// Zero the inverse workspace and the A diag(beta) tiles once (their unwritten
-// triangles must stay zero) and set the unit diagonal of I - R.
+// Zero the A diag(beta) tiles once (the inverse rewrites them in full).
 __device__ __forceinline__ void clear_chunk_workspace(ChunkSmem& S, int t) {
-  uint32_t* p = reinterpret_cast<uint32_t*>(S.Rh);
-  const int n = static_cast<int>((reinterpret_cast<uint8_t*>(S.rq) - reinterpret_cast<uint8_t*>(S.Rh)) / 4);
-  for (int e = t; e < n; e += 128) p[e] = 0u;
+  uint16_t* b = reinterpret_cast<uint16_t*>(S.abh);
+  for (int e = t; e < 2 * 16 * AS; e += 128) b[e] = 0;
   named_bar(1, 128);
-  if (t < 16) {
-    S.P0h[t * AS + t] = __float2bfloat16_rn(1.f);
-    S.P0f[t][t] = 1.f;
-  }
 }
 
 // Build the record of one chunk whose q, k, g_raw tiles were issued into `raw`
@@ -421,16 +420,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     for (int e = 0; e < 4; ++e) {
       const int i = r0 + (e >> 1) * 8, j = c0 + (e & 1);
       if (mat == 0) {
-        if (j < i) {
-          const float r = S.beta[i] * acc[e];
-          __nv_bfloat16 hi, lo;
-          split_bf16(r, hi, lo);
-          S.Rh[i * AS + j] = hi;
-          S.Rl[i * AS + j] = lo;
-          S.P0h[i * AS + j] = __hneg(hi);
-          S.P0l[i * AS + j] = __hneg(lo);
-          S.P0f[i][j] = -r;
-        }
+        S.Rf[i][j] = j < i ? S.beta[i] * acc[e] : 0.f;
       } else {
         *reinterpret_cast<float*>(rec + aqk_offset(i, j)) = j <= i ? acc[e] : 0.f;
       }
@@ -438,45 +428,47 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   }
   chunk_sync();
 
-  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8) in four dependent levels of
-  // tensor-core tile products (warp w: tile w & 1 of product w >> 1); the last
-  // level writes A diag(beta) as bf16 high / low ----
-  {
-    const int nt = w & 1;
-    float c[4];
-    if (w < 2) {  // R^2
-      tile_product(S.Rh, S.Rl, S.Rh, S.Rl, nullptr, nt, l, c);
-      store_tile(S.R2h, S.R2l, nullptr, nt, l, c);
-    }
-    chunk_sync();
-    if (w < 2) {  // P1 = (I-R)(I+R^2)
-      tile_product(S.P0h, S.P0l, S.R2h, S.R2l, S.P0f, nt, l, c);
-      store_tile(S.P1h, S.P1l, S.P1f, nt, l, c);
-    } else {      // R^4
-      tile_product(S.R2h, S.R2l, S.R2h, S.R2l, nullptr, nt, l, c);
-      store_tile(S.R4h, S.R4l, nullptr, nt, l, c);
-    }
-    chunk_sync();
-    if (w < 2) {  // P2 = P1 (I+R^4), into the I - R slots
-      tile_product(S.P1h, S.P1l, S.R4h, S.R4l, S.P1f, nt, l, c);
-      store_tile(S.P0h, S.P0l, S.P0f, nt, l, c);
-    } else {      // R^8, into the R slots
-      tile_product(S.R4h, S.R4l, S.R4h, S.R4l, nullptr, nt, l, c);
-      store_tile(S.Rh, S.Rl, nullptr, nt, l, c);
-    }
-    chunk_sync();
-    if (w < 2) {  // A = P2 (I+R^8), times diag(beta)
-      tile_product(S.P0h, S.P0l, S.Rh, S.Rl, S.P0f, nt, l, c);
-      const int g = l >> 2, j = nt * 8 + 2 * (l & 3);
-      const float b0 = S.beta[j], b1 = S.beta[j + 1];
-      const float ab[4] = {c[0] * b0, c[1] * b1, c[2] * b0, c[3] * b1};
+  // ---- A = (I - R)(I + R^2)(I + R^4)(I + R^8): four dependent levels of
+  // register-resident tensor-core products in warp 0, no shared memory or
+  // barriers between them; it writes A diag(beta) as bf16 high / low ----
+  if (w == 0) {
+    const int g = l >> 2, q2 = (l & 3) * 2;
+    Mat16 R, P0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = g + (e >> 1) * 8, jj = j + (e & 1);
-        __nv_bfloat16 hi, lo;
-        split_bf16(ab[e], hi, lo);
-        S.abh[i * AS + jj] = hi;
-        S.abl[i * AS + jj] = lo;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int i = g + 8 * h2, j = 8 * nt + q2;
+        const float2 r = *reinterpret_cast<const float2*>(&S.Rf[i][j]);
+        R.m[nt][2 * h2] = r.x;
+        R.m[nt][2 * h2 + 1] = r.y;
+        P0.m[nt][2 * h2] = (i == j ? 1.f : 0.f) - r.x;
+        P0.m[nt][2 * h2 + 1] = (i == j + 1 ? 1.f : 0.f) - r.y;
+      }
+    const OpA Ra = as_a(R);
+    const Mat16 R2 = mat_mul(Ra, as_b(Ra), nullptr);                     // R^2
+    const OpA R2a = as_a(R2);
+    const OpB R2b = as_b(R2a);
+    const Mat16 P1 = mat_mul(as_a(P0), R2b, &P0);                        // (I-R)(I+R^2)
+    const Mat16 R4 = mat_mul(R2a, R2b, nullptr);                         // R^4
+    const OpA R4a = as_a(R4);
+    const OpB R4b = as_b(R4a);
+    const Mat16 P2 = mat_mul(as_a(P1), R4b, &P1);                        // P1 (I+R^4)
+    const Mat16 R8 = mat_mul(R4a, R4b, nullptr);                         // R^8
+    const Mat16 A = mat_mul(as_a(P2), as_b(as_a(R8)), &P2);              // P2 (I+R^8)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int j = 8 * nt + q2;
+      const float b0 = S.beta[j], b1 = S.beta[j + 1];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int i = g + 8 * h2;
+        const float x0 = A.m[nt][2 * h2] * b0, x1 = A.m[nt][2 * h2 + 1] * b1;
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+        const float2 hf = __bfloat1622float2(hi);
+        *reinterpret_cast<__nv_bfloat162*>(S.abh + i * AS + j) = hi;
+        *reinterpret_cast<__nv_bfloat162*>(S.abl + i * AS + j) =
+            __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
       }
     }
   }
