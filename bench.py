@@ -40,7 +40,17 @@ WORKLOAD_TEXT = {
     "long": "1 sequence x 131072 tokens, H=32, D=128, bf16, g_raw~N(2,1), zero initial state",
     "varlen": "64 packed sequences, lengths U[1,16384] not multiples of 16, H=32, init 0.02*N(0,1)",
     "b2": "B=2 sequences x T=8192 tokens, H=32, D=128, bf16 (profiling size)",
+    "decode": "one serving step: 256 sequences x 1 token, H=32, D=128, bf16, fp32 states "
+              "0.02*N(0,1) in and out",
 }
+PATH_TEXT = {
+    "fused": "kda_fwd_fused = fused_kernel (chunk math + tcgen05 recurrence, one launch)",
+    "split": "kda_fwd = chunk_prep_kernel (K1) + recurrence_kernel (K2, tcgen05)",
+    "decode": "kda_decode = decode_kernel (token-by-token recurrence, state slices in registers)",
+}
+PATH_KERNEL = {"fused": "fused_kernel (the whole step)", "split": "whole kda_fwd step (K1 + K2)",
+               "decode": "decode_kernel (the whole step)"}
+PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1}
 
 
 def load_peaks():
@@ -215,8 +225,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b8")
-    ap.add_argument("--path", choices=["fused", "split"], default="fused",
-                    help="fused: kda_fwd_fused (one kernel); split: kda_fwd (K1 + K2)")
+    ap.add_argument("--path", choices=["fused", "split", "decode"], default=None,
+                    help="fused: kda_fwd_fused (one kernel); split: kda_fwd (K1 + K2); decode: "
+                         "kda_decode (recurrent schedule).  Default: decode for the decode "
+                         "workload, fused otherwise")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=0,
                     help="oracle sample size for cpu_baseline (0 = one unit per core)")
@@ -252,7 +264,12 @@ def main():
     def step_fused():
         kda.kda_fwd_fused(*a, N=N, out=out, final_state=fs, stream=stream)
 
-    step = step_fused if args.path == "fused" else step_split
+    def step_decode():
+        kda.kda_decode(*a, N=N, out=out, final_state=fs, stream=stream)
+
+    if args.path is None:
+        args.path = "decode" if args.workload == "decode" else "fused"
+    step = {"fused": step_fused, "split": step_split, "decode": step_decode}[args.path]
 
     for _ in range(args.warmup):
         step()
@@ -311,7 +328,7 @@ def main():
         kda.kda_forward_host(host["q"], host["k"], host["v"], host["g_raw"], host["beta_raw"],
                              inp["scale"], inp["lower_bound"], host["initial_state"],
                              host["cu_seqlens"], N=N, out=out_h, final_state=fs_h, stream=stream,
-                             fused=args.path == "fused")
+                             schedule=args.path)
 
     e2e_ms = None
     if args.e2e_steps > 0:
@@ -345,16 +362,14 @@ def main():
             "workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
             "global_batch": N * world, "seq_len": T // N if inp["cu_seqlens"] is None else None,
             "heads": H, "head_dim": 128, "tokens_per_step": tokens_per_step,
-            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
-            "path": ("kda_fwd_fused = fused_kernel (chunk math + tcgen05 recurrence, one launch)"
-                     if args.path == "fused" else
-                     "kda_fwd = chunk_prep_kernel (K1) + recurrence_kernel (K2, tcgen05)"),
+            "l2": ("states larger than L2 (no flush)" if args.workload == "decode"
+                   else "inputs larger than L2 (no flush)"),
+            "parallelism": f"replicas x{world}", "path": PATH_TEXT[args.path],
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "traffic": None,
-            "kernel": "fused_kernel (the whole step)" if args.path == "fused"
-                      else "whole kda_fwd step (K1 + K2)",
+            "kernel": PATH_KERNEL[args.path],
             "alg_bytes_per_launch": alg_bytes, "alg_flop_per_launch": alg_flop,
             "tensor_frac": alg_flop / (ms * 1e-3) / 1e12 / tc,
             "roofline_ms": max(alg_bytes / hbm / 1e9, alg_flop / tc / 1e12) * 1e3,
@@ -362,14 +377,16 @@ def main():
         },
         "kernels": {
             "fused_kernel": {"ms": ms if args.path == "fused" else other_ms},
-            "split_path": {"ms": other_ms if args.path == "fused" else ms,
+            "split_path": {"ms": ms if args.path == "split" else
+                           (other_ms if args.path == "fused" else None),
                            "chunk_prep_kernel_ms": k1_ms, "recurrence_kernel_ms": k2_ms},
+            **({"decode_kernel": {"ms": ms}} if args.path == "decode" else {}),
         },
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {
             "value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
             "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (1 if args.path == "fused" else 2) * args.steps,
+        "gpu_launches": PATH_LAUNCHES[args.path] * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1

@@ -23,12 +23,21 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
-    "kda_forward_host", "kda_fwd_fused", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
+    "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
 ]
 
 CHUNK = 16
 HEAD_DIM = 128
 REC_BYTES = 26112
+
+SCHEDULES = {"split": 0, "fused": 1, "decode": 2}
+
+
+class _Options(ctypes.Structure):
+    """kda_options of include/kda.h."""
+    _fields_ = [("schedule", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+                ("gate", ctypes.c_int32)]
+
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED",
           3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_LAUNCH", 5: "KDA_ERR_TIMEOUT"}
@@ -64,6 +73,11 @@ def load(build_if_missing: bool = False):
         lib.kda_fwd.restype = ctypes.c_int
         lib.kda_fwd_fused.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P, P]
         lib.kda_fwd_fused.restype = ctypes.c_int
+        lib.kda_decode.argtypes = lib.kda_fwd_fused.argtypes
+        lib.kda_decode.restype = ctypes.c_int
+        lib.kda_forward.argtypes = [P, P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P,
+                                    P, sz, P]
+        lib.kda_forward.restype = ctypes.c_int
         lib.kda_fwd_noalloc.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P,
                                         P]
         lib.kda_fwd_noalloc.restype = ctypes.c_int
@@ -185,6 +199,76 @@ def kda_fwd_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=No
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024
 
 
+def kda_decode(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
+               cu_seqlens=None, N=None, out=None, final_state=None, stream=None,
+               output_final_state=True):
+    """The forward pass in the recurrent (decode) schedule: token by token, the
+    state slice of each (sequence, head, 32 value rows) in registers.  For a few
+    tokens per sequence per call; final_state may be initial_state itself
+    (updated in place).  Returns (out, final_state)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw)):
+        _need(t, name, torch.bfloat16, (T_total, H, D))
+    _need(beta_raw, "beta_raw", torch.bfloat16, (T_total, H))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T_total, H, D))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, D, D))
+    st = load().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                           float(scale), float(lower_bound), _ptr(initial_state),
+                           _ptr(cu_seqlens), T_total, H, N, D, _ptr(out), _ptr(final_state),
+                           _stream(stream))
+    _check(st, "kda_decode")
+    return out, final_state
+
+
+def kda_forward(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
+                cu_seqlens=None, N=None, out=None, final_state=None, schedule="fused",
+                workspace=None, stream=None, output_final_state=True):
+    """The forward pass with the options of kda_forward in include/kda.h, read off
+    the tensors: states fp32 or bf16 (both the same; the final state is allocated
+    with the initial state's dtype), g_raw [T_total, H, 128] (per channel) or
+    [T_total, H] (one gate per token and head).  schedule: "fused", "split" or
+    "decode".  Returns (out, final_state)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, (T_total, H, D))
+    per_head = g_raw.dim() == 2
+    _need(g_raw, "g_raw", torch.bfloat16, (T_total, H) if per_head else (T_total, H, D))
+    _need(beta_raw, "beta_raw", torch.bfloat16, (T_total, H))
+    dtypes = {t.dtype for t in (initial_state, final_state) if t is not None}
+    if len(dtypes) > 1:
+        raise TypeError("initial_state and final_state must have the same dtype")
+    sdt = dtypes.pop() if dtypes else torch.float32
+    if sdt not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"states must be float32 or bfloat16, got {sdt}")
+    if initial_state is not None:
+        _need(initial_state, "initial_state", sdt, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T_total, H, D))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=sdt, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", sdt, (N, H, D, D))
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    opts = _Options(SCHEDULES[schedule], 1 if sdt == torch.bfloat16 else 0, 1 if per_head else 0)
+    st = load().kda_forward(ctypes.byref(opts), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+                            _ptr(beta_raw), float(scale), float(lower_bound),
+                            _ptr(initial_state), _ptr(cu_seqlens), T_total, H, N, D, _ptr(out),
+                            _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "kda_forward")
+    return out, final_state
+
+
 def kda_fwd_noalloc(q, k, v, g_raw, beta_raw, scale, lower_bound, out, final_state=None,
                     initial_state=None, cu_seqlens=None, N=None, stream=None):
     """kda_fwd for callers that cannot allocate device memory: the chunk records
@@ -245,20 +329,21 @@ def kda_selftest_tcgen05(device="cuda"):
 
 def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
                      cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
-                     stream=None, fused=True, groups=8):
+                     stream=None, schedule="fused", groups=8):
     """Forward pass on host (CPU, ideally pinned) tensors; returns (out, final_state)
     as host tensors (allocated pinned if not given), ready once `stream` is.
 
     The sequences are split into up to `groups` contiguous groups.  Group p's
-    inputs go host->device on a copy stream; its forward pass (kda_fwd_fused, or
-    kda_fwd with fused=False) runs on a stream of its own once they have arrived,
+    inputs go host->device on a copy stream; its forward pass (`schedule`:
+    "fused" = kda_fwd_fused, "split" = kda_fwd, "decode" = kda_decode) runs on a
+    stream of its own once they have arrived,
     so it overlaps the copies of the later groups; its outputs go device->host on
     a third stream, overlapping the remaining input copies (the link carries
     both directions at once).  `stream` (default: the current stream) orders the
     whole call: nothing starts before work already queued on it, and it waits
     for the last copy."""
     stream = torch.cuda.current_stream(device) if stream is None else stream
-    fwd = kda_fwd_fused if fused else kda_fwd
+    fwd = {"fused": kda_fwd_fused, "split": kda_fwd, "decode": kda_decode}[schedule]
     T_total, H, D, N = _geometry(q, None, N) if cu_seqlens is None else (
         q.shape[0], q.shape[1], q.shape[2], cu_seqlens.shape[0] - 1)
     if cu_seqlens is not None:

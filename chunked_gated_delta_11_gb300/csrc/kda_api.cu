@@ -12,14 +12,19 @@ namespace kda {
 cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const void* g,
                               const void* beta_raw, float scale, float lower_bound, float eps,
                               const int32_t* cu, int64_t T_total, int H, int N, void* ws,
-                              int sm_count, cudaStream_t stream);
-cudaError_t launch_recurrence(const void* ws, const float* init, const int32_t* cu,
-                              int64_t T_total, int H, int N, void* out, float* final_state,
-                              int* err, cudaStream_t stream);
+                              int gate_scalar, int sm_count, cudaStream_t stream);
+cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
+                              int64_t T_total, int H, int N, void* out, void* final_state,
+                              FwdOpts opts, int* err, cudaStream_t stream);
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
                          const void* beta_raw, float scale, float lower_bound, float eps,
-                         const float* init, const int32_t* cu, int64_t T_total, int H, int N,
-                         void* out, float* final_state, int* err, cudaStream_t stream);
+                         const void* init, const int32_t* cu, int64_t T_total, int H, int N,
+                         void* out, void* final_state, FwdOpts opts, int* err,
+                         cudaStream_t stream);
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* g,
+                          const void* beta_raw, float scale, float lower_bound, float eps,
+                          const void* init, const int32_t* cu, int64_t T_total, int H, int N,
+                          void* out, void* final_state, FwdOpts opts, cudaStream_t stream);
 
 // Error word written by kernels when a bounded wait runs out.  Kernels get its
 // address as an argument; cudaGetSymbolAddress is resolved once per device.
@@ -71,20 +76,23 @@ kda_status check_sizes(int64_t T_total, int32_t H, int32_t N, int32_t D,
   return KDA_OK;
 }
 
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
 kda_status check_inputs(const void* q, const void* k, const void* v, const void* g,
-                        const void* beta_raw, float scale, float lower_bound, int64_t T_total) {
+                        const void* beta_raw, float scale, float lower_bound, int64_t T_total,
+                        bool gate_scalar = false) {
   if (!(lower_bound >= -5.0f && lower_bound <= 0.0f)) return KDA_ERR_UNSUPPORTED;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return KDA_ERR_INVALID_ARG;
   if (T_total > 0) {
     if (!q || !k || !v || !g || !beta_raw) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g))
-      return KDA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(beta_raw) & 1u) != 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return KDA_ERR_INVALID_ARG;
+    if (gate_scalar ? !aligned2(g) : !aligned16(g)) return KDA_ERR_INVALID_ARG;
+    if (!aligned2(beta_raw)) return KDA_ERR_INVALID_ARG;
   }
   return KDA_OK;
 }
 
-kda_status check_outputs(const void* out, const float* initial_state, const float* final_state,
+kda_status check_outputs(const void* out, const void* initial_state, const void* final_state,
                          int64_t T_total) {
   if (T_total > 0 && (!out || !aligned16(out))) return KDA_ERR_INVALID_ARG;
   if (initial_state && !aligned16(initial_state)) return KDA_ERR_INVALID_ARG;
@@ -103,6 +111,55 @@ extern "C" size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int3
   return static_cast<size_t>((bytes + 255) & ~static_cast<int64_t>(255));
 }
 
+namespace {
+
+// The forward pass behind every entry point.  schedule: 0 split (K1 then K2
+// through `workspace`, or one allocated on the stream), 1 fused, 2 decode.
+kda_status forward(int schedule, FwdOpts opts, const void* q, const void* k, const void* v,
+                   const void* g_raw, const void* beta_raw, float scale, float lower_bound,
+                   const void* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                   int32_t H, int32_t N, int32_t D, void* out, void* final_state,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total,
+                        opts.gate_scalar != 0)) != KDA_OK)
+    return s;
+  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
+  const size_t need = schedule == 0 ? kda_workspace_size(T_total, H, N, D) : 0;
+  if (schedule == 0 && workspace && (!aligned16(workspace) || workspace_bytes < need))
+    return KDA_ERR_WORKSPACE;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (schedule == 1) {
+    e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
+                     cu_seqlens, T_total, H, N, out, final_state, opts, info.err, st);
+  } else if (schedule == 2) {
+    e = launch_decode(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
+                      cu_seqlens, T_total, H, N, out, final_state, opts, st);
+  } else {
+    void* ws = workspace;
+    if (!ws) {
+      if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_WORKSPACE;
+      }
+    }
+    if (T_total > 0)
+      e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, cu_seqlens,
+                            T_total, H, N, ws, opts.gate_scalar, info.sm_count, st);
+    if (e == cudaSuccess)
+      e = launch_recurrence(ws, initial_state, cu_seqlens, T_total, H, N, out, final_state, opts,
+                            info.err, st);
+    if (!workspace) cudaFreeAsync(ws, st);
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
 extern "C" kda_status kda_chunk_prep(const void* q, const void* k, const void* v,
                                      const void* g_raw, const void* beta_raw, float scale,
                                      float lower_bound, const int32_t* cu_seqlens,
@@ -118,7 +175,7 @@ extern "C" kda_status kda_chunk_prep(const void* q, const void* k, const void* v
   if ((s = device_info(info)) != KDA_OK) return s;
   if (T_total == 0) return KDA_OK;
   cudaError_t e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
-                                    cu_seqlens, T_total, H, N, workspace, info.sm_count,
+                                    cu_seqlens, T_total, H, N, workspace, 0, info.sm_count,
                                     static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
@@ -136,7 +193,8 @@ extern "C" kda_status kda_chunk_recurrence(const void* workspace, size_t workspa
   DeviceInfo info;
   if ((s = device_info(info)) != KDA_OK) return s;
   cudaError_t e = launch_recurrence(workspace, initial_state, cu_seqlens, T_total, H, N, out,
-                                    final_state, info.err, static_cast<cudaStream_t>(stream));
+                                    final_state, FwdOpts{0, 0}, info.err,
+                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
@@ -146,32 +204,9 @@ extern "C" kda_status kda_fwd(const void* q, const void* k, const void* v, const
                               int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
                               float* final_state, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
-  if (s != KDA_OK) return s;
-  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total)) != KDA_OK)
-    return s;
-  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
-  const size_t need = kda_workspace_size(T_total, H, N, D);
-  if (workspace && (!aligned16(workspace) || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
-  DeviceInfo info;
-  if ((s = device_info(info)) != KDA_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  void* ws = workspace;
-  if (!ws) {
-    if (cudaMallocAsync(&ws, need, st) != cudaSuccess) {
-      cudaGetLastError();
-      return KDA_ERR_WORKSPACE;
-    }
-  }
-  cudaError_t e = cudaSuccess;
-  if (T_total > 0)
-    e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, cu_seqlens,
-                          T_total, H, N, ws, info.sm_count, st);
-  if (e == cudaSuccess)
-    e = launch_recurrence(ws, initial_state, cu_seqlens, T_total, H, N, out, final_state,
-                          info.err, st);
-  if (!workspace) cudaFreeAsync(ws, st);
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  return forward(0, FwdOpts{0, 0}, q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state,
+                 cu_seqlens, T_total, H, N, D, out, final_state, workspace, workspace_bytes,
+                 stream);
 }
 
 extern "C" kda_status kda_fwd_fused(const void* q, const void* k, const void* v,
@@ -180,17 +215,36 @@ extern "C" kda_status kda_fwd_fused(const void* q, const void* k, const void* v,
                                     const int32_t* cu_seqlens, int64_t T_total, int32_t H,
                                     int32_t N, int32_t D, void* out, float* final_state,
                                     void* stream) {
-  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
-  if (s != KDA_OK) return s;
-  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total)) != KDA_OK)
-    return s;
-  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
-  DeviceInfo info;
-  if ((s = device_info(info)) != KDA_OK) return s;
-  cudaError_t e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
-                               initial_state, cu_seqlens, T_total, H, N, out, final_state,
-                               info.err, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  return forward(1, FwdOpts{0, 0}, q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state,
+                 cu_seqlens, T_total, H, N, D, out, final_state, nullptr, 0, stream);
+}
+
+extern "C" kda_status kda_decode(const void* q, const void* k, const void* v, const void* g_raw,
+                                 const void* beta_raw, float scale, float lower_bound,
+                                 const float* initial_state, const int32_t* cu_seqlens,
+                                 int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
+                                 float* final_state, void* stream) {
+  return forward(2, FwdOpts{0, 0}, q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state,
+                 cu_seqlens, T_total, H, N, D, out, final_state, nullptr, 0, stream);
+}
+
+extern "C" kda_status kda_forward(const kda_options* opts, const void* q, const void* k,
+                                  const void* v, const void* g_raw, const void* beta_raw,
+                                  float scale, float lower_bound, const void* initial_state,
+                                  const int32_t* cu_seqlens, int64_t T_total, int32_t H,
+                                  int32_t N, int32_t D, void* out, void* final_state,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!opts) return KDA_ERR_INVALID_ARG;
+  const int32_t sc = opts->schedule, sd = opts->state_dtype, gt = opts->gate;
+  if (sc != KDA_SCHEDULE_SPLIT && sc != KDA_SCHEDULE_FUSED && sc != KDA_SCHEDULE_DECODE)
+    return KDA_ERR_INVALID_ARG;
+  if ((sd != KDA_STATE_F32 && sd != KDA_STATE_BF16) ||
+      (gt != KDA_GATE_PER_CHANNEL && gt != KDA_GATE_PER_HEAD))
+    return KDA_ERR_INVALID_ARG;
+  const int schedule = sc == KDA_SCHEDULE_SPLIT ? 0 : sc == KDA_SCHEDULE_FUSED ? 1 : 2;
+  return forward(schedule, FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
+                 g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens, T_total, H, N,
+                 D, out, final_state, workspace, workspace_bytes, stream);
 }
 
 extern "C" kda_status kda_device_status(void* stream) {

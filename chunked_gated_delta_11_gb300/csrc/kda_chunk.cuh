@@ -150,16 +150,38 @@ struct TileLoader {
       *reinterpret_cast<uint4*>(d + 2048) = make_uint4(fill, fill, fill, fill);
   }
 };
+// Scalar gate (one g_raw per token and head, broadcast over the key channels):
+// the g tile is written with plain stores.  gs points at the chunk's first
+// token, head h; its token stride is `gstride` elements.
+__device__ __forceinline__ void broadcast_gate_tile(const TileLoader& L, uint8_t* tile,
+                                                    const __nv_bfloat16* gs, int64_t gstride,
+                                                    int nc) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int row = L.row + 8 * half;
+    uint32_t w = 0xFF80FF80u;
+    if (row < nc) {
+      const uint32_t b = __bfloat16_as_ushort(gs[row * gstride]);
+      w = b | (b << 16);
+    }
+    *reinterpret_cast<uint4*>(tile + L.soff + 2048 * half) = make_uint4(w, w, w, w);
+  }
+}
 // q, k and g_raw of one chunk (pointers at its first token, head h): the first
-// cp.async group of its raw tiles
+// cp.async group of its raw tiles.  gstride > 0: g_raw is one value per token
+// and head (token stride gstride), broadcast over the key channels.
 __device__ __forceinline__ void issue_qkg_loads(const TileLoader& L, uint8_t* raw,
                                                 const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                                const __nv_bfloat16* g, int nc) {
+                                                const __nv_bfloat16* g, int nc,
+                                                int64_t gstride = 0) {
   L.load(raw + RAW_Q * 4096, q, nc, 0u);
   L.load(raw + RAW_K * 4096, k, nc, 0u);
   // g_raw rows past the end hold -inf: sigma(-inf) = 0 gives a = 2^0 = 1 exactly,
   // so those tokens neither decay nor change the running products
-  L.load(raw + RAW_G * 4096, g, nc, 0xFF80FF80u);
+  if (gstride > 0)
+    broadcast_gate_tile(L, raw + RAW_G * 4096, g, gstride, nc);
+  else
+    L.load(raw + RAW_G * 4096, g, nc, 0xFF80FF80u);
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 // v of one chunk into a v buffer: the second group

@@ -64,6 +64,20 @@ __host__ __device__ constexpr int u_offset(int c, int i) {
 }
 __host__ __device__ constexpr int aqk_offset(int i, int j) { return ka_offset(128 + i, j); }
 
+// Per-call options of the forward pass (uniform over the grid).
+struct FwdOpts {
+  int state_bf16;   // initial / final states are bf16 instead of fp32
+  int gate_scalar;  // g_raw is one value per token and head [T_total, H]
+};
+
+// Address of element `elem` of a state buffer of fp32 (or bf16) entries; null stays null.
+__device__ __forceinline__ const void* state_at(const void* base, int64_t elem, bool bf16) {
+  return base ? static_cast<const uint8_t*>(base) + elem * (bf16 ? 2 : 4) : nullptr;
+}
+__device__ __forceinline__ void* state_at(void* base, int64_t elem, bool bf16) {
+  return base ? static_cast<uint8_t*>(base) + elem * (bf16 ? 2 : 4) : nullptr;
+}
+
 // ---------------------------------------------------------------------------
 // small PTX wrappers
 // ---------------------------------------------------------------------------

@@ -55,12 +55,13 @@ __device__ __forceinline__ bool chunk_all(bool pred) {
   return r != 0;
 }
 
+template <bool kGateScalar>
 __global__ void __launch_bounds__(F_THREADS, 2)
 fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e, float eps,
-             const float* __restrict__ init, const int32_t* __restrict__ cu, int64_t T_total,
-             int H, int N, __nv_bfloat16* __restrict__ out, float* __restrict__ final_state,
+             const void* init, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
+             __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts,
              int* __restrict__ err) {
   constexpr int NST = F_NST;
   extern __shared__ uint8_t smem_raw[];
@@ -95,7 +96,8 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
   const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
   if (w < 4)
-    load_state(tb, lane_off, init ? init + state_base + static_cast<int64_t>(t) * kDim : nullptr);
+    load_state(tb, lane_off, state_at(init, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+               opts.state_bf16);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -112,6 +114,9 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     uint8_t* vt = smem + F_V_OFF;
     const int64_t row_stride = static_cast<int64_t>(H) * kDim;
     const TileLoader loader(tc, row_stride);
+    // g_raw of head h: per channel [T, H, 128], or one value per token [T, H]
+    const int64_t gstride = kGateScalar ? H : row_stride;
+    const __nv_bfloat16* g0 = g + (kGateScalar ? h : static_cast<int64_t>(h) * kDim);
     auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
       t0 = bos + static_cast<int64_t>(c) * kChunk;
       nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
@@ -121,7 +126,8 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       int nc;
       chunk_geom(c, t0, nc);
       const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      issue_qkg_loads(loader, rawbuf(c), q + base, k + base, g + base, nc);
+      issue_qkg_loads(loader, rawbuf(c), q + base, k + base, g0 + t0 * gstride, nc,
+                      kGateScalar ? gstride : 0);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
     clear_chunk_workspace(CS, tc);
@@ -166,37 +172,52 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
-               final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-               err, smem + F_OST_OFF, release);
+               state_at(final_state, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+               opts.state_bf16, err, smem + F_OST_OFF, release);
   }
   tc_fence_before();
   __syncthreads();
   if (w == 0) tmem_dealloc(tb, TM_COLS);
 }
 
-cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
-                         const void* beta_raw, float scale, float lower_bound, float eps,
-                         const float* init, const int32_t* cu, int64_t T_total, int H, int N,
-                         void* out, float* final_state, int* err, cudaStream_t stream) {
+template <bool kGateScalar>
+cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta_raw, float scale, float lower_bound, float eps,
+                           const void* init, const int32_t* cu, int64_t T_total, int H, int N,
+                           void* out, void* final_state, FwdOpts opts, int* err,
+                           cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     // the register split above is only safe if every thread starts with F_REGS
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<kGateScalar>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != F_REGS) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
+    e = cudaFuncSetAttribute(fused_kernel<kGateScalar>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units == 0) return cudaSuccess;
-  fused_kernel<<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
+  fused_kernel<kGateScalar><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
       static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, err);
+      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
+                         const void* beta_raw, float scale, float lower_bound, float eps,
+                         const void* init, const int32_t* cu, int64_t T_total, int H, int N,
+                         void* out, void* final_state, FwdOpts opts, int* err,
+                         cudaStream_t stream) {
+  return opts.gate_scalar
+             ? launch_fused_t<true>(q, k, v, g, beta_raw, scale, lower_bound, eps, init, cu,
+                                    T_total, H, N, out, final_state, opts, err, stream)
+             : launch_fused_t<false>(q, k, v, g, beta_raw, scale, lower_bound, eps, init, cu,
+                                     T_total, H, N, out, final_state, opts, err, stream);
 }
 
 }  // namespace kda

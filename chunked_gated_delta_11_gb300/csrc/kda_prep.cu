@@ -19,7 +19,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
                   const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e,
                   float eps, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
-                  uint8_t* __restrict__ ws, int64_t n_items) {
+                  uint8_t* __restrict__ ws, int64_t n_items, int gate_scalar) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PrepSmem& P = *reinterpret_cast<PrepSmem*>(smem_raw);
   const int t = threadIdx.x;
@@ -50,7 +50,10 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     return false;
   };
   auto start = [&](const Item& it) -> uint32_t {
-    issue_qkg_loads(loader, P.raw, q + it.base, k + it.base, g + it.base, it.nc);
+    if (gate_scalar)
+      issue_qkg_loads(loader, P.raw, q + it.base, k + it.base, g + it.t0 * H + it.h, it.nc, H);
+    else
+      issue_qkg_loads(loader, P.raw, q + it.base, k + it.base, g + it.base, it.nc);
     return (t < it.nc) ? __bfloat16_as_ushort(beta_raw[(it.t0 + t) * H + it.h]) : 0u;
   };
 
@@ -82,7 +85,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
 cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const void* g,
                               const void* beta_raw, float scale, float lower_bound, float eps,
                               const int32_t* cu, int64_t T_total, int H, int N, void* ws,
-                              int sm_count, cudaStream_t stream) {
+                              int gate_scalar, int sm_count, cudaStream_t stream) {
   const int64_t n_items = slot_count(T_total, N) * H;
   const int smem = static_cast<int>(sizeof(PrepSmem));
   static bool attr_done = false;  // per process; the attribute is per function
@@ -102,7 +105,7 @@ cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
       static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      cu, T_total, H, N, static_cast<uint8_t*>(ws), n_items);
+      cu, T_total, H, N, static_cast<uint8_t*>(ws), n_items, gate_scalar);
   return cudaGetLastError();
 }
 

@@ -19,9 +19,9 @@ constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) 
 static_assert(2 * (K2_SMEM + 1024) <= 228 * 1024, "recurrence kernel must fit two CTAs per SM");
 
 __global__ void __launch_bounds__(K2_THREADS, 2)
-recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init,
+recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
                   const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
-                  __nv_bfloat16* __restrict__ out, float* __restrict__ final_state,
+                  __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts,
                   int* __restrict__ err) {
   constexpr int NST = K2_NST;
   extern __shared__ uint8_t smem_raw[];
@@ -57,7 +57,8 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   const uint32_t tb = ctl->tmem;
   const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
   const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
-  load_state(tb, lane_off, init ? init + state_base + static_cast<int64_t>(t) * kDim : nullptr);
+  load_state(tb, lane_off, state_at(init, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+             opts.state_bf16);
   int issued = 0;
   if (t == 0) {
     const int pre = nchunks < NST ? nchunks : NST;
@@ -81,8 +82,8 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
     }
   };
   state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
-             final_state ? final_state + state_base + static_cast<int64_t>(t) * kDim : nullptr,
-             err, smem + K2_OST_OFF, refill);
+             state_at(final_state, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+             opts.state_bf16, err, smem + K2_OST_OFF, refill);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory
     for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)
@@ -93,9 +94,9 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const float* __restrict__ init
   if (w == 0) tmem_dealloc(tb, TM_COLS);
 }
 
-cudaError_t launch_recurrence(const void* ws, const float* init, const int32_t* cu,
-                              int64_t T_total, int H, int N, void* out, float* final_state,
-                              int* err, cudaStream_t stream) {
+cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
+                              int64_t T_total, int H, int N, void* out, void* final_state,
+                              FwdOpts opts, int* err, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(recurrence_kernel,
@@ -107,7 +108,7 @@ cudaError_t launch_recurrence(const void* ws, const float* init, const int32_t* 
   if (units == 0) return cudaSuccess;
   recurrence_kernel<<<static_cast<unsigned>(units), K2_THREADS, K2_SMEM, stream>>>(
       static_cast<const uint8_t*>(ws), init, cu, T_total, H, N,
-      static_cast<__nv_bfloat16*>(out), final_state, err);
+      static_cast<__nv_bfloat16*>(out), final_state, opts, err);
   return cudaGetLastError();
 }
 

@@ -77,16 +77,25 @@ __device__ __forceinline__ bool state_all(bool pred) {
   return r != 0;
 }
 
-// Initial state (or zeros) -> tensor memory.  State threads only (t < 128).
-__device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off,
-                                           const float* __restrict__ src) {
+// Initial state row (fp32, or bf16 if `bf16`; null = zeros) -> tensor memory.
+// State threads only (t < 128).
+__device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off, const void* src,
+                                           bool bf16) {
 #pragma unroll
   for (int qd = 0; qd < 4; ++qd) {
     uint32_t r[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
-      const float4 x = src ? __ldg(reinterpret_cast<const float4*>(src + qd * 32 + i))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (src && bf16) {
+        const uint2 b = __ldg(reinterpret_cast<const uint2*>(
+            static_cast<const __nv_bfloat16*>(src) + qd * 32 + i));
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+        x = make_float4(lo.x, lo.y, hi.x, hi.y);
+      } else if (src) {
+        x = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(src) + qd * 32 + i));
+      }
       r[i] = __float_as_uint(x.x);
       r[i + 1] = __float_as_uint(x.y);
       r[i + 2] = __float_as_uint(x.z);
@@ -155,15 +164,17 @@ __device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* b
 // also issues every MMA.  `ring` is the 1024-aligned record ring (stage stride
 // REC_STRIDE_SMEM).  On thread 0, `stage_free(c, s)` runs once all MMAs of
 // record c are done and every state thread has finished reading it.
+// `final_dst` is thread v's row of the final state (fp32, or bf16 if
+// `state_bf16`; null = not written).
 // `ostage` is 4 KB of shared memory (1 KB per state warp) that turns each
 // warp's 16 x 32 output tile into 16-byte stores.
 template <int NST, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
-                                           __nv_bfloat16* __restrict__ out,
-                                           float* __restrict__ final_dst, int* err,
-                                           uint8_t* ostage, StageFree&& stage_free) {
+                                           __nv_bfloat16* __restrict__ out, void* final_dst,
+                                           bool state_bf16, int* err, uint8_t* ostage,
+                                           StageFree&& stage_free) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   // chunk 0: snapshot the initial state and apply chunk 0's decay
@@ -279,10 +290,16 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(final_dst + qd * 32 + i) =
-            make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                        __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+      for (int i = 0; i < 32; i += 4) {
+        if (state_bf16)
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(final_dst) + qd * 32 + i) =
+              make_uint2(pack_bf16(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                         pack_bf16(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+        else
+          *reinterpret_cast<float4*>(static_cast<float*>(final_dst) + qd * 32 + i) =
+              make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                          __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+      }
     }
   }
 }

@@ -21,6 +21,8 @@ Workloads (all D = d_k = d_v = 128, lower_bound = -5, scale = 128 ** -0.5):
  slow    unscored stress variant of ``long`` with g_raw ~ N(-6, 1), i.e.
          retention close to 1 (long-range accumulation)
  b2      profiling size: 2 sequences of 8192 tokens, H = 32
+ decode  one serving step: 256 sequences of 1 token, H = 32, initial states
+         ~ 0.02 N(0, 1) (the decode regime: moving the states dominates)
 ======  =====================================================================
 
 Draw order is q, k, v, g_raw, beta_raw, initial_state; sequence lengths come
@@ -61,6 +63,8 @@ WORKLOADS = {
     "slow": Workload("slow", H=32, N=1, T=131072, init_std=None, g_mean=-6.0, seed=5),
     # profiling size: like b8 with 2 sequences (inputs 537 MB, still larger than L2)
     "b2": Workload("b2", H=32, N=2, T=8192, init_std=None, seed=6),
+    # one decode step of a serving batch: 256 sequences x 1 new token, states in/out
+    "decode": Workload("decode", H=32, N=256, T=1, init_std=0.02, seed=7),
 }
 
 

@@ -94,6 +94,52 @@ kda_status kda_fwd_fused(const void* q, const void* k, const void* v, const void
                          int32_t H, int32_t N, int32_t D, void* out, float* final_state,
                          void* stream);
 
+/* The same forward pass in the recurrent (decode) schedule: the token-by-token
+ * recurrence of "You Could Have Come Up with Kimi Delta Attention" (sec. 4,
+ * boxed), run as in its sec. 5 decode regime.  One CTA per (sequence, head, 32
+ * value rows) keeps that slice of the fp32 state in registers and walks the
+ * sequence's tokens in order.  Meant for short sequences and stateful serving
+ * (a few tokens per sequence per call), where moving the state dominates; for
+ * long sequences kda_fwd_fused is the faster schedule of the same result.
+ * Same arguments, results and errors as kda_fwd_fused.  final_state may be the
+ * same buffer as initial_state (updated in place).  Results agree with the
+ * chunkwise entry points to rounding. */
+kda_status kda_decode(const void* q, const void* k, const void* v, const void* g_raw,
+                      const void* beta_raw, float scale, float lower_bound,
+                      const float* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                      int32_t H, int32_t N, int32_t D, void* out, float* final_state,
+                      void* stream);
+
+/* Options of kda_forward. */
+enum { KDA_SCHEDULE_SPLIT = 0, KDA_SCHEDULE_FUSED = 1, KDA_SCHEDULE_DECODE = 2 };
+enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 };
+enum { KDA_GATE_PER_CHANNEL = 0, KDA_GATE_PER_HEAD = 1 };
+typedef struct {
+  int32_t schedule;     /* KDA_SCHEDULE_*: kda_fwd (split), kda_fwd_fused, kda_decode */
+  int32_t state_dtype;  /* KDA_STATE_*: dtype of initial_state and final_state (both) */
+  int32_t gate;         /* KDA_GATE_*: g_raw [T_total, H, D] or [T_total, H] */
+} kda_options;
+
+/* The forward pass with options, on any schedule.
+ * state_dtype = KDA_STATE_BF16: initial_state and final_state are bf16
+ *   [N, H, V, K] (16-byte aligned), converted to and from the fp32 state at
+ *   load and store; both have that dtype, as the FlashKDA API requires of a
+ *   given pair ("FlashKDA: MoonshotAI's High-Performance Kimi Delta Attention
+ *   Kernels", API reference).  The state itself stays fp32 inside the pass.
+ * gate = KDA_GATE_PER_HEAD: g_raw is bf16 [T_total, H] (2-byte aligned), one
+ *   gate per token and head shared by every key channel, so alpha_t is a scalar
+ *   times the identity: the Gated DeltaNet special case of KDA ("You Could
+ *   Have Come Up with Kimi Delta Attention", sec. 3), with the same gate map
+ *   log alpha = lower_bound * sigmoid(g_raw).
+ * workspace / workspace_bytes are used by KDA_SCHEDULE_SPLIT only (as in
+ * kda_fwd).  Everything else is as in kda_fwd; a null `opts` or an unknown
+ * option value returns KDA_ERR_INVALID_ARG. */
+kda_status kda_forward(const kda_options* opts, const void* q, const void* k, const void* v,
+                       const void* g_raw, const void* beta_raw, float scale, float lower_bound,
+                       const void* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                       int32_t H, int32_t N, int32_t D, void* out, void* final_state,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the fixed workspace array used by kda_fwd_noalloc (64 MiB). */
 #define KDA_NOALLOC_WORKSPACE_BYTES (64 * 1024 * 1024)
 
@@ -105,8 +151,8 @@ kda_status kda_fwd_fused(const void* q, const void* k, const void* v, const void
  * records go to a fixed 64 MiB device array inside libkda, which every GPU that
  * loads the library's device code holds until the process exits.
  * Limit: kda_workspace_size(T_total, H, N, D) must not exceed
- * KDA_NOALLOC_WORKSPACE_BYTES (e.g. T_total + 16 (N + 1) <= 976 tokens at
- * H = 32, <= 31,296 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
+ * KDA_NOALLOC_WORKSPACE_BYTES (e.g. T_total + 16 (N + 1) <= 1280 tokens at
+ * H = 32, <= 41,120 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
  * anything is launched.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, with that device current), so make

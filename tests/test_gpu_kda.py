@@ -288,7 +288,7 @@ def test_host_buffer_entry_point_grouped(path):
     out, fs = kda.kda_forward_host(host["q"], host["k"], host["v"], host["g_raw"],
                                    host["beta_raw"], inp["scale"], inp["lower_bound"],
                                    host["initial_state"], inp["cu_seqlens"], groups=3,
-                                   fused=path == "fused")
+                                   schedule=path)
     torch.cuda.synchronize()
     od, sd = run(to_dev(inp), path)
     assert torch.equal(out, od.cpu()) and torch.equal(fs, sd.cpu())
