@@ -10,19 +10,24 @@
 //   O    = Qdec S_c^T + Aqk E^T        (chunk outputs, sec. 6.5)
 //   S'   = S_c Diag(dlast) + E Kend    (state fast-forward, sec. 6.4)
 //
+// The key-side factors carry a per-token rescaling D = diag(rk), rk_j =
+// 1 / |k_j|, that cancels in these products: the record holds W' = D W,
+// U' = D U (so the recurrence forms E'^T = D E^T), Kend' = D^-1 Kend = the
+// unnormalised k_j D_{j+1:last}, and Aqk' = Aqk D^-1.
+//
 // Byte layout of one record (REC_BYTES):
-//   [OFF_B1, +8192)    [Qdec ; W], 32 rows x 128 key channels, bf16, K-major
+//   [OFF_B1, +8192)    [Qdec ; W'], 32 rows x 128 key channels, bf16, K-major
 //                      with the 128-byte swizzle: 2 blocks of 64 channels, each
 //                      32 rows x 128 B; row n of block kb at kb*4096 + n*128,
 //                      its 16-byte piece c at (c ^ (n & 7))*16.
-//                      Rows 0..15 are Qdec, rows 16..31 are W.
-//   [OFF_KA, +9216)    [Kend ; Aqk] fp32 (the tensor core reads its tf32
+//                      Rows 0..15 are Qdec, rows 16..31 are W'.
+//   [OFF_KA, +9216)    [Kend' ; Aqk'] fp32 (the tensor core reads its tf32
 //                      part), 144 rows r x 16 tokens j as two K=8 tiles (j 0-7,
 //                      j 8-15) of 4608 B, K-major with the 32-byte swizzle: row
 //                      r at r*32, 16-byte piece p at (p ^ ((r >> 2) & 1))*16.
-//                      Rows 0..127 are Kend[j][d] (r = d), rows 128..143 are
-//                      Aqk[i][j] (r = 128 + i; chi_ij for j <= i, zero above).
-//   [OFF_U,  +8192)    U^T fp32 [128 value channels c][16 tokens i], 64 B per
+//                      Rows 0..127 are Kend'[j][d] (r = d), rows 128..143 are
+//                      Aqk'[i][j] (r = 128 + i; zero above the diagonal).
+//   [OFF_U,  +8192)    U'^T fp32 [128 value channels c][16 tokens i], 64 B per
 //                      row c; its four 16-byte pieces (4 tokens each) in the
 //                      order p ^ (2 * ((c >> 1) & 1)).
 //   [OFF_DL, +512)     dlast fp32 [128] = diagonal of D_{0:C-1}.

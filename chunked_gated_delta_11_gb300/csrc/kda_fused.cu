@@ -130,7 +130,6 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
                       kGateScalar ? gstride : 0);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
-    clear_chunk_workspace(CS, tc);
     uint32_t bbits[2] = {0u, 0u};  // beta_raw bits of chunks c and c+1
     if (nchunks > 0) bbits[0] = start(0);
     if (nchunks > 1) bbits[1] = start(1);

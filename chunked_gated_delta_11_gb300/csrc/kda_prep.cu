@@ -25,7 +25,6 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int t = threadIdx.x;
   const int64_t row_stride = static_cast<int64_t>(H) * kDim;
   const TileLoader loader(t, row_stride);
-  clear_chunk_workspace(P.chunk, t);
 
   // the next used slot at or after `item` on this CTA's grid stride
   struct Item {

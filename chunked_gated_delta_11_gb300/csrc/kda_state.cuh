@@ -5,18 +5,19 @@
 //
 // One CTA owns one (sequence, head) unit.  Its 128 x 128 fp32 state S lives in
 // tensor memory, row v in lane v, next to a bf16 snapshot Sb of it.  For each
-// chunk record c (layout in kda_common.cuh), with S = S_c Diag(dlast_c)
-// already applied and Sb = bf16(S_c):
+// chunk record c (layout in kda_common.cuh: W', U', Kend', Aqk' carry the
+// per-token key-norm rescaling D that cancels in the products below), with
+// S = S_c Diag(dlast_c) already applied and Sb = bf16(S_c):
 //
 //   MMA1 (tcgen05 kind::f16, bf16, M=128 N=32 K=128, 8 instructions):
-//        D1[v][n] = sum_d Sb[v][d] B1[n][d],  B1 = [Qdec ; W]
-//        -> D1[v][i] = (Qdec S_c^T)[i][v],  D1[v][16+i] = (W S_c^T)[i][v]
+//        D1[v][n] = sum_d Sb[v][d] B1[n][d],  B1 = [Qdec ; W']
+//        -> D1[v][i] = (Qdec S_c^T)[i][v],  D1[v][16+i] = (W' S_c^T)[i][v]
 //   state threads (thread v = row v):
-//        e[v][i] = U[i][v] - D1[v][16+i]    (corrected errors, sec. 6.3)
-//        E^T -> tensor memory (fp32; the MMA reads its tf32 part)
+//        e'[v][i] = U'[i][v] - D1[v][16+i]    (corrected errors D E^T, sec. 6.3)
+//        E'^T -> tensor memory (fp32; the MMA reads its tf32 part)
 //   MMA2 (kind::tf32, M=128 N=144 K=16, 2 instructions), D = [S | D1 cols 0-15]:
-//        S[v][d]    += sum_j E^T[v][j] Kend[j][d]          (write, sec. 6.4)
-//        D1[v][i]   += sum_j E^T[v][j] Aqk[i][j]  -> o[i][v] (read, sec. 6.5)
+//        S[v][d]    += sum_j E'^T[v][j] Kend'[j][d]        (write, sec. 6.4)
+//        D1[v][i]   += sum_j E'^T[v][j] Aqk'[i][j]  -> o[i][v] (read, sec. 6.5)
 //   state threads: o read out; then, once record c+1 is there,
 //        Sb = bf16(S) (= bf16(S_{c+1})),  S *= dlast_{c+1}   (forget, sec. 6.4)
 //   while MMA1 of chunk c+1 runs: o -> bf16 -> out.

@@ -174,14 +174,17 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const vo
  *   ((floor(bos_n / 16) + n + c) * H + h) * 26112
  * with bos_n the first token of sequence n, and holds, for the chunk's tokens
  * i < 16 (rows past the sequence end are zero), in this order:
- *   [Qdec ; W] bf16 32 x 128, 128-byte-swizzled K-major tiles;
- *   [Kend ; Aqk] fp32 144 x 16 (Kend^T rows 0-127, Aqk rows 128-143), two
- *   32-byte-swizzled K=8 tiles;  U^T fp32 [128][16];  dlast fp32 [128];
+ *   [Qdec ; W'] bf16 32 x 128, 128-byte-swizzled K-major tiles;
+ *   [Kend' ; Aqk'] fp32 144 x 16 (Kend'^T rows 0-127, Aqk' rows 128-143), two
+ *   32-byte-swizzled K=8 tiles;  U'^T fp32 [128][16];  dlast fp32 [128];
  * where (sec. 6.1-6.6 of "You Could Have Come Up with Kimi Delta Attention")
  *   Qdec_i = scale q^_i D_{0:i},  Kend_i = k^_i D_{i+1:last},
  *   Akk = (I + R)^-1 with R_ij = beta_i <k^_j|D_{j+1:i}|k^_i> (j < i),
  *   W = Akk diag(beta) [k^_i D_{0:i}],  U = Akk diag(beta) V,
- *   Aqk_ij = scale <k^_j|D_{j+1:i}|q^_i> (j <= i),  dlast = diag(D_{0:last}).
+ *   Aqk_ij = scale <k^_j|D_{j+1:i}|q^_i> (j <= i),  dlast = diag(D_{0:last}),
+ * stored with the per-token key norms rk_j = 1 / |k_j| moved between factors
+ * (the products the recurrence forms are unchanged):  W'_i = rk_i W_i,
+ * U'_i = rk_i U_i,  Kend'_j = Kend_j / rk_j,  Aqk'_ij = Aqk_ij / rk_j.
  * The byte layout of each tile is given in chunked_gated_delta_11_gb300/csrc/
  * kda_common.cuh. */
 kda_status kda_chunk_prep(const void* q, const void* k, const void* v, const void* g_raw,

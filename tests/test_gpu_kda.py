@@ -81,7 +81,7 @@ def _ka_offset(r, j):
 
 
 def decode_record(rec):
-    """Record bytes -> factors (layout: [Qdec ; W] bf16, [Kend ; Aqk] fp32, U, dlast)."""
+    """Record bytes -> fields (layout: [Qdec ; W'] bf16, [Kend' ; Aqk'] fp32, U', dlast)."""
     rec = np.asarray(rec, dtype=np.uint8)
     nn, dd = np.meshgrid(np.arange(32), np.arange(128), indexing="ij")
     b1 = (rec.view(np.uint16)[_b1_offset(nn, dd) // 2].astype(np.uint32) << 16).view(np.float32)
@@ -94,6 +94,15 @@ def decode_record(rec):
     return {"Qdec": b1[:16].astype(np.float64), "W": b1[16:].astype(np.float64),
             "Kend": ka[:, :128].astype(np.float64), "Aqk": ka[:, 128:].T.astype(np.float64),
             "U": U, "dlast": dl}
+
+
+def record_convention(f, rk):
+    """The oracle's chunk factors in the record's convention: with D = diag(rk),
+    rk_j = 1 / |k_j| (the key norm of token j), the record holds W' = D W,
+    U' = D U, Kend' = D^-1 Kend and Aqk' = Aqk D^-1, whose products in the
+    recurrence equal the unscaled ones."""
+    return {"Qdec": f["Qdec"], "W": rk[:, None] * f["W"], "U": rk[:, None] * f["U"],
+            "Kend": f["Kend"] / rk[:, None], "Aqk": f["Aqk"] / rk[None, :], "dlast": f["dlast"]}
 
 
 @pytest.mark.parametrize("lengths,H", [([64], 1), ([45], 2), ([7, 0, 33, 16], 2)])
@@ -109,6 +118,7 @@ def test_chunk_records_match_oracle_factors(lengths, H):
                                       f64(inp["beta_raw"]), inp["lower_bound"])
     cu = inp["cu_seqlens"].cpu().numpy()
     f = oracle.chunk_factors(qh, kh, f64(inp["v"]), la, beta, inp["scale"], cu_seqlens=cu)
+    kraw = f64(inp["k"])
     got = {k_: [] for k_ in f if k_ != "Akk"}
     ref = {k_: [] for k_ in got}
     chunk = 0
@@ -118,9 +128,14 @@ def test_chunk_records_match_oracle_factors(lengths, H):
             for h in range(H):
                 slot = bos // 16 + n + c
                 r = decode_record(wsh[(slot * H + h) * kda.REC_BYTES:][:kda.REC_BYTES])
+                kc = np.zeros((16, 128))
+                t0 = bos + 16 * c
+                kc[:min(16, eos - t0)] = kraw[t0:min(t0 + 16, eos), h]
+                rk = 1.0 / np.sqrt((kc * kc).sum(-1) + oracle.DEFAULT_EPS)
+                fr = record_convention({k_: f[k_][chunk, h] for k_ in got}, rk)
                 for key in got:
                     got[key].append(r[key].reshape(-1))
-                    ref[key].append(f[key][chunk, h].reshape(-1))
+                    ref[key].append(fr[key].reshape(-1))
             chunk += 1
     for key in got:
         g_ = np.concatenate(got[key])

@@ -4,12 +4,16 @@ A plain numpy restatement of where the kernels round, written from the
 chunkwise form ("You Could Have Come Up with Kimi Delta Attention", sec. 6)
 and independent of the CUDA sources:
 
-- intra-chunk products Mkk = Kdec Kinv^T, Mqk = Qdec Kinv^T and W = A diag(beta)
-  Kdec with bf16 operands and fp32 accumulation (FlashKDA's chunk-kernel
+- the normalisation applied to the 16 x 16 matrices and per-token rows (rq,
+  rk) instead of the 128-channel factors, which the kernels keep unnormalised
+  (q P, k P, k Q, k / P);
+- intra-chunk products Mkk = kP (k/P)^T, Mqk = qP (k/P)^T and W' = A' diag(beta
+  rk^2) kP with bf16 operands and fp32 accumulation (FlashKDA's chunk-kernel
   precision, "FlashKDA v1: A Deep Dive", sec. 3);
-- U = A diag(beta) V with A diag(beta) as a bf16 high part plus remainder;
-- the Neumann-product inverse as bf16 products of high/low operand splits
-  (high*high + high*low + low*high), fp32 accumulation;
+- A' = (I + R')^-1 in fp32 (forward substitution), R' = strictly-lower(diag(beta
+  rk^2) Mkk);
+- U' = A' diag(beta rk) V with A' diag(beta rk) as a bf16 high part plus
+  remainder;
 - the first recurrence product on bf16 operands (a bf16 snapshot of the fp32
   state times [Qdec; W] stored as bf16, as FlashKDA's bf16 state), fp32
   accumulation;
@@ -84,25 +88,24 @@ def model_forward(inp):
             dl = P[:, -1]
             Qs = np.ones_like(a)
             Qs[:, :-1] = np.cumprod(a[:, ::-1], axis=1, dtype=f32)[:, ::-1][:, 1:]
-            Qd = qq * rq[..., None] * P
-            Kd = kk * rk[..., None] * P
-            Ke = kk * rk[..., None] * Qs
+            Qu = qq * P
+            Ku = kk * P
+            Ke = kk * Qs
             Ki = Ke / dl[:, None, :]
-            Mkk = mm(bf16(Kd), bf16(Ki).transpose(0, 2, 1))
-            Mqk = mm(bf16(Qd), bf16(Ki).transpose(0, 2, 1))
-            R = np.tril(beta[:, :, None] * Mkk, -1)
-            I = np.eye(16, dtype=f32)
-            R2 = mm3(R, R)
-            R4 = mm3(R2, R2)
-            R8 = mm3(R4, R4)
-            P1 = (I - R) + mm3(I - R, R2)
-            P2 = P1 + mm3(P1, R4)
-            A = P2 + mm3(P2, R8)
-            Ab = A * beta[:, None, :]
-            Ab_hi = bf16(Ab)
-            W = mm(Ab_hi, bf16(Kd))
-            U = mm(Ab_hi, vv) + mm(bf16(Ab - Ab_hi), vv)
-            Aqk = np.tril(Mqk)
+            Mkk = mm(bf16(Ku), bf16(Ki).transpose(0, 2, 1))
+            Mqk = mm(bf16(Qu), bf16(Ki).transpose(0, 2, 1))
+            cw = beta * rk * rk
+            cu = beta * rk
+            R = np.tril(cw[:, :, None] * Mkk, -1)
+            I = np.eye(16)
+            A = np.linalg.inv(I + R.astype(np.float64)).astype(f32)
+            Aw = A * cw[:, None, :]
+            Au = A * cu[:, None, :]
+            Au_hi = bf16(Au)
+            W = mm(bf16(Aw), bf16(Ku))
+            U = mm(Au_hi, vv) + mm(bf16(Au - Au_hi), vv)
+            Qd = rq[..., None] * Qu
+            Aqk = np.tril(rq[..., None] * Mqk)
             D1 = mm(bf16(S), bf16(np.concatenate([W, Qd], 1)).transpose(0, 2, 1))
             E = tf32_trunc(U - D1[:, :, :16].transpose(0, 2, 1))
             O = D1[:, :, 16:].transpose(0, 2, 1) + mm(tf32_trunc(Aqk), E)
