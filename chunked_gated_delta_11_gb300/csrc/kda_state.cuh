@@ -139,14 +139,16 @@ __device__ __forceinline__ void snapshot_and_decay(uint32_t tb, uint32_t lane_of
 }
 
 // MMA1 on the record at shared address sb: 8 bf16 K=16 steps into D1.
-// Issuing thread only.
+// Issuing thread only.  The K steps of one 64-channel block are 32 bytes
+// apart and the two blocks 4096 bytes, which moves only the descriptor's
+// start-address field (bits 0-13, in 16-byte units).
 __device__ __forceinline__ void issue_mma1(uint32_t sb, uint32_t tb, uint64_t* bar) {
   const uint32_t id1 = make_idesc(1, 128, 32);
+  const uint64_t bd0 = make_sdesc(sb + OFF_B1, 16, 1024, 2);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t bd = make_sdesc(sb + OFF_B1 + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024, 2);
-    mma_bf16_ts(tb + TM_D1, tb + TM_SB + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
-  }
+  for (int kk = 0; kk < 8; ++kk)
+    mma_bf16_ts(tb + TM_D1, tb + TM_SB + kk * 8, bd0 + static_cast<uint64_t>((kk >> 2) * 256 + (kk & 3) * 2),
+                id1, kk > 0 ? 1u : 0u);
   tc_commit(bar);
 }
 
