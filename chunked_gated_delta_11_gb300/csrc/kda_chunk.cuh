@@ -74,6 +74,7 @@ struct ChunkSmem {
   float Aw[16][AS];  // A' diag(beta rk^2)
   float Au[16][AS];  // A' diag(beta rk)
   float rq[16], rk[16], beta[16];
+  float g2[4][16];  // partial squared norms (warp w: q for w < 2, k otherwise)
 };
 
 __host__ __device__ __forceinline__ constexpr int raw_row_off(int i) {
@@ -255,21 +256,22 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   const int rbase = raw_row_off(8 * hf) + d0 * 2;
   auto roff = [&](int ii) { return rbase + ii * RAW_ROW; };
 
-  // Warp w: Gram tile G[i][j] = sum_d X[i][d] X[j][d] of X = q (w < 2) or k,
-  // columns j = 8 (w & 1) .. +7, of which only the diagonal is kept.  Two
-  // accumulator chains; the gate math below fills their latency.
-  const int nx = (w >> 1) ? RAW_K : RAW_Q, ntn = w & 1;
-  float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  // Warp w: the 16 x 16 Gram matrix G = X X^T of X = q (w < 2) or k over the
+  // channels of k-steps 4 (w & 1) .. +3, of which only the diagonal is kept.
+  // In X X^T the B fragments of each k-step are registers of the A fragment
+  // (rows 0-7: a0, a2; rows 8-15: a1, a3), so one ldmatrix per k-step feeds
+  // both column tiles.  The gate math below fills the MMA latency.
+  const int nx = (w >> 1) ? RAW_K : RAW_Q;
+  float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // column tiles 0, 1
   {
     const int mi = l >> 3;
-    const uint8_t* pa = raw_row(raw, nx, (l & 7) + (mi & 1) * 8) + (mi >> 1) * 16;
-    const uint8_t* pb = raw_row(raw, nx, ntn * 8 + (l & 7)) + (mi & 1) * 16;
+    const uint8_t* pa = raw_row(raw, nx, (l & 7) + (mi & 1) * 8) + (mi >> 1) * 16 + (w & 1) * 128;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a[4], b[2];
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4];
       ldsm_x4(a, pa + kk * 32);
-      ldsm_x2(b, pb + kk * 32);
-      mma16816(gacc[kk & 1], a, b[0], b[1]);
+      mma16816(gacc[0], a, a[0], a[2]);
+      mma16816(gacc[1], a, a[1], a[3]);
     }
   }
   // retention factors of this thread's 8 tokens, two channels each, and their
@@ -289,17 +291,24 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     }
   }
   {
-    // diagonal: lane (g = l >> 2, c = l & 3) holds columns 2c, 2c+1 of rows g
-    // (acc 0, 1) and g + 8 (acc 2, 3) of the tile
+    // diagonal: lane (g = l >> 2, c = l & 3) holds columns 8 nt + 2c, +1 of
+    // rows g (acc 0, 1) and g + 8 (acc 2, 3) of column tile nt; the two warps
+    // of a matrix add their halves of the channels
     const int g = l >> 2, e = g - 2 * (l & 3);
     if (e == 0 || e == 1) {
-      const float s2 = ntn ? (e ? gacc[0][3] + gacc[1][3] : gacc[0][2] + gacc[1][2])
-                           : (e ? gacc[0][1] + gacc[1][1] : gacc[0][0] + gacc[1][0]);
-      const int i = ntn * 8 + g;
+      S.g2[w][g] = e ? gacc[0][1] : gacc[0][0];
+      S.g2[w][g + 8] = e ? gacc[1][3] : gacc[1][2];
+    }
+    if (w < 2)
+      named_bar(3, 64);  // the q pair
+    else
+      named_bar(4, 64);  // the k pair
+    if ((w & 1) == 0 && l < 16) {
+      const float s2 = S.g2[w][l] + S.g2[w + 1][l];
       if (nx == RAW_Q)
-        S.rq[i] = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
+        S.rq[l] = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
       else
-        S.rk[i] = rsqrtf(s2 + eps);
+        S.rk[l] = rsqrtf(s2 + eps);
     }
   }
   // products over the other half from the neighbouring lane

@@ -29,7 +29,7 @@
 //                      Aqk'[i][j] (r = 128 + i; zero above the diagonal).
 //   [OFF_U,  +8192)    U'^T fp32 [128 value channels c][16 tokens i], 64 B per
 //                      row c; its four 16-byte pieces (4 tokens each) in the
-//                      order p ^ (2 * ((c >> 1) & 1)).
+//                      order p ^ (2 ((c >> 1) & 1) + ((c >> 2) & 1)).
 //   [OFF_DL, +512)     dlast fp32 [128] = diagonal of D_{0:C-1}.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
@@ -64,8 +64,12 @@ __host__ __device__ constexpr int ka_offset(int r, int j) {
 }
 __host__ __device__ constexpr int kend_offset(int d, int j) { return ka_offset(d, j); }
 // Byte offset of U^T element (value channel c, token i).
+// The piece order swizzle keeps both the chunk side's stores (rows c, c + 2 of
+// an MMA tile at once) and the state side's row reads (8 consecutive rows)
+// conflict-free.
+__host__ __device__ constexpr int u_piece_swz(int c) { return (((c >> 1) & 1) << 1) | ((c >> 2) & 1); }
 __host__ __device__ constexpr int u_offset(int c, int i) {
-  return OFF_U + c * 64 + ((((i >> 2) ^ (((c >> 1) & 1) << 1))) << 4) + ((i & 3) << 2);
+  return OFF_U + c * 64 + (((i >> 2) ^ u_piece_swz(c)) << 4) + ((i & 3) << 2);
 }
 __host__ __device__ constexpr int aqk_offset(int i, int j) { return ka_offset(128 + i, j); }
 

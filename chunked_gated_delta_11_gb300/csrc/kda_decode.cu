@@ -5,8 +5,11 @@
 // read and write dominate and there are no 16-token chunks to batch.
 //
 // One CTA per (sequence, head, 32 value rows): 256 threads, thread
-// (row r = t / 8, slice s = t % 8) keeps S[32 b + r][16 s .. 16 s + 15] (fp32)
-// in registers for the whole call.  Per token:
+// (row r = t / 8, slice s = t % 8) keeps the 16 entries S[32 b + r][4 (8 j + s) + e]
+// (j, e = 0..3; fp32) in registers for the whole call: four groups of four
+// channels, interleaved over the slices so that the eight slices of a row read
+// eight consecutive 16-byte words of the per-token vectors (no bank conflicts)
+// and their state loads stay coalesced.  Per token:
 //   threads 0-127 (channel c = t): q_c, k_c, g_c -> alpha_c = 2^(lb log2e sigma(g_c));
 //     squared norms reduced over the CTA; k^_c, s q^_c, alpha_c -> shared memory
 //   every thread, on its 16 entries:  S *= alpha  (forget)
@@ -38,31 +41,31 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   const int vrow = tile * DEC_ROWS + r;
   int64_t bos, eos;
   seq_bounds(cu, T_total, N, n, bos, eos);
-  const int64_t sbase = ((static_cast<int64_t>(n) * H + h) * kDim + vrow) * kDim + sl * 16;
+  const int64_t sbase = ((static_cast<int64_t>(n) * H + h) * kDim + vrow) * kDim + sl * 4;
+  // entries 4 j .. 4 j + 3 of s[] are channels 4 (8 j + sl) .. + 3: element offset 32 j
 
   float s[16];
   if (init && opts.state_bf16) {
     const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(init) + sbase;
 #pragma unroll
-    for (int i = 0; i < 16; i += 8) {
-      const uint4 b = *reinterpret_cast<const uint4*>(src + i);
-      const uint32_t wv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
-        s[i + 2 * j] = f.x;
-        s[i + 2 * j + 1] = f.y;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const uint2 b = *reinterpret_cast<const uint2*>(src + 32 * j);
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+      s[4 * j] = lo.x;
+      s[4 * j + 1] = lo.y;
+      s[4 * j + 2] = hi.x;
+      s[4 * j + 3] = hi.y;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const float4 x = init ? *reinterpret_cast<const float4*>(static_cast<const float*>(init) + sbase + i)
+    for (int j = 0; j < 4; ++j) {
+      const float4 x = init ? *reinterpret_cast<const float4*>(static_cast<const float*>(init) + sbase + 32 * j)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      s[i] = x.x;
-      s[i + 1] = x.y;
-      s[i + 2] = x.z;
-      s[i + 3] = x.w;
+      s[4 * j] = x.x;
+      s[4 * j + 1] = x.y;
+      s[4 * j + 2] = x.z;
+      s[4 * j + 3] = x.w;
     }
   }
   const float hl = 0.5f * lb_log2e;
@@ -98,7 +101,7 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     float pred = 0.f;
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4) {
-      const float4 a = sa4[sl * 4 + i4], kk = sk4[sl * 4 + i4];
+      const float4 a = sa4[i4 * 8 + sl], kk = sk4[i4 * 8 + sl];
       s[4 * i4] *= a.x;
       s[4 * i4 + 1] *= a.y;
       s[4 * i4 + 2] *= a.z;
@@ -114,7 +117,7 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
     float o_acc = 0.f;
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4) {
-      const float4 kk = sk4[sl * 4 + i4], qq = sq4[sl * 4 + i4];
+      const float4 kk = sk4[i4 * 8 + sl], qq = sq4[i4 * 8 + sl];
       s[4 * i4] = fmaf(e, kk.x, s[4 * i4]);
       s[4 * i4 + 1] = fmaf(e, kk.y, s[4 * i4 + 1]);
       s[4 * i4 + 2] = fmaf(e, kk.z, s[4 * i4 + 2]);
@@ -132,15 +135,14 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
   if (final_state && opts.state_bf16) {
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(final_state) + sbase;
 #pragma unroll
-    for (int i = 0; i < 16; i += 8)
-      *reinterpret_cast<uint4*>(dst + i) =
-          make_uint4(pack_bf16(s[i], s[i + 1]), pack_bf16(s[i + 2], s[i + 3]),
-                     pack_bf16(s[i + 4], s[i + 5]), pack_bf16(s[i + 6], s[i + 7]));
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint2*>(dst + 32 * j) =
+          make_uint2(pack_bf16(s[4 * j], s[4 * j + 1]), pack_bf16(s[4 * j + 2], s[4 * j + 3]));
   } else if (final_state) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 4)
-      *reinterpret_cast<float4*>(static_cast<float*>(final_state) + sbase + i) =
-          make_float4(s[i], s[i + 1], s[i + 2], s[i + 3]);
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<float4*>(static_cast<float*>(final_state) + sbase + 32 * j) =
+          make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
   }
 }
 

@@ -205,7 +205,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tmem_ld16(tb + TM_D1 + 16 + lane_off, d1);
       tmem_wait_ld();
       const float4* U4 = reinterpret_cast<const float4*>(st + OFF_U + v * 64);
-      const int usw = ((v >> 1) & 1) << 1;  // piece order of row v (u_offset)
+      const int usw = u_piece_swz(v);  // piece order of row v (u_offset)
       uint32_t pk[16];
       // (the tensor core reads the tf32 part of these fp32 values)
       const float2 m1 = make_float2(-1.f, -1.f);

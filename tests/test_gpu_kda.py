@@ -88,7 +88,8 @@ def decode_record(rec):
     jj, rr = np.meshgrid(np.arange(16), np.arange(144), indexing="ij")
     ka = rec.view(np.float32)[_ka_offset(rr, jj) // 4]          # [j][r]
     cc, ii_ = np.meshgrid(np.arange(128), np.arange(16), indexing="ij")
-    uoff = 17408 + cc * 64 + ((((ii_ >> 2) ^ (((cc >> 1) & 1) << 1))) << 4) + ((ii_ & 3) << 2)
+    swz = (((cc >> 1) & 1) << 1) | ((cc >> 2) & 1)
+    uoff = 17408 + cc * 64 + (((ii_ >> 2) ^ swz) << 4) + ((ii_ & 3) << 2)
     U = rec.view(np.float32)[uoff // 4].T
     dl = rec[25600:26112].view(np.float32)
     return {"Qdec": b1[:16].astype(np.float64), "W": b1[16:].astype(np.float64),
