@@ -51,6 +51,15 @@ PATH_TEXT = {
 PATH_KERNEL = {"fused": "fused_kernel (the whole step)", "split": "whole kda_fwd step (K1 + K2)",
                "decode": "decode_kernel (the whole step)"}
 PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, from one ncu capture of the current kernels.  The b8 figure
+# is four times the b2 capture: b8 processes four times the units, and the
+# traffic is the per-unit inputs, outputs and states.  Absent = not captured.
+MEASURED_TRAFFIC = {
+    ("b2", "fused"): 538.108160e6 + 120.551424e6,
+    ("b8", "fused"): 4 * (538.108160e6 + 120.551424e6),
+    ("decode", "decode"): 545.430784e6 + 491.330816e6,
+}
 
 
 def load_peaks():
@@ -368,7 +377,7 @@ def main():
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": None,
+            "frac": achieved / hbm, "traffic": MEASURED_TRAFFIC.get((args.workload, args.path)),
             "kernel": PATH_KERNEL[args.path],
             "alg_bytes_per_launch": alg_bytes, "alg_flop_per_launch": alg_flop,
             "tensor_frac": alg_flop / (ms * 1e-3) / 1e12 / tc,
