@@ -95,20 +95,22 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(p)));
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_u32(p)));
-}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_u32(p)));
 }
-__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const void* p) {
+// the same loads from a 32-bit shared-memory address (constant offsets fold
+// into the instruction)
+__device__ __forceinline__ void ldsm_x4_t_at(uint32_t (&r)[4], uint32_t a) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2_t_at(uint32_t (&r)[2], uint32_t a) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
                : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_u32(p)));
+               : "r"(a));
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -371,16 +373,16 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   // ---- Mkk (warps 0,1) -> -R'^T, Mqk (warps 2,3) -> Aqk'; Qdec -> record ----
   {
     const int mat = w >> 1, nt = w & 1;
-    const uint8_t* A = mat ? S.qd : S.kd;
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // even / odd k-steps
     const int mi = l >> 3;
+    // channel rows kk*16 + r of the tiles are drv_off(r, h) + 512 kk
+    const uint32_t abase = smem_u32(mat ? S.qd : S.kd) + drv_off((l & 7) + (mi >> 1) * 8, mi & 1);
+    const uint32_t bbase = smem_u32(S.ki) + drv_off((l & 7) + (mi & 1) * 8, nt);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const int arow = kk * 16 + (l & 7) + (mi >> 1) * 8;  // channel
-      const int brow = kk * 16 + (l & 7) + (mi & 1) * 8;
       uint32_t ar[4], br[2];
-      ldsm_x4_t(ar, A + drv_off(arow, mi & 1));
-      ldsm_x2_t(br, S.ki + drv_off(brow, nt));
+      ldsm_x4_t_at(ar, abase + kk * 512);
+      ldsm_x2_t_at(br, bbase + kk * 512);
       mma16816(acc2[kk & 1], ar, br[0], br[1]);
     }
     // Qdec = diag(rq) qP, bf16 rows 0..15 of [Qdec ; W'] (this thread's pairs)
