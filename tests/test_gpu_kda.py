@@ -320,3 +320,27 @@ def test_fused_agrees_with_split_on_b8():
     assert_close(f64(o2), f64(o1), "fused vs split out")
     assert_close(f64(s2), f64(s1), "fused vs split state")
     print(f"[parity] fused vs split bit-identical: out {torch.equal(o1, o2)} state {torch.equal(s1, s2)}")
+
+
+# Zero query / key rows: the key norm factor rk = 1 / sqrt(0 + eps) is at its
+# largest (1e3), which the record's rescaled factors (W' = D W, U' = D U,
+# Kend' = D^-1 Kend) must carry without loss; a zero key row contributes
+# nothing to the state and a zero query row reads nothing.
+@pytest.mark.parametrize("path", PATHS + ["decode"])
+def test_zero_query_and_key_rows(path):
+    inp = synth.make_inputs(0, 2, lengths=[40, 19], seed=21, init_std=0.02)
+    for t_, h_ in ((5, 0), (20, 1), (39, 0), (41, 1), (58, 0)):
+        inp["k"][t_, h_] = 0
+    for t_, h_ in ((7, 1), (20, 0), (45, 1)):
+        inp["q"][t_, h_] = 0
+    inp = to_dev(inp)
+    if path == "decode":
+        out, fs = kda.kda_decode(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                                 inp["scale"], inp["lower_bound"], inp["initial_state"],
+                                 inp["cu_seqlens"], N=inp["N"])
+        assert kda.kda_device_status() == 0
+    else:
+        out, fs = run(inp, path)
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "out")
+    assert_close(f64(fs), rs, "final_state")
