@@ -47,10 +47,13 @@ PATH_TEXT = {
     "fused": "kda_fwd_fused = fused_kernel (chunk math + tcgen05 recurrence, one launch)",
     "split": "kda_fwd = chunk_prep_kernel (K1) + recurrence_kernel (K2, tcgen05)",
     "decode": "kda_decode = decode_kernel (token-by-token recurrence, state slices in registers)",
+    "segmented": "kda_fwd_segmented = seg_plan_kernel + fused_kernel (every sequence in P pieces, "
+                 "X and M roles) + affine_scan_kernel + seg_fixup_kernel",
 }
 PATH_KERNEL = {"fused": "fused_kernel (the whole step)", "split": "whole kda_fwd step (K1 + K2)",
-               "decode": "decode_kernel (the whole step)"}
-PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1}
+               "decode": "decode_kernel (the whole step)",
+               "segmented": "whole kda_fwd_segmented step (4 launches)"}
+PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # dominant kernel, from one ncu capture of the current kernels.  The b8 figure
 # is four times the b2 capture: b8 processes four times the units, and the
@@ -234,10 +237,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b8")
-    ap.add_argument("--path", choices=["fused", "split", "decode"], default=None,
+    ap.add_argument("--path", choices=["fused", "split", "decode", "segmented"], default=None,
                     help="fused: kda_fwd_fused (one kernel); split: kda_fwd (K1 + K2); decode: "
-                         "kda_decode (recurrent schedule).  Default: decode for the decode "
-                         "workload, fused otherwise")
+                         "kda_decode (recurrent schedule); segmented: kda_fwd_segmented (every "
+                         "sequence in pieces joined by a scan of their state maps, automatic "
+                         "piece count).  Default: decode for the decode workload, fused "
+                         "otherwise")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=0,
                     help="oracle sample size for cpu_baseline (0 = one unit per core)")
@@ -278,7 +283,16 @@ def main():
 
     if args.path is None:
         args.path = "decode" if args.workload == "decode" else "fused"
-    step = {"fused": step_fused, "split": step_split, "decode": step_decode}[args.path]
+    segments = kda.kda_segments_auto(T, H, N) if args.path == "segmented" else 1
+    ws_seg = torch.empty(max(1, kda.kda_segmented_workspace_size(T, H, N, segments=segments)),
+                         dtype=torch.uint8, device="cuda") if args.path == "segmented" else None
+
+    def step_segmented():
+        kda.kda_fwd_segmented(*a, N=N, segments=segments, out=out, final_state=fs,
+                              workspace=ws_seg, stream=stream)
+
+    step = {"fused": step_fused, "split": step_split, "decode": step_decode,
+            "segmented": step_segmented}[args.path]
 
     for _ in range(args.warmup):
         step()
@@ -301,7 +315,7 @@ def main():
 
     # the other path, and the split path's per-kernel durations, on the same stream
     reps = max(10, min(args.steps, 50))
-    other = step_split if args.path == "fused" else step_fused
+    other = step_split if args.path in ("fused",) else step_fused
     for _ in range(3):
         other()
     ev0.record(stream)
@@ -369,6 +383,7 @@ def main():
         "data": "synthetic",
         "config": {
             "workload": f"{args.workload}: {WORKLOAD_TEXT.get(args.workload, '')}",
+            **({"segments": segments} if args.path == "segmented" else {}),
             "global_batch": N * world, "seq_len": T // N if inp["cu_seqlens"] is None else None,
             "heads": H, "head_dim": 128, "tokens_per_step": tokens_per_step,
             "l2": ("states larger than L2 (no flush)" if args.workload == "decode"
@@ -390,6 +405,8 @@ def main():
                            (other_ms if args.path == "fused" else None),
                            "chunk_prep_kernel_ms": k1_ms, "recurrence_kernel_ms": k2_ms},
             **({"decode_kernel": {"ms": ms}} if args.path == "decode" else {}),
+            **({"segmented_path": {"ms": ms, "segments": segments}}
+               if args.path == "segmented" else {}),
         },
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {

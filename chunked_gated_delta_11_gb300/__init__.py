@@ -23,7 +23,8 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
-    "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc", "REC_BYTES", "CHUNK", "HEAD_DIM",
+    "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc",
+    "kda_fwd_segmented", "kda_segments_auto", "kda_segmented_workspace_size", "REC_BYTES", "CHUNK", "HEAD_DIM",
 ]
 
 CHUNK = 16
@@ -89,6 +90,13 @@ def load(build_if_missing: bool = False):
         lib.kda_device_status.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_fwd_segmented.argtypes = [P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P,
+                                          P, i32, i32, P, sz, P]
+        lib.kda_fwd_segmented.restype = ctypes.c_int
+        lib.kda_segmented_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+        lib.kda_segmented_workspace_size.restype = sz
+        lib.kda_segments_auto.argtypes = [i64, i32, i32]
+        lib.kda_segments_auto.restype = i32
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]
         lib.kda_selftest_tcgen05.restype = ctypes.c_int
         _lib = lib
@@ -269,6 +277,53 @@ def kda_forward(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None
     return out, final_state
 
 
+def kda_segments_auto(T_total: int, H: int, N: int) -> int:
+    """Pieces per sequence kda_fwd_segmented picks by itself on the current device."""
+    return int(load().kda_segments_auto(int(T_total), int(H), int(N)))
+
+
+def kda_segmented_workspace_size(T_total: int, H: int, N: int, segments: int = 0,
+                                 D: int = HEAD_DIM) -> int:
+    return int(load().kda_segmented_workspace_size(int(T_total), int(H), int(N), int(D),
+                                                   int(segments)))
+
+
+def kda_fwd_segmented(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
+                      cu_seqlens=None, N=None, segments=0, out=None, final_state=None,
+                      workspace=None, stream=None, output_final_state=True):
+    """The forward pass with every sequence cut into `segments` pieces run at
+    once and joined by a scan of their state maps (kda_fwd_segmented in
+    include/kda.h; 0 = the automatic count).  States fp32; g_raw
+    [T_total, H, 128] (per channel) or [T_total, H] (one gate per token and
+    head).  Returns (out, final_state)."""
+    T_total, H, D, N = _geometry(q, cu_seqlens, N)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, (T_total, H, D))
+    per_head = g_raw.dim() == 2
+    _need(g_raw, "g_raw", torch.bfloat16, (T_total, H) if per_head else (T_total, H, D))
+    _need(beta_raw, "beta_raw", torch.bfloat16, (T_total, H))
+    if initial_state is not None:
+        _need(initial_state, "initial_state", torch.float32, (N, H, D, D))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (T_total, H, D))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    if final_state is not None:
+        _need(final_state, "final_state", torch.float32, (N, H, D, D))
+    ws_bytes = 0
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
+    st = load().kda_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                                  float(scale), float(lower_bound), _ptr(initial_state),
+                                  _ptr(cu_seqlens), T_total, H, N, D, _ptr(out),
+                                  _ptr(final_state), int(segments), 1 if per_head else 0,
+                                  _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "kda_fwd_segmented")
+    return out, final_state
+
+
 def kda_fwd_noalloc(q, k, v, g_raw, beta_raw, scale, lower_bound, out, final_state=None,
                     initial_state=None, cu_seqlens=None, N=None, stream=None):
     """kda_fwd for callers that cannot allocate device memory: the chunk records
@@ -335,15 +390,17 @@ def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state
 
     The sequences are split into up to `groups` contiguous groups.  Group p's
     inputs go host->device on a copy stream; its forward pass (`schedule`:
-    "fused" = kda_fwd_fused, "split" = kda_fwd, "decode" = kda_decode) runs on a
-    stream of its own once they have arrived,
+    "fused" = kda_fwd_fused, "split" = kda_fwd, "decode" = kda_decode,
+    "segmented" = kda_fwd_segmented) runs on a stream of its own once they have
+    arrived,
     so it overlaps the copies of the later groups; its outputs go device->host on
     a third stream, overlapping the remaining input copies (the link carries
     both directions at once).  `stream` (default: the current stream) orders the
     whole call: nothing starts before work already queued on it, and it waits
     for the last copy."""
     stream = torch.cuda.current_stream(device) if stream is None else stream
-    fwd = {"fused": kda_fwd_fused, "split": kda_fwd, "decode": kda_decode}[schedule]
+    fwd = {"fused": kda_fwd_fused, "split": kda_fwd, "decode": kda_decode,
+           "segmented": kda_fwd_segmented}[schedule]
     T_total, H, D, N = _geometry(q, None, N) if cu_seqlens is None else (
         q.shape[0], q.shape[1], q.shape[2], cu_seqlens.shape[0] - 1)
     if cu_seqlens is not None:

@@ -19,8 +19,15 @@ cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* c
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
                          const void* beta_raw, float scale, float lower_bound, float eps,
                          const void* init, const int32_t* cu, int64_t T_total, int H, int N,
-                         void* out, void* final_state, FwdOpts opts, int* err,
+                         void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
                          cudaStream_t stream);
+cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, int32_t* cu_seg,
+                            int32_t* blk, cudaStream_t stream);
+cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
+                               float* final_state, cudaStream_t stream);
+cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
+                             const float* sstart, const void* y, void* out, int sm_count,
+                             cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* g,
                           const void* beta_raw, float scale, float lower_bound, float eps,
                           const void* init, const int32_t* cu, int64_t T_total, int H, int N,
@@ -135,7 +142,8 @@ kda_status forward(int schedule, FwdOpts opts, const void* q, const void* k, con
   cudaError_t e = cudaSuccess;
   if (schedule == 1) {
     e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
-                     cu_seqlens, T_total, H, N, out, final_state, opts, info.err, st);
+                     cu_seqlens, T_total, H, N, out, final_state, opts, SegArgs{0, nullptr, nullptr},
+                     info.err, st);
   } else if (schedule == 2) {
     e = launch_decode(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
                       cu_seqlens, T_total, H, N, out, final_state, opts, st);
@@ -245,6 +253,123 @@ extern "C" kda_status kda_forward(const kda_options* opts, const void* q, const 
   return forward(schedule, FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
                  g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens, T_total, H, N,
                  D, out, final_state, workspace, workspace_bytes, stream);
+}
+
+namespace {
+
+constexpr int kMaxSegments = 64;
+
+int64_t round256(int64_t x) { return (x + 255) & ~static_cast<int64_t>(255); }
+
+// Byte offsets of the segmented pass's workspace parts (each 256-byte aligned):
+// cu_seg and blk [N P + 1] int32, the X and M final states [N P, H, 128, 128]
+// fp32, the M outputs y [T_total, H, 128] bf16.
+struct SegLayout {
+  int64_t cu, blk, xs, ms, y, total;
+};
+SegLayout seg_layout(int64_t T_total, int32_t H, int32_t N, int32_t P) {
+  SegLayout L;
+  const int64_t ns = static_cast<int64_t>(N) * P;
+  const int64_t states = ns * H * KDA_HEAD_DIM * KDA_HEAD_DIM * 4;
+  L.cu = 0;
+  L.blk = L.cu + round256((ns + 1) * 4);
+  L.xs = L.blk + round256((ns + 1) * 4);
+  L.ms = L.xs + round256(states);
+  L.y = L.ms + round256(states);
+  L.total = L.y + round256(T_total * H * KDA_HEAD_DIM * 2);
+  return L;
+}
+
+// Segments per sequence for a device with `sms` SMs: the fused kernel runs
+// two CTAs per SM, and P segments take N H (2 P - 1) CTAs (X roles for all,
+// M roles for all but the first); each segment keeps at least 64 chunks.
+int32_t auto_segments(int64_t T_total, int32_t H, int32_t N, int sms) {
+  const int64_t units = static_cast<int64_t>(N) * H;
+  if (units <= 0 || sms <= 0) return 1;
+  int64_t P = (2 * static_cast<int64_t>(sms) / units + 1) / 2;
+  const int64_t chunks = (T_total / N + 15) / 16;
+  if (P > chunks / 64) P = chunks / 64;
+  if (P > kMaxSegments) P = kMaxSegments;
+  return static_cast<int32_t>(P < 1 ? 1 : P);
+}
+
+kda_status seg_checks(int64_t T_total, int32_t H, int32_t N, int32_t D, int32_t segments,
+                      const int32_t* cu_seqlens) {
+  kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if (segments < 0 || segments > kMaxSegments) return KDA_ERR_INVALID_ARG;
+  if (T_total >= (static_cast<int64_t>(1) << 31)) return KDA_ERR_INVALID_ARG;  // int32 boundaries
+  if (static_cast<int64_t>(N) * kMaxSegments * H * 2 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t kda_segments_auto(int64_t T_total, int32_t H, int32_t N) {
+  if (check_sizes(T_total, H, N, KDA_HEAD_DIM, reinterpret_cast<const int32_t*>(1)) != KDA_OK)
+    return 1;
+  DeviceInfo info;
+  if (device_info(info) != KDA_OK) return 1;
+  return auto_segments(T_total, H, N, info.sm_count);
+}
+
+extern "C" size_t kda_segmented_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D,
+                                               int32_t segments) {
+  if (seg_checks(T_total, H, N, D, segments, reinterpret_cast<const int32_t*>(1)) != KDA_OK)
+    return 0;
+  const int32_t P = segments == 0 ? kda_segments_auto(T_total, H, N) : segments;
+  if (P <= 1) return 0;
+  return static_cast<size_t>(seg_layout(T_total, H, N, P).total);
+}
+
+extern "C" kda_status kda_fwd_segmented(const void* q, const void* k, const void* v,
+                                        const void* g_raw, const void* beta_raw, float scale,
+                                        float lower_bound, const float* initial_state,
+                                        const int32_t* cu_seqlens, int64_t T_total, int32_t H,
+                                        int32_t N, int32_t D, void* out, float* final_state,
+                                        int32_t segments, int32_t gate, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  kda_status s = seg_checks(T_total, H, N, D, segments, cu_seqlens);
+  if (s != KDA_OK) return s;
+  if (gate != KDA_GATE_PER_CHANNEL && gate != KDA_GATE_PER_HEAD) return KDA_ERR_INVALID_ARG;
+  const FwdOpts opts{0, gate == KDA_GATE_PER_HEAD};
+  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total,
+                        opts.gate_scalar != 0)) != KDA_OK)
+    return s;
+  if ((s = check_outputs(out, initial_state, final_state, T_total)) != KDA_OK) return s;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  const int32_t P = segments == 0 ? auto_segments(T_total, H, N, info.sm_count) : segments;
+  if (P <= 1 || T_total == 0)
+    return forward(1, opts, q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state,
+                   cu_seqlens, T_total, H, N, D, out, final_state, nullptr, 0, stream);
+  const SegLayout L = seg_layout(T_total, H, N, P);
+  if (workspace && (!aligned16(workspace) || workspace_bytes < static_cast<size_t>(L.total)))
+    return KDA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, static_cast<size_t>(L.total), st) != cudaSuccess) {
+      cudaGetLastError();
+      return KDA_ERR_WORKSPACE;
+    }
+  }
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  int32_t* cu_seg = reinterpret_cast<int32_t*>(wb + L.cu);
+  int32_t* blk = reinterpret_cast<int32_t*>(wb + L.blk);
+  float* xs = reinterpret_cast<float*>(wb + L.xs);
+  float* ms = reinterpret_cast<float*>(wb + L.ms);
+  __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(wb + L.y);
+  const int Nseg = N * P;
+  cudaError_t e = launch_seg_plan(cu_seqlens, T_total, N, P, cu_seg, blk, st);
+  if (e == cudaSuccess)
+    e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
+                     cu_seg, T_total, H, Nseg, out, xs, opts, SegArgs{P, y, ms}, info.err, st);
+  if (e == cudaSuccess) e = launch_affine_scan(xs, ms, N, P, H, final_state, st);
+  if (e == cudaSuccess)
+    e = launch_seg_fixup(cu_seg, blk, Nseg, H, xs, y, out, info.sm_count, st);
+  if (!workspace) cudaFreeAsync(ws, st);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 extern "C" kda_status kda_device_status(void* stream) {

@@ -79,6 +79,24 @@ struct FwdOpts {
   int gate_scalar;  // g_raw is one value per token and head [T_total, H]
 };
 
+// Segmented launch of the fused kernel (the affine-map split of each sequence
+// into P pieces, kda_segmented.cu).  With P > 0 the kernel's N is the number
+// of segments, N_seq * P, and its grid holds two CTAs per (segment, head):
+//   blocks [0, N H)      X role: the segment from a zero state (the first
+//                        segment of each sequence from that sequence's initial
+//                        state, element ((n / P) H + h) of `init`), outputs to
+//                        `out`, final state to `final_state` [N, H, V, K];
+//   blocks [N H, 2 N H)  M role: the same segment with v = 0 from the identity,
+//                        whose state is the product of the segment's
+//                        transition matrices and whose outputs are those
+//                        matrices applied to the scaled queries; outputs to `y`,
+//                        final state to `m_final`.  Not run for first segments.
+struct SegArgs {
+  int P;                 // segments per sequence; 0 = a plain forward pass
+  __nv_bfloat16* y;      // M-role outputs [T_total, H, 128]
+  float* m_final;        // M-role final states [N, H, 128, 128] (fp32)
+};
+
 // Address of element `elem` of a state buffer of fp32 (or bf16) entries; null stays null.
 __device__ __forceinline__ const void* state_at(const void* base, int64_t elem, bool bf16) {
   return base ? static_cast<const uint8_t*>(base) + elem * (bf16 ? 2 : 4) : nullptr;

@@ -61,7 +61,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e, float eps,
              const void* init, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
-             __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts,
+             __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts, SegArgs seg,
              int* __restrict__ err) {
   constexpr int NST = F_NST;
   extern __shared__ uint8_t smem_raw[];
@@ -69,8 +69,16 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   ChunkSmem& CS = *reinterpret_cast<ChunkSmem*>(smem + F_CHUNK_OFF);
   auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + F_CTL_OFF);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
-  const int unit = blockIdx.x;
+  int unit = blockIdx.x;
+  const bool mrole = seg.P > 0 && unit >= N * H;  // segmented launch, M role (SegArgs)
+  if (mrole) unit -= N * H;
   const int n = unit / H, h = unit - (unit / H) * H;
+  // a first segment starts from the sequence's own state: it needs no M role
+  if (mrole && n % seg.P == 0) return;
+  // initial state: the M role starts from the identity, a later segment from
+  // zero, a first segment from its sequence's state
+  const void* init_u = (mrole || (seg.P > 0 && n % seg.P != 0)) ? nullptr : init;
+  const int64_t init_unit = seg.P > 0 ? n / seg.P : n;
   int64_t bos, eos;
   seq_bounds(cu, T_total, N, n, bos, eos);
   const int nchunks = static_cast<int>((eos - bos + kChunk - 1) / kChunk);
@@ -95,9 +103,10 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   const uint32_t tb = ctl->tmem;
   const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
   const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
+  const int64_t init_base = (init_unit * H + h) * kDim * kDim;
   if (w < 4)
-    load_state(tb, lane_off, state_at(init, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
-               opts.state_bf16);
+    load_state(tb, lane_off, state_at(init_u, init_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+               opts.state_bf16, mrole ? t : -1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -147,7 +156,9 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
         return chunk_all(ok);
       };
       auto load_v = [&] {
-        issue_v_loads(loader, vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim, nc);
+        // M role: v = 0, every row of the tile takes the zero fill
+        issue_v_loads(loader, vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim,
+                      mrole ? 0 : nc);
       };
       auto next_qkg = [&]() -> bool {
         if (c + 2 >= nchunks) return false;
@@ -170,8 +181,9 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_STATE_REGS));
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
-    state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
-               state_at(final_state, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+    state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, mrole ? seg.y : out,
+               state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
+                        state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
                opts.state_bf16, err, smem + F_OST_OFF, release);
   }
   tc_fence_before();
@@ -183,7 +195,7 @@ template <bool kGateScalar>
 cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const void* g,
                            const void* beta_raw, float scale, float lower_bound, float eps,
                            const void* init, const int32_t* cu, int64_t T_total, int H, int N,
-                           void* out, void* final_state, FwdOpts opts, int* err,
+                           void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
                            cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
@@ -197,26 +209,27 @@ cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const vo
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int64_t units = static_cast<int64_t>(N) * H;
+  const int64_t units = static_cast<int64_t>(N) * H * (seg.P > 0 ? 2 : 1);
   if (units == 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   fused_kernel<kGateScalar><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
       static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, err);
+      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
                          const void* beta_raw, float scale, float lower_bound, float eps,
                          const void* init, const int32_t* cu, int64_t T_total, int H, int N,
-                         void* out, void* final_state, FwdOpts opts, int* err,
+                         void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
                          cudaStream_t stream) {
   return opts.gate_scalar
              ? launch_fused_t<true>(q, k, v, g, beta_raw, scale, lower_bound, eps, init, cu,
-                                    T_total, H, N, out, final_state, opts, err, stream)
+                                    T_total, H, N, out, final_state, opts, seg, err, stream)
              : launch_fused_t<false>(q, k, v, g, beta_raw, scale, lower_bound, eps, init, cu,
-                                     T_total, H, N, out, final_state, opts, err, stream);
+                                     T_total, H, N, out, final_state, opts, seg, err, stream);
 }
 
 }  // namespace kda

@@ -1,0 +1,286 @@
+// kda_segmented.cu -- the forward pass with every sequence cut into P pieces
+// that run at the same time, for few long sequences whose (sequence, head)
+// units alone would leave most SMs idle.
+//
+// Each token step of the recurrence ("You Could Have Come Up with Kimi Delta
+// Attention", sec. 4) is an affine map of the state (rows = value index):
+//   S_t = S_{t-1} A_t + B_t,   A_t = Diag(alpha_t) (I - beta_t k_t k_t^T),
+//                              B_t = beta_t v_t k_t^T,
+// so a segment of tokens maps its starting state S_0 to S_0 M + X, where
+// M = A_1 ... A_n and X is the segment's state from a zero start.  Inside the
+// segment S_t = S_0 M_t + X_t, hence o_t = S_t (s q_t) = X_t (s q_t) + S_0 y_t
+// with y_t = M_t (s q_t).  The scan of these maps is the exchange step that a
+// context-parallel split of a long sequence needs; here all pieces run on one
+// GPU:
+//   1. seg_plan_kernel      segment boundaries (chunk-aligned) and the fix-up
+//                           work list;
+//   2. fused_kernel         one launch with two CTAs per (segment, head)
+//                           (SegArgs in kda_common.cuh): X role (the segment
+//                           from zero, or from the sequence's initial state for
+//                           its first segment) -> out, X; M role (v = 0 from
+//                           the identity: its state is M_t, its output y_t);
+//   3. affine_scan_kernel   per (sequence, head): S_0 of every later segment
+//                           and the final state, S <- S M_j + X_j in fp32;
+//   4. seg_fixup_kernel     out_t += S_0 y_t for the tokens of later segments
+//                           (bf16 tensor-core MMA, fp32 accumulation).
+#include "kda_chunk.cuh"
+
+namespace kda {
+
+constexpr int SG_BLOCK = 128;  // tokens per fix-up work item (4 warps x 32)
+constexpr int SG_ROW = 272;    // padded byte stride of a 128 x bf16 row in shared memory
+
+// Segment j of sequence n covers chunks [nch j / P, nch (j + 1) / P) of the
+// sequence's nch chunks (floor division), so every boundary but the last is a
+// chunk boundary and segments differ in length by at most one chunk (empty
+// segments when nch < P).  cu_seg [N P + 1] holds the boundaries as a packed
+// cu_seqlens over the same token array; blk [N P + 1] the exclusive prefix
+// over segments of their fix-up work items (first segments have none).
+// One CTA.
+__global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total, int N, int P,
+                                int32_t* __restrict__ cu_seg, int32_t* __restrict__ blk) {
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    int64_t bos, eos;
+    seq_bounds(cu, T_total, N, n, bos, eos);
+    const int64_t nch = (eos - bos + kChunk - 1) / kChunk;
+    for (int j = 0; j < P; ++j) {
+      const int64_t b = bos + kChunk * ((nch * j) / P);
+      int64_t e = bos + kChunk * ((nch * (j + 1)) / P);
+      if (e > eos) e = eos;
+      cu_seg[static_cast<int64_t>(n) * P + j] = static_cast<int32_t>(b);
+      blk[static_cast<int64_t>(n) * P + j + 1] =
+          j == 0 ? 0 : static_cast<int32_t>((e - b + SG_BLOCK - 1) / SG_BLOCK);
+    }
+    if (n == N - 1) cu_seg[static_cast<int64_t>(N) * P] = static_cast<int32_t>(eos);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    blk[0] = 0;
+    const int64_t ns = static_cast<int64_t>(N) * P;
+    for (int64_t s = 0; s < ns; ++s) blk[s + 1] += blk[s];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The scan.  One CTA per (sequence, head), 256 threads, each owning an 8 x 8
+// block of the 128 x 128 state.  S is kept transposed in shared memory
+// (St[k][v], row stride SC_LD floats) so that a thread's 8 values of one key
+// column are two float4 loads; M_j is staged row-major.  xs holds the X role's
+// final states [N P, H, V, K]; for every later segment j its entry is replaced
+// by that segment's starting state S_0 (read by the fix-up).
+// ---------------------------------------------------------------------------
+constexpr int SC_THREADS = 256;
+constexpr int SC_LD = 132;
+constexpr int SC_SMEM = (kDim * SC_LD + kDim * kDim) * 4;
+
+__global__ void __launch_bounds__(SC_THREADS)
+affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
+                   float* __restrict__ final_state) {
+  extern __shared__ float4 sc_smem4[];
+  float* St = reinterpret_cast<float*>(sc_smem4);
+  float* Ms = St + kDim * SC_LD;
+  const int unit = blockIdx.x;
+  const int n = unit / H, h = unit - (unit / H) * H;
+  const int t = threadIdx.x;
+  const int rv = (t >> 4) * 8, ck = (t & 15) * 8;  // value rows rv.., key columns ck..
+  auto base = [&](int64_t s) { return (s * H + h) * kDim * kDim; };
+  const int64_t s0 = static_cast<int64_t>(n) * P;
+  {
+    const float* x0 = xs + base(s0);
+    for (int i = t; i < kDim * kDim; i += SC_THREADS) St[(i & 127) * SC_LD + (i >> 7)] = x0[i];
+  }
+  __syncthreads();
+  for (int j = 1; j < P; ++j) {
+    float* xj = xs + base(s0 + j);
+    const float4* mj = reinterpret_cast<const float4*>(ms + base(s0 + j));
+    for (int i = t; i < kDim * kDim / 4; i += SC_THREADS) reinterpret_cast<float4*>(Ms)[i] = mj[i];
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const float4 x0 = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck);
+      const float4 x1 = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck + 4);
+      acc[a][0] = x0.x; acc[a][1] = x0.y; acc[a][2] = x0.z; acc[a][3] = x0.w;
+      acc[a][4] = x1.x; acc[a][5] = x1.y; acc[a][6] = x1.z; acc[a][7] = x1.w;
+    }
+    __syncthreads();  // M_j staged
+#pragma unroll 2
+    for (int kk = 0; kk < kDim; ++kk) {
+      const float4 sa = *reinterpret_cast<const float4*>(St + kk * SC_LD + rv);
+      const float4 sb = *reinterpret_cast<const float4*>(St + kk * SC_LD + rv + 4);
+      const float4 ma = *reinterpret_cast<const float4*>(Ms + kk * kDim + ck);
+      const float4 mb = *reinterpret_cast<const float4*>(Ms + kk * kDim + ck + 4);
+      const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+      const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
+    }
+    // segment j starts from the S before this step (X_j was read above)
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      float r[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) r[b] = St[(ck + b) * SC_LD + rv + a];
+      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) = make_float4(r[0], r[1], r[2], r[3]);
+      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck + 4) = make_float4(r[4], r[5], r[6], r[7]);
+    }
+    __syncthreads();  // every read of St and Ms is done
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) St[(ck + b) * SC_LD + rv + a] = acc[a][b];
+    __syncthreads();
+  }
+  if (final_state) {
+    float* f = final_state + (static_cast<int64_t>(n) * H + h) * kDim * kDim;
+    for (int i = t; i < kDim * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The fix-up: out[t, h, :] += S_0 y[t, h, :] for the tokens of every later
+// segment.  Work item = (head, 128-token block of one segment), numbered head
+// major so that a CTA's contiguous range of items mostly shares one (segment,
+// head) and loads its S_0 once: S_0 (fp32) -> bf16 [v][k] in shared memory,
+// read as B fragments (ldmatrix); y is read straight into A fragments and out
+// is updated in place in the accumulator layout.  Warp w: tokens 32 w .. +31
+// of the block (two 16-row tiles sharing every B fragment), 16 column tiles
+// of 8 values, K = 128.
+// ---------------------------------------------------------------------------
+constexpr int FX_THREADS = 128;
+constexpr int FX_SMEM = kDim * SG_ROW;
+
+__global__ void __launch_bounds__(FX_THREADS)
+seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__ blk, int Nseg,
+                 int H, const float* __restrict__ sstart, const __nv_bfloat16* __restrict__ y,
+                 __nv_bfloat16* __restrict__ out) {
+  extern __shared__ uint8_t fx_smem[];
+  uint8_t* sb = fx_smem;
+  const int t = threadIdx.x, w = t >> 5, l = t & 31;
+  const int64_t nblk = __ldg(blk + Nseg);
+  const int64_t total = nblk * H;
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t i1 = (i0 + per < total) ? i0 + per : total;
+  const int64_t row_stride = static_cast<int64_t>(H) * kDim;
+  int cur_s = -1, cur_h = -1;
+  for (int64_t it = i0; it < i1; ++it) {
+    const int h = static_cast<int>(it / nblk);
+    const int gb = static_cast<int>(it - static_cast<int64_t>(h) * nblk);
+    // the segment s with blk[s] <= gb < blk[s + 1]
+    int lo = 0, hi = Nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(blk + mid) <= gb)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int s = lo;
+    const int64_t t0 = __ldg(cu_seg + s) + static_cast<int64_t>(gb - __ldg(blk + s)) * SG_BLOCK;
+    const int64_t rem = __ldg(cu_seg + s + 1) - t0;
+    const int nt = static_cast<int>(rem < SG_BLOCK ? rem : SG_BLOCK);
+    if (s != cur_s || h != cur_h) {
+      __syncthreads();  // the previous S_0 is no longer read
+      const float2* src = reinterpret_cast<const float2*>(
+          sstart + (static_cast<int64_t>(s) * H + h) * kDim * kDim);
+      for (int i = t; i < kDim * kDim / 2; i += FX_THREADS) {
+        const float2 x = __ldg(src + i);
+        const int v = i >> 6, kp = i & 63;
+        *reinterpret_cast<uint32_t*>(sb + v * SG_ROW + kp * 4) = pack_bf16(x.x, x.y);
+      }
+      __syncthreads();
+      cur_s = s;
+      cur_h = h;
+    }
+    const int rbase = 32 * w;
+    if (rbase >= nt) continue;  // no barrier inside an item: warps may skip theirs
+    // A fragments: y rows rbase + 16 mt + (l >> 2) (+8), key pairs 2 (l & 3) (+8)
+    uint32_t a[2][8][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = rbase + 16 * mt + (l >> 2) + 8 * hr;
+        const uint32_t* yr = reinterpret_cast<const uint32_t*>(
+            y + (t0 + r) * row_stride + static_cast<int64_t>(h) * kDim);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          a[mt][kk][hr] = r < nt ? __ldg(yr + kk * 8 + (l & 3)) : 0u;
+          a[mt][kk][2 + hr] = r < nt ? __ldg(yr + kk * 8 + 4 + (l & 3)) : 0u;
+        }
+      }
+    }
+#pragma unroll 1
+    for (int n8 = 0; n8 < 16; ++n8) {
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint8_t* brow = sb + (n8 * 8 + (l & 7)) * SG_ROW + (l >> 3) * 16;
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        uint32_t b[4];
+        ldsm_x4(b, brow + k2 * 64);
+        mma16816(acc[0], a[0][2 * k2], b[0], b[1]);
+        mma16816(acc[1], a[1][2 * k2], b[0], b[1]);
+        mma16816(acc[0], a[0][2 * k2 + 1], b[2], b[3]);
+        mma16816(acc[1], a[1][2 * k2 + 1], b[2], b[3]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = rbase + 16 * mt + (l >> 2) + 8 * hr;
+          if (r < nt) {
+            uint32_t* p = reinterpret_cast<uint32_t*>(out + (t0 + r) * row_stride +
+                                                      static_cast<int64_t>(h) * kDim + n8 * 8 +
+                                                      2 * (l & 3));
+            const uint32_t ov = *p;
+            const float2 o = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
+            *p = pack_bf16(o.x + acc[mt][2 * hr], o.y + acc[mt][2 * hr + 1]);
+          }
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, int32_t* cu_seg,
+                            int32_t* blk, cudaStream_t stream) {
+  seg_plan_kernel<<<1, 1024, 0, stream>>>(cu, T_total, N, P, cu_seg, blk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
+                               float* final_state, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        affine_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t units = static_cast<int64_t>(N) * H;
+  if (units == 0) return cudaSuccess;
+  affine_scan_kernel<<<static_cast<unsigned>(units), SC_THREADS, SC_SMEM, stream>>>(
+      xs, ms, N, P, H, final_state);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
+                             const float* sstart, const void* y, void* out, int sm_count,
+                             cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        seg_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FX_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (Nseg == 0) return cudaSuccess;
+  seg_fixup_kernel<<<static_cast<unsigned>(4 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
+      cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(y),
+      static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -79,16 +79,21 @@ __device__ __forceinline__ bool state_all(bool pred) {
 }
 
 // Initial state row (fp32, or bf16 if `bf16`; null = zeros) -> tensor memory.
+// identity_row >= 0 loads row identity_row of the identity matrix instead.
 // State threads only (t < 128).
 __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off, const void* src,
-                                           bool bf16) {
+                                           bool bf16, int identity_row = -1) {
 #pragma unroll
   for (int qd = 0; qd < 4; ++qd) {
     uint32_t r[32];
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (src && bf16) {
+      if (identity_row >= 0) {
+        const int d = identity_row - (qd * 32 + i);
+        x = make_float4(d == 0 ? 1.f : 0.f, d == 1 ? 1.f : 0.f, d == 2 ? 1.f : 0.f,
+                        d == 3 ? 1.f : 0.f);
+      } else if (src && bf16) {
         const uint2 b = __ldg(reinterpret_cast<const uint2*>(
             static_cast<const __nv_bfloat16*>(src) + qd * 32 + i));
         const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));

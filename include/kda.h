@@ -200,6 +200,50 @@ kda_status kda_chunk_recurrence(const void* workspace, size_t workspace_bytes,
                                 int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
                                 float* final_state, void* stream);
 
+/* The forward pass for few long sequences: every sequence is cut into
+ * `segments` pieces that run at the same time and are joined by a scan of
+ * their state maps.  Each token step of the recurrence is an affine map of
+ * the state, S -> S A_t + beta_t v_t k^_t^T with A_t = Diag(alpha_t)
+ * (I - beta_t k^_t k^_t^T) ("You Could Have Come Up with Kimi Delta
+ * Attention", sec. 4), so a piece maps its starting state S_0 to S_0 M + X:
+ *   - M = A_1 ... A_n comes from running the piece with v = 0 from the
+ *     identity; that run's outputs are y_t = M_t (scale q^_t);
+ *   - X comes from running the piece from zero, with outputs o^X_t;
+ *   - a scan over the pieces of each (sequence, head), S_0 <- S_0 M + X in
+ *     fp32, gives every piece its S_0 and the final state;
+ *   - o_t = o^X_t + S_0 y_t, added on the tensor cores (bf16 S_0 and y, fp32
+ *     sums, rounded to bf16 once more).
+ * Pieces are whole 16-token chunks: piece j of a sequence with c chunks holds
+ * chunks [floor(c j / P), floor(c (j + 1) / P)), so pieces may be empty when
+ * c < P.  Results equal kda_fwd_fused's up to rounding.
+ * Arguments are those of kda_fwd_fused (states fp32), plus:
+ *   segments   pieces per sequence P, 1..64; 0 = kda_segments_auto().  P = 1
+ *              is kda_fwd_fused itself (no workspace).
+ *   gate       KDA_GATE_PER_CHANNEL or KDA_GATE_PER_HEAD (as in kda_forward).
+ *   workspace  device memory of kda_segmented_workspace_size() bytes (16-byte
+ *              aligned), or NULL (= cudaMallocAsync / cudaFreeAsync on the
+ *              stream).  It holds the piece boundaries, the X and M states of
+ *              every piece (2 N P H 64 KiB) and y (T_total H 256 bytes).
+ * T_total must be below 2^31 (piece boundaries are int32).  The runtime is set
+ * by the longest piece: the pieces' units take N H (2 P - 1) CTAs of the fused
+ * kernel, two per SM. */
+kda_status kda_fwd_segmented(const void* q, const void* k, const void* v, const void* g_raw,
+                             const void* beta_raw, float scale, float lower_bound,
+                             const float* initial_state, const int32_t* cu_seqlens,
+                             int64_t T_total, int32_t H, int32_t N, int32_t D, void* out,
+                             float* final_state, int32_t segments, int32_t gate,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes kda_fwd_segmented needs for these sizes and `segments`
+ * (0 = the automatic count); 0 when it needs none or the sizes are invalid. */
+size_t kda_segmented_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D,
+                                    int32_t segments);
+
+/* The automatic piece count on the current device: the largest P with
+ * N H (2 P - 1) <= 2 x (SM count), at most 64, and at least 64 chunks per
+ * piece on average; 1 means no split. */
+int32_t kda_segments_auto(int64_t T_total, int32_t H, int32_t N);
+
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: KDA_OK, or KDA_ERR_TIMEOUT if a kernel's bounded wait ran
  * out since the last call (its outputs are then invalid), or KDA_ERR_LAUNCH if

@@ -116,3 +116,30 @@ def test_forward_rejects_bad_options(lib):
         assert lib.kda_forward(ctypes.byref(opts), *args) == 1, bad
     opts = kda._Options(1, 0, 0)
     assert lib.kda_forward(ctypes.byref(opts), *args[:9], 64, 1, 1, 64, *args[13:]) == 2  # D
+
+
+def test_segmented_workspace_size(lib):
+    # boundaries and work list (256 B each), X and M states (N P H 64 KiB each), y (T H 256 B)
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=4) == 512 + 2 * 4 * 4 * 65536 + 4096 * 4 * 256
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=1) == 0   # plain fused pass
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=65) == 0  # more than 64 pieces
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=-1) == 0
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=4, D=64) == 0
+    assert kda.kda_segmented_workspace_size(1 << 31, 1, 1, segments=2) == 0  # int32 boundaries
+
+
+def test_segmented_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+
+    def call(T=64, H=1, N=1, D=128, segments=2, gate=0, q=FAKE, lb=-5.0, ws=None, ws_bytes=0):
+        return lib.kda_fwd_segmented(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), 0.1, lb, None,
+                                     None, T, H, N, D, P(FAKE), None, segments, gate,
+                                     P(ws) if ws else None, ws_bytes, None)
+    assert call(segments=65) == 1
+    assert call(segments=-1) == 1
+    assert call(gate=2) == 1
+    assert call(D=64) == 2
+    assert call(lb=-6.0) == 2
+    assert call(q=FAKE + 8) == 1
+    assert call(T=65, N=2) == 1
+    assert call(T=1 << 31) == 1

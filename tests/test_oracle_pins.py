@@ -339,3 +339,39 @@ def test_golden_regression_record():
                           c["lower_bound"], eps=c["eps"])
     np.testing.assert_allclose(o, np.array(rec["out"]), rtol=0, atol=1e-14)
     np.testing.assert_allclose(S, np.array(rec["final_state"]), rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# P-i  affine split.  Each token step is an affine map of the state (sec. 4:
+#      S_t = S_{t-1} Diag(alpha_t)(I - beta_t k_t k_t^T) + beta_t v_t k_t^T),
+#      so a segment maps its start S_0 to S_0 M + X, with M the run from the
+#      identity with v = 0 and X the run from zero, and o_t = o^X_t + S_0 y_t
+#      where y_t is the first run's output.  Composed over the segments this
+#      must reproduce the whole run (the segmented forward pass relies on it).
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cuts", [[0, 32, 64, 100], [0, 16, 100], [0, 0, 50, 100], [0, 37, 99, 100]])
+@pytest.mark.parametrize("lb", [-0.05, -5.0])
+def test_pi_affine_split_composes(cuts, lb):
+    rng = np.random.default_rng(77)
+    c = rand_case(100, 2, 8, V=6, rng=rng, lb=lb, init=True)
+    s = 0.4
+    o_ref, S_ref = oracle.fwd(c["q"], c["k"], c["v"], c["la"], c["beta"], s, c["S0"])
+    S = c["S0"][0].copy()                                   # [H, V, K]
+    o = np.zeros_like(o_ref)
+    eye = np.broadcast_to(np.eye(8), (1, 2, 8, 8)).copy()
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if a == b:
+            continue
+        sl = slice(a, b)
+        oX, X = oracle.fwd(c["q"][sl], c["k"][sl], c["v"][sl], c["la"][sl], c["beta"][sl], s)
+        y, M = oracle.fwd(c["q"][sl], c["k"][sl], np.zeros((b - a, 2, 8)), c["la"][sl],
+                          c["beta"][sl], s, eye)
+        o[sl] = oX + np.einsum("hvk,thk->thv", S, y)
+        S = np.einsum("hvk,hkj->hvj", S, M[0]) + X[0]
+    assert rel(o, o_ref) < 1e-12
+    assert rel(S, S_ref[0]) < 1e-12
+    # and the split is not vacuous: the handed-over state changes the outputs
+    if lb == -0.05:
+        o_zero, _ = oracle.fwd(c["q"][cuts[-2]:], c["k"][cuts[-2]:], c["v"][cuts[-2]:],
+                               c["la"][cuts[-2]:], c["beta"][cuts[-2]:], s)
+        assert rel(o_zero, o_ref[cuts[-2]:]) > 1e-3
