@@ -40,6 +40,10 @@ WORKLOAD_TEXT = {
     "long": "1 sequence x 131072 tokens, H=32, D=128, bf16, g_raw~N(2,1), zero initial state",
     "varlen": "64 packed sequences, lengths U[1,16384] not multiples of 16, H=32, init 0.02*N(0,1)",
     "b2": "B=2 sequences x T=8192 tokens, H=32, D=128, bf16 (profiling size)",
+    "slow": "1 sequence x 131072 tokens, H=32, D=128, bf16, g_raw~N(-6,1) (slow decay), zero "
+            "initial state",
+    "l32": "1 sequence x 32768 tokens, H=32, D=128, bf16, g_raw~N(2,1) (profiling size of the "
+           "segmented path)",
     "decode": "one serving step: 256 sequences x 1 token, H=32, D=128, bf16, fp32 states "
               "0.02*N(0,1) in and out",
 }

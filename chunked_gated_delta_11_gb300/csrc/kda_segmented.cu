@@ -27,7 +27,7 @@
 
 namespace kda {
 
-constexpr int SG_BLOCK = 128;  // tokens per fix-up work item (4 warps x 32)
+constexpr int SG_BLOCK = 64;   // tokens per fix-up work item (4 warps x 16)
 constexpr int SG_ROW = 272;    // padded byte stride of a 128 x bf16 row in shared memory
 
 // Segment j of sequence n covers chunks [nch j / P, nch (j + 1) / P) of the
@@ -62,15 +62,19 @@ __global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total,
 }
 
 // ---------------------------------------------------------------------------
-// The scan.  One CTA per (sequence, head), 256 threads, each owning an 8 x 8
-// block of the 128 x 128 state.  S is kept transposed in shared memory
-// (St[k][v], row stride SC_LD floats) so that a thread's 8 values of one key
-// column are two float4 loads; M_j is staged row-major.  xs holds the X role's
-// final states [N P, H, V, K]; for every later segment j its entry is replaced
-// by that segment's starting state S_0 (read by the fix-up).
+// The scan.  Rows of S M + X depend only on the same rows of S, so each
+// (sequence, head) is split over SC_SPLIT CTAs of SC_ROWS value rows.  256
+// threads, each owning a 4 x 4 block of the CTA's 32 x 128 rows.  The rows are
+// kept transposed in shared memory (St[k][v], row stride SC_LD floats) so
+// that a thread's 4 values of one key column are one float4 load; M_j is
+// staged row-major.  xs holds the X role's final states [N P, H, V, K]; for
+// every later segment j its entry is replaced by that segment's starting state
+// S_0 (read by the fix-up).
 // ---------------------------------------------------------------------------
 constexpr int SC_THREADS = 256;
-constexpr int SC_LD = 132;
+constexpr int SC_SPLIT = 4;
+constexpr int SC_ROWS = kDim / SC_SPLIT;  // 32
+constexpr int SC_LD = SC_ROWS + 4;
 constexpr int SC_SMEM = (kDim * SC_LD + kDim * kDim) * 4;
 
 __global__ void __launch_bounds__(SC_THREADS)
@@ -79,84 +83,90 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
   extern __shared__ float4 sc_smem4[];
   float* St = reinterpret_cast<float*>(sc_smem4);
   float* Ms = St + kDim * SC_LD;
-  const int unit = blockIdx.x;
+  const int unit = blockIdx.x / SC_SPLIT, part = blockIdx.x - unit * SC_SPLIT;
   const int n = unit / H, h = unit - (unit / H) * H;
   const int t = threadIdx.x;
-  const int rv = (t >> 4) * 8, ck = (t & 15) * 8;  // value rows rv.., key columns ck..
+  const int rv = (t >> 5) * 4, ck = (t & 31) * 4;  // local value rows rv.., key columns ck..
+  const int64_t row0 = static_cast<int64_t>(part) * SC_ROWS * kDim;  // first row of the part
   auto base = [&](int64_t s) { return (s * H + h) * kDim * kDim; };
   const int64_t s0 = static_cast<int64_t>(n) * P;
   {
-    const float* x0 = xs + base(s0);
-    for (int i = t; i < kDim * kDim; i += SC_THREADS) St[(i & 127) * SC_LD + (i >> 7)] = x0[i];
+    const float* x0 = xs + base(s0) + row0;
+    for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) St[(i & 127) * SC_LD + (i >> 7)] = x0[i];
   }
   __syncthreads();
   for (int j = 1; j < P; ++j) {
-    float* xj = xs + base(s0 + j);
+    float* xj = xs + base(s0 + j) + row0;
     const float4* mj = reinterpret_cast<const float4*>(ms + base(s0 + j));
     for (int i = t; i < kDim * kDim / 4; i += SC_THREADS) reinterpret_cast<float4*>(Ms)[i] = mj[i];
-    float acc[8][8];
+    float acc[4][4];
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      const float4 x0 = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck);
-      const float4 x1 = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck + 4);
-      acc[a][0] = x0.x; acc[a][1] = x0.y; acc[a][2] = x0.z; acc[a][3] = x0.w;
-      acc[a][4] = x1.x; acc[a][5] = x1.y; acc[a][6] = x1.z; acc[a][7] = x1.w;
+    for (int a = 0; a < 4; ++a) {
+      const float4 x = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck);
+      acc[a][0] = x.x; acc[a][1] = x.y; acc[a][2] = x.z; acc[a][3] = x.w;
     }
     __syncthreads();  // M_j staged
-#pragma unroll 2
+#pragma unroll 4
     for (int kk = 0; kk < kDim; ++kk) {
       const float4 sa = *reinterpret_cast<const float4*>(St + kk * SC_LD + rv);
-      const float4 sb = *reinterpret_cast<const float4*>(St + kk * SC_LD + rv + 4);
       const float4 ma = *reinterpret_cast<const float4*>(Ms + kk * kDim + ck);
-      const float4 mb = *reinterpret_cast<const float4*>(Ms + kk * kDim + ck + 4);
-      const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-      const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+      const float sv[4] = {sa.x, sa.y, sa.z, sa.w};
+      const float mv[4] = {ma.x, ma.y, ma.z, ma.w};
 #pragma unroll
-      for (int a = 0; a < 8; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
     }
     // segment j starts from the S before this step (X_j was read above)
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      float r[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) r[b] = St[(ck + b) * SC_LD + rv + a];
-      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) = make_float4(r[0], r[1], r[2], r[3]);
-      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck + 4) = make_float4(r[4], r[5], r[6], r[7]);
-    }
+    for (int a = 0; a < 4; ++a)
+      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
+          make_float4(St[ck * SC_LD + rv + a], St[(ck + 1) * SC_LD + rv + a],
+                      St[(ck + 2) * SC_LD + rv + a], St[(ck + 3) * SC_LD + rv + a]);
     __syncthreads();  // every read of St and Ms is done
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 8; ++b) St[(ck + b) * SC_LD + rv + a] = acc[a][b];
+      for (int b = 0; b < 4; ++b) St[(ck + b) * SC_LD + rv + a] = acc[a][b];
     __syncthreads();
   }
   if (final_state) {
-    float* f = final_state + (static_cast<int64_t>(n) * H + h) * kDim * kDim;
-    for (int i = t; i < kDim * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
+    float* f = final_state + (static_cast<int64_t>(n) * H + h) * kDim * kDim + row0;
+    for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
   }
 }
 
 // ---------------------------------------------------------------------------
 // The fix-up: out[t, h, :] += S_0 y[t, h, :] for the tokens of every later
-// segment.  Work item = (head, 128-token block of one segment), numbered head
+// segment.  Work item = (head, 64-token block of one segment), numbered head
 // major so that a CTA's contiguous range of items mostly shares one (segment,
-// head) and loads its S_0 once: S_0 (fp32) -> bf16 [v][k] in shared memory,
-// read as B fragments (ldmatrix); y is read straight into A fragments and out
-// is updated in place in the accumulator layout.  Warp w: tokens 32 w .. +31
-// of the block (two 16-row tiles sharing every B fragment), 16 column tiles
+// head) and converts its S_0 once: S_0 (fp32) -> bf16 [v][k] in shared memory,
+// read as B fragments (ldmatrix).  The item's rows of y and out arrive by
+// cp.async into padded shared tiles (coalesced 16-byte pieces; y rows past the
+// segment end are zero-filled), y is read as A fragments (ldmatrix), the sums
+// are added to the out tile in the accumulator layout, and the tile goes back
+// in 16-byte pieces.  Warp w: tokens 16 w .. +15 of the block, 16 column tiles
 // of 8 values, K = 128.
 // ---------------------------------------------------------------------------
 constexpr int FX_THREADS = 128;
-constexpr int FX_SMEM = kDim * SG_ROW;
+constexpr int FX_S_BYTES = kDim * SG_ROW;        // S_0, bf16 [128][128], padded rows
+constexpr int FX_T_BYTES = SG_BLOCK * SG_ROW;    // one [64][128] bf16 tile, padded rows
+constexpr int FX_SMEM = FX_S_BYTES + 2 * FX_T_BYTES;
 
-__global__ void __launch_bounds__(FX_THREADS)
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool pred) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(pred ? 16 : 0)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(FX_THREADS, 3)
 seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__ blk, int Nseg,
                  int H, const float* __restrict__ sstart, const __nv_bfloat16* __restrict__ y,
                  __nv_bfloat16* __restrict__ out) {
-  extern __shared__ uint8_t fx_smem[];
+  extern __shared__ __align__(16) uint8_t fx_smem[];
   uint8_t* sb = fx_smem;
+  uint8_t* yt = fx_smem + FX_S_BYTES;
+  uint8_t* ot = yt + FX_T_BYTES;
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int64_t nblk = __ldg(blk + Nseg);
   const int64_t total = nblk * H;
@@ -181,8 +191,20 @@ seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__
     const int64_t t0 = __ldg(cu_seg + s) + static_cast<int64_t>(gb - __ldg(blk + s)) * SG_BLOCK;
     const int64_t rem = __ldg(cu_seg + s + 1) - t0;
     const int nt = static_cast<int>(rem < SG_BLOCK ? rem : SG_BLOCK);
+    __syncthreads();  // the previous item's tiles (and S_0) are no longer read
+    // this item's y and out rows: 16 pieces of 16 bytes per row
+    const __nv_bfloat16* ybase = y + t0 * row_stride + static_cast<int64_t>(h) * kDim;
+    __nv_bfloat16* obase = out + t0 * row_stride + static_cast<int64_t>(h) * kDim;
+#pragma unroll
+    for (int k = 0; k < SG_BLOCK * 16 / FX_THREADS; ++k) {
+      const int i = t + k * FX_THREADS, r = i >> 4, c = i & 15;
+      const bool in = r < nt;
+      const int64_t go = (in ? r : 0) * row_stride + c * 8;
+      cp_async16_zfill(yt + r * SG_ROW + c * 16, ybase + go, in);
+      cp_async16_zfill(ot + r * SG_ROW + c * 16, obase + go, in);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (s != cur_s || h != cur_h) {
-      __syncthreads();  // the previous S_0 is no longer read
       const float2* src = reinterpret_cast<const float2*>(
           sstart + (static_cast<int64_t>(s) * H + h) * kDim * kDim);
       for (int i = t; i < kDim * kDim / 2; i += FX_THREADS) {
@@ -190,56 +212,46 @@ seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__
         const int v = i >> 6, kp = i & 63;
         *reinterpret_cast<uint32_t*>(sb + v * SG_ROW + kp * 4) = pack_bf16(x.x, x.y);
       }
-      __syncthreads();
       cur_s = s;
       cur_h = h;
     }
-    const int rbase = 32 * w;
-    if (rbase >= nt) continue;  // no barrier inside an item: warps may skip theirs
-    // A fragments: y rows rbase + 16 mt + (l >> 2) (+8), key pairs 2 (l & 3) (+8)
-    uint32_t a[2][8][4];
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int rbase = 16 * w;
+    if (rbase < nt) {
+      uint32_t a[8][4];
+      const uint8_t* arow = yt + (rbase + (l & 7) + ((l >> 3) & 1) * 8) * SG_ROW + (l >> 4) * 16;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+      for (int kk = 0; kk < 8; ++kk) ldsm_x4(a[kk], arow + kk * 32);
+      const int g = l >> 2, q2 = 2 * (l & 3);
+#pragma unroll 2
+      for (int n8 = 0; n8 < 16; ++n8) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t* brow = sb + (n8 * 8 + (l & 7)) * SG_ROW + (l >> 3) * 16;
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = rbase + 16 * mt + (l >> 2) + 8 * hr;
-        const uint32_t* yr = reinterpret_cast<const uint32_t*>(
-            y + (t0 + r) * row_stride + static_cast<int64_t>(h) * kDim);
+        for (int k2 = 0; k2 < 4; ++k2) {
+          uint32_t b[4];
+          ldsm_x4(b, brow + k2 * 64);
+          mma16816(acc, a[2 * k2], b[0], b[1]);
+          mma16816(acc, a[2 * k2 + 1], b[2], b[3]);
+        }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          a[mt][kk][hr] = r < nt ? __ldg(yr + kk * 8 + (l & 3)) : 0u;
-          a[mt][kk][2 + hr] = r < nt ? __ldg(yr + kk * 8 + 4 + (l & 3)) : 0u;
+        for (int hr = 0; hr < 2; ++hr) {
+          uint32_t* p = reinterpret_cast<uint32_t*>(ot + (rbase + g + 8 * hr) * SG_ROW +
+                                                    (n8 * 8 + q2) * 2);
+          const uint32_t o32 = *p;
+          const float2 o = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o32));
+          *p = pack_bf16(o.x + acc[2 * hr], o.y + acc[2 * hr + 1]);
         }
       }
     }
-#pragma unroll 1
-    for (int n8 = 0; n8 < 16; ++n8) {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint8_t* brow = sb + (n8 * 8 + (l & 7)) * SG_ROW + (l >> 3) * 16;
+    __syncthreads();
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        uint32_t b[4];
-        ldsm_x4(b, brow + k2 * 64);
-        mma16816(acc[0], a[0][2 * k2], b[0], b[1]);
-        mma16816(acc[1], a[1][2 * k2], b[0], b[1]);
-        mma16816(acc[0], a[0][2 * k2 + 1], b[2], b[3]);
-        mma16816(acc[1], a[1][2 * k2 + 1], b[2], b[3]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = rbase + 16 * mt + (l >> 2) + 8 * hr;
-          if (r < nt) {
-            uint32_t* p = reinterpret_cast<uint32_t*>(out + (t0 + r) * row_stride +
-                                                      static_cast<int64_t>(h) * kDim + n8 * 8 +
-                                                      2 * (l & 3));
-            const uint32_t ov = *p;
-            const float2 o = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov));
-            *p = pack_bf16(o.x + acc[mt][2 * hr], o.y + acc[mt][2 * hr + 1]);
-          }
-        }
-      }
+    for (int k = 0; k < SG_BLOCK * 16 / FX_THREADS; ++k) {
+      const int i = t + k * FX_THREADS, r = i >> 4, c = i & 15;
+      if (r < nt)
+        *reinterpret_cast<uint4*>(obase + r * row_stride + c * 8) =
+            *reinterpret_cast<const uint4*>(ot + r * SG_ROW + c * 16);
     }
   }
 }
@@ -259,7 +271,7 @@ cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int64_t units = static_cast<int64_t>(N) * H;
+  const int64_t units = static_cast<int64_t>(N) * H * SC_SPLIT;
   if (units == 0) return cudaSuccess;
   affine_scan_kernel<<<static_cast<unsigned>(units), SC_THREADS, SC_SMEM, stream>>>(
       xs, ms, N, P, H, final_state);
@@ -277,7 +289,7 @@ cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg
     attr_done = true;
   }
   if (Nseg == 0) return cudaSuccess;
-  seg_fixup_kernel<<<static_cast<unsigned>(4 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
+  seg_fixup_kernel<<<static_cast<unsigned>(3 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
       cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(y),
       static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();

@@ -63,6 +63,8 @@ WORKLOADS = {
     "slow": Workload("slow", H=32, N=1, T=131072, init_std=None, g_mean=-6.0, seed=5),
     # profiling size: like b8 with 2 sequences (inputs 537 MB, still larger than L2)
     "b2": Workload("b2", H=32, N=2, T=8192, init_std=None, seed=6),
+    # profiling size for the segmented path: one sequence, like long (g_raw ~ N(2, 1))
+    "l32": Workload("l32", H=32, N=1, T=32768, init_std=None, g_mean=2.0, seed=8),
     # one decode step of a serving batch: 256 sequences x 1 new token, states in/out
     "decode": Workload("decode", H=32, N=256, T=1, init_std=0.02, seed=7),
 }
