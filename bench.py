@@ -59,13 +59,17 @@ PATH_KERNEL = {"fused": "fused_kernel (the whole step)", "split": "whole kda_fwd
                "segmented": "whole kda_fwd_segmented step (4 launches)"}
 PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# dominant kernel, from one ncu capture of the current kernels.  The b8 figure
+# dominant kernel (per step for the segmented path, whose roofline entry is the
+# whole step), from one ncu capture of the current kernels.  The b8 figure
 # is four times the b2 capture: b8 processes four times the units, and the
 # traffic is the per-unit inputs, outputs and states.  Absent = not captured.
 MEASURED_TRAFFIC = {
     ("b2", "fused"): 538.076160e6 + 120.122368e6,
     ("b8", "fused"): 4 * (538.076160e6 + 120.122368e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
+    # the whole kda_fwd_segmented step: its four launches on the long workload
+    ("long", "segmented"): (6340.4064e6 + 1919.716352e6) + 18.882816e6 + 15.872e3
+                           + (1734.447616e6 + 814.037248e6),
 }
 
 

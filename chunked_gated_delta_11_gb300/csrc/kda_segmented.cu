@@ -2,8 +2,9 @@
 // that run at the same time, for few long sequences whose (sequence, head)
 // units alone would leave most SMs idle.
 //
-// Each token step of the recurrence ("You Could Have Come Up with Kimi Delta
-// Attention", sec. 4) is an affine map of the state (rows = value index):
+// Each token step of the recurrence is an affine map of the state, with a
+// diagonal-plus-low-rank linear part ("You Could Have Come Up with Kimi Delta
+// Attention", sec. 4.1; rows = value index):
 //   S_t = S_{t-1} A_t + B_t,   A_t = Diag(alpha_t) (I - beta_t k_t k_t^T),
 //                              B_t = beta_t v_t k_t^T,
 // so a segment of tokens maps its starting state S_0 to S_0 M + X, where

@@ -205,7 +205,7 @@ kda_status kda_chunk_recurrence(const void* workspace, size_t workspace_bytes,
  * their state maps.  Each token step of the recurrence is an affine map of
  * the state, S -> S A_t + beta_t v_t k^_t^T with A_t = Diag(alpha_t)
  * (I - beta_t k^_t k^_t^T) ("You Could Have Come Up with Kimi Delta
- * Attention", sec. 4), so a piece maps its starting state S_0 to S_0 M + X:
+ * Attention", sec. 4.1), so a piece maps its starting state S_0 to S_0 M + X:
  *   - M = A_1 ... A_n comes from running the piece with v = 0 from the
  *     identity; that run's outputs are y_t = M_t (scale q^_t);
  *   - X comes from running the piece from zero, with outputs o^X_t;

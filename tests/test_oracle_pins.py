@@ -342,7 +342,7 @@ def test_golden_regression_record():
 
 
 # ---------------------------------------------------------------------------
-# P-i  affine split.  Each token step is an affine map of the state (sec. 4:
+# P-i  affine split.  Each token step is an affine map of the state (sec. 4.1:
 #      S_t = S_{t-1} Diag(alpha_t)(I - beta_t k_t k_t^T) + beta_t v_t k_t^T),
 #      so a segment maps its start S_0 to S_0 M + X, with M the run from the
 #      identity with v = 0 and X the run from zero, and o_t = o^X_t + S_0 y_t
