@@ -230,14 +230,15 @@ __device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
 //   next_qkg()   once the factor pass is done with `raw`: issue a later chunk's
 //                q, k, g_raw tiles (into `raw` or another buffer); returns
 //                whether it issued them.
-// Returns may_write().
+// Returns may_write().  With u_zero (v known to be zero) U' is zero and is
+// neither formed nor written; the reader must take it as zero.
 template <class MayWrite, class LoadV, class NextQKG>
 __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, uint8_t* vt,
                                                    bool newer_qkg, uint32_t beta_raw_bits,
                                                    int nc, float scale,
                                                    float lb_log2e, float eps, uint8_t* rec, int t,
                                                    MayWrite&& may_write, LoadV&& load_v,
-                                                   NextQKG&& next_qkg) {
+                                                   NextQKG&& next_qkg, bool u_zero = false) {
   const int w = t >> 5, l = t & 31;
   if (newer_qkg)
     asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -486,6 +487,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     // U'^T [c][i] = V^T (A' diag(beta rk))^T: A = V^T from the raw v tile
     // (transposed load), B[j][i] = (A' diag(beta rk))[i][j] as high and low
     // bf16 parts; each lane then holds two consecutive tokens of one channel
+    if (u_zero) return true;
     uint32_t bh[4], bl[4];
     split2(ld2(&S.Au[g][q2]), bh[0], bl[0]);
     split2(ld2(&S.Au[g][q2 + 8]), bh[1], bl[1]);

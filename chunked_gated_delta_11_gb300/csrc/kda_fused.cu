@@ -167,7 +167,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       };
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
       if (!build_chunk_record(CS, rawbuf(c), vt, c + 1 < nchunks, bbits[0], nc, scale,
-                              lb_log2e, eps, rec, tc, may_write, load_v, next_qkg))
+                              lb_log2e, eps, rec, tc, may_write, load_v, next_qkg, mrole))
         break;
       // every thread's record stores -> async proxy, then one arrival per warp
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -184,7 +184,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, mrole ? seg.y : out,
                state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
                         state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
-               opts.state_bf16, err, smem + F_OST_OFF, release);
+               opts.state_bf16, err, smem + F_OST_OFF, release, mrole);
   }
   tc_fence_before();
   __syncthreads();

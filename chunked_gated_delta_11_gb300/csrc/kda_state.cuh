@@ -175,14 +175,15 @@ __device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* b
 // `final_dst` is thread v's row of the final state (fp32, or bf16 if
 // `state_bf16`; null = not written).
 // `ostage` is 4 KB of shared memory (1 KB per state warp) that turns each
-// warp's 16 x 32 output tile into 16-byte stores.
+// warp's 16 x 32 output tile into 16-byte stores.  u_zero: the records carry
+// no U' (v is zero), which is taken as zero.
 template <int NST, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out, void* final_dst,
                                            bool state_bf16, int* err, uint8_t* ostage,
-                                           StageFree&& stage_free) {
+                                           StageFree&& stage_free, bool u_zero = false) {
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   // chunk 0: snapshot the initial state and apply chunk 0's decay
@@ -216,7 +217,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 u = U4[i4 ^ usw];
+        const float4 u = u_zero ? make_float4(0.f, 0.f, 0.f, 0.f) : U4[i4 ^ usw];
         const float2 e0 = __ffma2_rn(make_float2(__uint_as_float(d1[i4 * 4]), __uint_as_float(d1[i4 * 4 + 1])),
                                      m1, make_float2(u.x, u.y));
         const float2 e1 = __ffma2_rn(make_float2(__uint_as_float(d1[i4 * 4 + 2]), __uint_as_float(d1[i4 * 4 + 3])),

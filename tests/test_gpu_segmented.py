@@ -120,3 +120,19 @@ def test_segmented_empty_input():
     out, fs = segmented(inp, 3)
     assert out.numel() == 0
     assert torch.equal(fs, inp["initial_state"])
+
+
+def test_segmented_through_host_buffers():
+    # the host-buffer entry point with the segmented schedule: packed sequences
+    # (one empty) in groups, initial states
+    inp = synth.make_inputs(0, 2, lengths=[900, 0, 333, 70], seed=63, init_std=0.02)
+    pin = {k: (inp[k].pin_memory() if inp[k] is not None else None)
+           for k in ("q", "k", "v", "g_raw", "beta_raw", "initial_state", "cu_seqlens")}
+    out, fs = kda.kda_forward_host(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta_raw"],
+                                   inp["scale"], inp["lower_bound"], pin["initial_state"],
+                                   pin["cu_seqlens"], schedule="segmented", groups=2)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "segmented host-buffer out")
+    assert_close(f64(fs), rs, "segmented host-buffer final_state")
