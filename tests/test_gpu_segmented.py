@@ -136,3 +136,16 @@ def test_segmented_through_host_buffers():
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, "segmented host-buffer out")
     assert_close(f64(fs), rs, "segmented host-buffer final_state")
+
+
+def test_segmented_without_final_state_and_small_workspace():
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[500, 200], seed=64, init_std=0.02))
+    out, fs = segmented(inp, 3, output_final_state=False)
+    assert fs is None
+    ro, _ = oracle_case(inp)
+    assert_close(f64(out), ro, "segmented out without a final state")
+    nbytes = kda.kda_segmented_workspace_size(inp["T_total"], 2, 2, segments=3)
+    small = torch.empty(nbytes - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kda.KdaError) as e:
+        segmented(inp, 3, workspace=small)
+    assert e.value.status == 3
