@@ -31,7 +31,7 @@ CHUNK = 16
 HEAD_DIM = 128
 REC_BYTES = 26112
 
-SCHEDULES = {"split": 0, "fused": 1, "decode": 2}
+SCHEDULES = {"split": 0, "fused": 1, "decode": 2, "segmented": 3}
 
 
 class _Options(ctypes.Structure):
@@ -241,8 +241,8 @@ def kda_forward(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None
     """The forward pass with the options of kda_forward in include/kda.h, read off
     the tensors: states fp32 or bf16 (both the same; the final state is allocated
     with the initial state's dtype), g_raw [T_total, H, 128] (per channel) or
-    [T_total, H] (one gate per token and head).  schedule: "fused", "split" or
-    "decode".  Returns (out, final_state)."""
+    [T_total, H] (one gate per token and head).  schedule: "fused", "split",
+    "decode" or "segmented" (automatic piece count).  Returns (out, final_state)."""
     T_total, H, D, N = _geometry(q, cu_seqlens, N)
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name, torch.bfloat16, (T_total, H, D))

@@ -24,7 +24,7 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
 cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, int32_t* cu_seg,
                             int32_t* blk, cudaStream_t stream);
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
-                               float* final_state, cudaStream_t stream);
+                               void* final_state, bool final_bf16, cudaStream_t stream);
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
                              cudaStream_t stream);
@@ -236,6 +236,15 @@ extern "C" kda_status kda_decode(const void* q, const void* k, const void* v, co
                  cu_seqlens, T_total, H, N, D, out, final_state, nullptr, 0, stream);
 }
 
+namespace {
+kda_status segmented_forward(FwdOpts opts, const void* q, const void* k, const void* v,
+                             const void* g_raw, const void* beta_raw, float scale,
+                             float lower_bound, const void* initial_state,
+                             const int32_t* cu_seqlens, int64_t T_total, int32_t H, int32_t N,
+                             int32_t D, void* out, void* final_state, int32_t segments,
+                             void* workspace, size_t workspace_bytes, void* stream);
+}  // namespace
+
 extern "C" kda_status kda_forward(const kda_options* opts, const void* q, const void* k,
                                   const void* v, const void* g_raw, const void* beta_raw,
                                   float scale, float lower_bound, const void* initial_state,
@@ -244,11 +253,17 @@ extern "C" kda_status kda_forward(const kda_options* opts, const void* q, const 
                                   void* workspace, size_t workspace_bytes, void* stream) {
   if (!opts) return KDA_ERR_INVALID_ARG;
   const int32_t sc = opts->schedule, sd = opts->state_dtype, gt = opts->gate;
-  if (sc != KDA_SCHEDULE_SPLIT && sc != KDA_SCHEDULE_FUSED && sc != KDA_SCHEDULE_DECODE)
+  if (sc != KDA_SCHEDULE_SPLIT && sc != KDA_SCHEDULE_FUSED && sc != KDA_SCHEDULE_DECODE &&
+      sc != KDA_SCHEDULE_SEGMENTED)
     return KDA_ERR_INVALID_ARG;
   if ((sd != KDA_STATE_F32 && sd != KDA_STATE_BF16) ||
       (gt != KDA_GATE_PER_CHANNEL && gt != KDA_GATE_PER_HEAD))
     return KDA_ERR_INVALID_ARG;
+  if (sc == KDA_SCHEDULE_SEGMENTED)
+    return segmented_forward(FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
+                             g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens,
+                             T_total, H, N, D, out, final_state, 0, workspace, workspace_bytes,
+                             stream);
   const int schedule = sc == KDA_SCHEDULE_SPLIT ? 0 : sc == KDA_SCHEDULE_FUSED ? 1 : 2;
   return forward(schedule, FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
                  g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens, T_total, H, N,
@@ -322,17 +337,17 @@ extern "C" size_t kda_segmented_workspace_size(int64_t T_total, int32_t H, int32
   return static_cast<size_t>(seg_layout(T_total, H, N, P).total);
 }
 
-extern "C" kda_status kda_fwd_segmented(const void* q, const void* k, const void* v,
-                                        const void* g_raw, const void* beta_raw, float scale,
-                                        float lower_bound, const float* initial_state,
-                                        const int32_t* cu_seqlens, int64_t T_total, int32_t H,
-                                        int32_t N, int32_t D, void* out, float* final_state,
-                                        int32_t segments, int32_t gate, void* workspace,
-                                        size_t workspace_bytes, void* stream) {
+namespace {
+
+// The segmented pass behind kda_fwd_segmented and KDA_SCHEDULE_SEGMENTED.
+kda_status segmented_forward(FwdOpts opts, const void* q, const void* k, const void* v,
+                             const void* g_raw, const void* beta_raw, float scale,
+                             float lower_bound, const void* initial_state,
+                             const int32_t* cu_seqlens, int64_t T_total, int32_t H, int32_t N,
+                             int32_t D, void* out, void* final_state, int32_t segments,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   kda_status s = seg_checks(T_total, H, N, D, segments, cu_seqlens);
   if (s != KDA_OK) return s;
-  if (gate != KDA_GATE_PER_CHANNEL && gate != KDA_GATE_PER_HEAD) return KDA_ERR_INVALID_ARG;
-  const FwdOpts opts{0, gate == KDA_GATE_PER_HEAD};
   if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total,
                         opts.gate_scalar != 0)) != KDA_OK)
     return s;
@@ -365,11 +380,27 @@ extern "C" kda_status kda_fwd_segmented(const void* q, const void* k, const void
   if (e == cudaSuccess)
     e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
                      cu_seg, T_total, H, Nseg, out, xs, opts, SegArgs{P, y, ms}, info.err, st);
-  if (e == cudaSuccess) e = launch_affine_scan(xs, ms, N, P, H, final_state, st);
+  if (e == cudaSuccess)
+    e = launch_affine_scan(xs, ms, N, P, H, final_state, opts.state_bf16 != 0, st);
   if (e == cudaSuccess)
     e = launch_seg_fixup(cu_seg, blk, Nseg, H, xs, y, out, info.sm_count, st);
   if (!workspace) cudaFreeAsync(ws, st);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_fwd_segmented(const void* q, const void* k, const void* v,
+                                        const void* g_raw, const void* beta_raw, float scale,
+                                        float lower_bound, const float* initial_state,
+                                        const int32_t* cu_seqlens, int64_t T_total, int32_t H,
+                                        int32_t N, int32_t D, void* out, float* final_state,
+                                        int32_t segments, int32_t gate, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (gate != KDA_GATE_PER_CHANNEL && gate != KDA_GATE_PER_HEAD) return KDA_ERR_INVALID_ARG;
+  return segmented_forward(FwdOpts{0, gate == KDA_GATE_PER_HEAD}, q, k, v, g_raw, beta_raw,
+                           scale, lower_bound, initial_state, cu_seqlens, T_total, H, N, D, out,
+                           final_state, segments, workspace, workspace_bytes, stream);
 }
 
 extern "C" kda_status kda_device_status(void* stream) {

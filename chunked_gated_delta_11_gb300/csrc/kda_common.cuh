@@ -85,7 +85,9 @@ struct FwdOpts {
 //   blocks [0, N H)      X role: the segment from a zero state (the first
 //                        segment of each sequence from that sequence's initial
 //                        state, element ((n / P) H + h) of `init`), outputs to
-//                        `out`, final state to `final_state` [N, H, V, K];
+//                        `out`, final state to `final_state` [N, H, V, K]
+//                        (always fp32 here; FwdOpts.state_bf16 then concerns
+//                        `init` only);
 //   blocks [N H, 2 N H)  M role: the same segment with v = 0 from the identity,
 //                        whose state is the product of the segment's
 //                        transition matrices and whose outputs are those

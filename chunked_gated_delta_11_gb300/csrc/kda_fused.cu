@@ -181,10 +181,12 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_STATE_REGS));
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
+    // a segmented launch writes every piece's final state to its fp32 workspace
+    const bool final_bf16 = opts.state_bf16 && seg.P == 0;
     state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, mrole ? seg.y : out,
                state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
-                        state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
-               opts.state_bf16, err, smem + F_OST_OFF, release, mrole);
+                        state_base + static_cast<int64_t>(t) * kDim, final_bf16),
+               final_bf16, err, smem + F_OST_OFF, release, mrole);
   }
   tc_fence_before();
   __syncthreads();

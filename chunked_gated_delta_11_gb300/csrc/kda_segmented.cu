@@ -21,7 +21,8 @@
 //                           its first segment) -> out, X; M role (v = 0 from
 //                           the identity: its state is M_t, its output y_t);
 //   3. affine_scan_kernel   per (sequence, head): S_0 of every later segment
-//                           and the final state, S <- S M_j + X_j in fp32;
+//                           and the final state (fp32 or bf16), S <- S M_j + X_j
+//                           in fp32;
 //   4. seg_fixup_kernel     out_t += S_0 y_t for the tokens of later segments
 //                           (bf16 tensor-core MMA, fp32 accumulation).
 #include "kda_chunk.cuh"
@@ -80,7 +81,7 @@ constexpr int SC_SMEM = (kDim * SC_LD + kDim * kDim) * 4;
 
 __global__ void __launch_bounds__(SC_THREADS)
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
-                   float* __restrict__ final_state) {
+                   void* __restrict__ final_state, bool final_bf16) {
   extern __shared__ float4 sc_smem4[];
   float* St = reinterpret_cast<float*>(sc_smem4);
   float* Ms = St + kDim * SC_LD;
@@ -132,8 +133,15 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
     __syncthreads();
   }
   if (final_state) {
-    float* f = final_state + (static_cast<int64_t>(n) * H + h) * kDim * kDim + row0;
-    for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
+    const int64_t f0 = (static_cast<int64_t>(n) * H + h) * kDim * kDim + row0;
+    if (final_bf16) {
+      __nv_bfloat16* f = static_cast<__nv_bfloat16*>(final_state) + f0;
+      for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS)
+        f[i] = __float2bfloat16_rn(St[(i & 127) * SC_LD + (i >> 7)]);
+    } else {
+      float* f = static_cast<float*>(final_state) + f0;
+      for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
+    }
   }
 }
 
@@ -264,7 +272,7 @@ cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, in
 }
 
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
-                               float* final_state, cudaStream_t stream) {
+                               void* final_state, bool final_bf16, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     const cudaError_t e = cudaFuncSetAttribute(
@@ -275,7 +283,7 @@ cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
   const int64_t units = static_cast<int64_t>(N) * H * SC_SPLIT;
   if (units == 0) return cudaSuccess;
   affine_scan_kernel<<<static_cast<unsigned>(units), SC_THREADS, SC_SMEM, stream>>>(
-      xs, ms, N, P, H, final_state);
+      xs, ms, N, P, H, final_state, final_bf16);
   return cudaGetLastError();
 }
 

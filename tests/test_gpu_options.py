@@ -10,7 +10,7 @@ from kda_testlib import assert_close, f64, oracle_case
 
 pytestmark = pytest.mark.gpu
 
-SCHEDULES = ["fused", "split", "decode"]
+SCHEDULES = ["fused", "split", "decode", "segmented"]
 
 
 def to_dev(inp):

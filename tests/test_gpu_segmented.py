@@ -149,3 +149,23 @@ def test_segmented_without_final_state_and_small_workspace():
     with pytest.raises(kda.KdaError) as e:
         segmented(inp, 3, workspace=small)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("per_head", [False, True])
+def test_segmented_schedule_options_bf16_states(per_head):
+    # kda_forward with the segmented schedule: bf16 initial and final states
+    # (the pieces' states stay fp32 inside), per-channel or per-head gate; the
+    # automatic count splits 512 chunks of 2 heads into 8 pieces
+    inp = to_dev(synth.make_inputs(8192, 2, 1, seed=65, init_std=0.02, g_mean=-3.0))
+    assert kda.kda_segments_auto(8192, 2, 1) > 1
+    init16 = inp["initial_state"].to(torch.bfloat16)
+    g = inp["g_raw"][:, :, 0].contiguous() if per_head else inp["g_raw"]
+    out, fs = kda.kda_forward(inp["q"], inp["k"], inp["v"], g, inp["beta_raw"], inp["scale"],
+                              inp["lower_bound"], init16, None, N=1, schedule="segmented")
+    assert kda.kda_device_status() == 0
+    assert fs.dtype == torch.bfloat16
+    ref = dict(inp, initial_state=init16.float(),
+               g_raw=g[:, :, None].expand(-1, -1, 128).contiguous() if per_head else g)
+    ro, rs = oracle_case(ref)
+    assert_close(f64(out), ro, "segmented schedule out (bf16 states)")
+    assert_close(f64(fs), rs, "segmented schedule final_state (bf16 states)")
