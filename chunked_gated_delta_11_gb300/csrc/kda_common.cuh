@@ -383,6 +383,34 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int64_t T_total, i
   }
 }
 
+// Longest-first order of packed sequences.  The chunkwise kernels run one CTA
+// per (sequence, head) and CTAs start in blockIdx order, so a varlen batch
+// whose longest sequences come last ends with a tail of a few long units.
+// Starting the longest sequences first (list scheduling, longest processing
+// time first) shortens it.  Returns the sequence of rank r (lengths
+// descending, ties by index).  Every thread of the CTA must call it.  It uses
+// `scratch` (kOrderMaxN + 1 ints of shared memory) and ends with a barrier,
+// after which scratch is free again.  For N <= kOrderMaxN; the cost is
+// N^2 / blockDim comparisons per thread.
+constexpr int kOrderMaxN = 256;
+static __device__ __noinline__ int seq_by_rank(const int32_t* __restrict__ cu, int N, int r,
+                                           int* scratch) {
+  int* len = scratch;
+  int* pick = scratch + kOrderMaxN;
+  for (int m = threadIdx.x; m < N; m += blockDim.x) len[m] = __ldg(cu + m + 1) - __ldg(cu + m);
+  __syncthreads();
+  for (int m = threadIdx.x; m < N; m += blockDim.x) {
+    const int lm = len[m];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) rank += (len[j] > lm) | ((len[j] == lm) & (j < m));
+    if (rank == r) *pick = m;  // ranks are a permutation: exactly one writer
+  }
+  __syncthreads();
+  const int n = *pick;
+  __syncthreads();
+  return n;
+}
+
 __host__ __device__ __forceinline__ int64_t slot_count(int64_t T_total, int N) {
   return T_total / kChunk + N + 1;
 }

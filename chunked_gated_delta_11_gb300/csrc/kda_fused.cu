@@ -72,7 +72,12 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   int unit = blockIdx.x;
   const bool mrole = seg.P > 0 && unit >= N * H;  // segmented launch, M role (SegArgs)
   if (mrole) unit -= N * H;
-  const int n = unit / H, h = unit - (unit / H) * H;
+  const int h = unit - (unit / H) * H;
+  // packed sequences start longest first (seq_by_rank); the chunk scratch is
+  // free until the build starts
+  const int n = (seg.P == 0 && cu && N > 1 && N <= kOrderMaxN)
+                    ? seq_by_rank(cu, N, unit / H, reinterpret_cast<int*>(smem + F_CHUNK_OFF))
+                    : unit / H;
   // a first segment starts from the sequence's own state: it needs no M role
   if (mrole && n % seg.P == 0) return;
   // initial state: the M role starts from the identity, a later segment from

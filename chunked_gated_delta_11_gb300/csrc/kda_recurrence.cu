@@ -29,7 +29,12 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
   auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + K2_CTL_OFF);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int unit = blockIdx.x;
-  const int n = unit / H, h = unit - (unit / H) * H;
+  const int h = unit - (unit / H) * H;
+  // packed sequences start longest first (seq_by_rank); the record ring is
+  // free until the first copy is issued
+  const int n = (cu && N > 1 && N <= kOrderMaxN)
+                    ? seq_by_rank(cu, N, unit / H, reinterpret_cast<int*>(smem))
+                    : unit / H;
   int64_t bos, eos;
   seq_bounds(cu, T_total, N, n, bos, eos);
   const int nchunks = static_cast<int>((eos - bos + kChunk - 1) / kChunk);
