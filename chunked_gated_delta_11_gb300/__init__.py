@@ -24,7 +24,8 @@ __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
     "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc",
-    "kda_fwd_segmented", "kda_segments_auto", "kda_segmented_workspace_size", "REC_BYTES", "CHUNK", "HEAD_DIM",
+    "kda_fwd_segmented", "kda_segments_auto", "kda_segmented_workspace_size",
+    "kda_validate_cu_seqlens", "REC_BYTES", "CHUNK", "HEAD_DIM",
 ]
 
 CHUNK = 16
@@ -97,6 +98,8 @@ def load(build_if_missing: bool = False):
         lib.kda_segmented_workspace_size.restype = sz
         lib.kda_segments_auto.argtypes = [i64, i32, i32]
         lib.kda_segments_auto.restype = i32
+        lib.kda_validate_cu_seqlens.argtypes = [P, i32, i64, P]
+        lib.kda_validate_cu_seqlens.restype = ctypes.c_int
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]
         lib.kda_selftest_tcgen05.restype = ctypes.c_int
         _lib = lib
@@ -364,6 +367,15 @@ def kda_chunk_recurrence(workspace, T_total, H, out, initial_state=None, final_s
                                      _ptr(final_state), _stream(stream))
     _check(st, "kda_chunk_recurrence")
     return out, final_state
+
+
+def kda_validate_cu_seqlens(cu_seqlens, T_total: int, stream=None):
+    """Queue the device check of cu_seqlens (starts at 0, non-decreasing, ends at
+    T_total); a violation shows as KDA_ERR_INVALID_ARG from kda_device_status()."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    st = load().kda_validate_cu_seqlens(_ptr(cu_seqlens), cu_seqlens.numel() - 1, int(T_total),
+                                        _stream(stream))
+    _check(st, "kda_validate_cu_seqlens")
 
 
 def kda_device_status(stream=None) -> int:

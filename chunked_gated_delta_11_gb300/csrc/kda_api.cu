@@ -33,9 +33,24 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const voi
                           const void* init, const int32_t* cu, int64_t T_total, int H, int N,
                           void* out, void* final_state, FwdOpts opts, cudaStream_t stream);
 
-// Error word written by kernels when a bounded wait runs out.  Kernels get its
-// address as an argument; cudaGetSymbolAddress is resolved once per device.
+// Error word written by kernels: KDA_ERR_TIMEOUT when a bounded wait runs out,
+// KDA_ERR_INVALID_ARG when validate_cu_kernel finds a bad cu_seqlens.  Kernels
+// get its address as an argument; cudaGetSymbolAddress is resolved once per
+// device.
 __device__ int g_kda_error = 0;
+
+// cu_seqlens must start at 0, be non-decreasing and end at T_total.  One
+// thread per entry; the first violation found latches KDA_ERR_INVALID_ARG
+// (later ones leave it).  No trap: the host reads the word back.
+__global__ void validate_cu_kernel(const int32_t* __restrict__ cu, int N, int64_t T_total,
+                                   int* __restrict__ err) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= N; i += gridDim.x * blockDim.x) {
+    const int64_t c = __ldg(cu + i);
+    bool bad = (i == 0 && c != 0) || (i == N && c != T_total);
+    if (i < N) bad = bad || __ldg(cu + i + 1) < c;
+    if (bad) atomicCAS(err, 0, static_cast<int>(KDA_ERR_INVALID_ARG));
+  }
+}
 
 namespace {
 
@@ -415,9 +430,24 @@ extern "C" kda_status kda_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpy(info.err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return KDA_ERR_LAUNCH;
-    return KDA_ERR_TIMEOUT;
+    return word == KDA_ERR_INVALID_ARG ? KDA_ERR_INVALID_ARG : KDA_ERR_TIMEOUT;
   }
   return KDA_OK;
+}
+
+extern "C" kda_status kda_validate_cu_seqlens(const int32_t* cu_seqlens, int32_t N,
+                                              int64_t T_total, void* stream) {
+  if (!cu_seqlens || N <= 0 || T_total < 0 || T_total >= (static_cast<int64_t>(1) << 31) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0)
+    return KDA_ERR_INVALID_ARG;
+  DeviceInfo info;
+  const kda_status s = device_info(info);
+  if (s != KDA_OK) return s;
+  const int threads = 256;
+  const int64_t blocks = (static_cast<int64_t>(N) + threads) / threads;
+  validate_cu_kernel<<<static_cast<unsigned>(blocks < 1024 ? blocks : 1024), threads, 0,
+                       static_cast<cudaStream_t>(stream)>>>(cu_seqlens, N, T_total, info.err);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 extern "C" const char* kda_status_string(kda_status status) {

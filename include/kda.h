@@ -29,7 +29,8 @@
  *   cu_seqlens       int32 [N + 1] on the device, or NULL.  With it, sequence
  *                    n is tokens [cu_seqlens[n], cu_seqlens[n+1]); it must
  *                    start at 0, be non-decreasing and end at T_total (not
- *                    checked: the values live on the device).  Without it
+ *                    checked by the forward calls, since the values live on
+ *                    the device: kda_validate_cu_seqlens checks them).  Without it
  *                    there are N sequences of T_total / N tokens each.
  *   D must be 128 (the head size the kernels are built for).
  *
@@ -250,10 +251,22 @@ size_t kda_segmented_workspace_size(int64_t T_total, int32_t H, int32_t N, int32
 int32_t kda_segments_auto(int64_t T_total, int32_t H, int32_t N);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
- * current device: KDA_OK, or KDA_ERR_TIMEOUT if a kernel's bounded wait ran
- * out since the last call (its outputs are then invalid), or KDA_ERR_LAUNCH if
- * the synchronisation itself failed. */
+ * current device: KDA_OK; KDA_ERR_TIMEOUT if a kernel's bounded wait ran out
+ * since the last call (its outputs are then invalid); KDA_ERR_INVALID_ARG if
+ * kda_validate_cu_seqlens found a bad cu_seqlens; or KDA_ERR_LAUNCH if the
+ * synchronisation itself failed. */
 kda_status kda_device_status(void* stream);
+
+/* Checks on the device, asynchronously on `stream`, what the forward entry
+ * points assume of a device cu_seqlens [N + 1]: it starts at 0, never
+ * decreases and ends at T_total.  A violation latches KDA_ERR_INVALID_ARG in
+ * the device error word (read it with kda_device_status); nothing traps.
+ * The forward calls themselves do not check (the values live on the device);
+ * run this first on untrusted input.  Returns KDA_ERR_INVALID_ARG for a null
+ * or misaligned pointer, N <= 0, or T_total outside [0, 2^31), and
+ * KDA_ERR_LAUNCH if the launch fails. */
+kda_status kda_validate_cu_seqlens(const int32_t* cu_seqlens, int32_t N, int64_t T_total,
+                                   void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* kda_status_string(kda_status status);

@@ -143,3 +143,11 @@ def test_segmented_rejects_bad_arguments(lib):
     assert call(q=FAKE + 8) == 1
     assert call(T=65, N=2) == 1
     assert call(T=1 << 31) == 1
+
+
+def test_validate_cu_seqlens_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    assert lib.kda_validate_cu_seqlens(None, 2, 10, None) == 1           # null
+    assert lib.kda_validate_cu_seqlens(P(FAKE), 0, 10, None) == 1        # no sequences
+    assert lib.kda_validate_cu_seqlens(P(FAKE + 2), 2, 10, None) == 1    # misaligned
+    assert lib.kda_validate_cu_seqlens(P(FAKE), 2, 1 << 31, None) == 1   # int32 range
