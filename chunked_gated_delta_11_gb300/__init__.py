@@ -459,10 +459,19 @@ def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state
         with torch.cuda.stream(work[gi]):
             if cu_g is not None:
                 cu_g.record_stream(work[gi])
+            # the split and segmented schedules get their workspace from torch's
+            # caching allocator (reused across calls) rather than the library's
+            # per-call stream-ordered allocation
+            extra = {}
+            nbytes = {"split": lambda: kda_workspace_size(t1 - t0, H, n1 - n0),
+                      "segmented": lambda: kda_segmented_workspace_size(t1 - t0, H, n1 - n0)
+                      }.get(schedule, lambda: 0)()
+            if nbytes > 0:
+                extra["workspace"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
             fwd(dev["q"][t0:t1], dev["k"][t0:t1], dev["v"][t0:t1], dev["g_raw"][t0:t1],
                 dev["beta_raw"][t0:t1], scale, lower_bound,
                 None if init_d is None else init_d[n0:n1], cu_g, N=n1 - n0,
-                out=out_d[t0:t1], final_state=fs_d[n0:n1], stream=work[gi])
+                out=out_d[t0:t1], final_state=fs_d[n0:n1], stream=work[gi], **extra)
             done = torch.cuda.Event()
             done.record(work[gi])
         copy_out.wait_event(done)
