@@ -64,12 +64,12 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # is four times the b2 capture: b8 processes four times the units, and the
 # traffic is the per-unit inputs, outputs and states.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 537.990912e6 + 120.364800e6,
-    ("b8", "fused"): 4 * (537.990912e6 + 120.364800e6),
+    ("b2", "fused"): 538.057216e6 + 120.378624e6,
+    ("b8", "fused"): 4 * (538.057216e6 + 120.378624e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
     # the whole kda_fwd_segmented step: its four launches on the long workload
-    ("long", "segmented"): 15.872e3 + (4702.772480e6 + 1910.221312e6) + 18.889216e6
-                           + (1734.583040e6 + 813.687040e6),
+    ("long", "segmented"): 16.384e3 + (4728.619520e6 + 1910.813184e6) + 18.883584e6
+                           + (1734.418432e6 + 813.688576e6),
 }
 
 
