@@ -76,3 +76,40 @@ def test_writes_stay_inside_outputs(schedule):
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, f"{schedule} out (guarded)")
     assert_close(f64(fs), rs, f"{schedule} final_state (guarded)")
+
+
+def _random_cases(n, seed=2024):
+    import random
+    rng = random.Random(seed)
+    special = [0, 1, 15, 16, 17, 31, 33, 64]
+    cases = []
+    for i in range(n):
+        k = rng.randint(1, 6)
+        lengths = [rng.choice(special) if rng.random() < 0.5 else rng.randint(1, 700)
+                   for _ in range(k)]
+        if sum(lengths) == 0:
+            lengths[0] = 5
+        cases.append((i, lengths, rng.randint(1, 3), rng.random() < 0.5, rng.randint(2, 6)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(8), ids=lambda c: f"case{c[0]}")
+def test_random_packings_all_schedules(case):
+    # seeded random packings (lengths around the chunk size, empty sequences,
+    # long ones), head counts, with or without initial states, through every
+    # schedule, each against the oracle
+    i, lengths, H, init, pieces = case
+    inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=100 + i,
+                                   init_std=0.02 if init else None))
+    ro, rs = oracle_case(inp)
+    a = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+         inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"])
+    N = inp["N"]
+    for name, run in (("fused", lambda: kda.kda_fwd_fused(*a, N=N)),
+                      ("split", lambda: kda.kda_fwd(*a, N=N)),
+                      ("decode", lambda: kda.kda_decode(*a, N=N)),
+                      ("segmented", lambda: kda.kda_fwd_segmented(*a, N=N, segments=pieces))):
+        out, fs = run()
+        assert kda.kda_device_status() == 0, name
+        assert_close(f64(out), ro, f"{name} out {lengths} H={H}")
+        assert_close(f64(fs), rs, f"{name} final_state {lengths} H={H}")
