@@ -70,7 +70,7 @@ typedef enum kda_status {
 size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D);
 
 /* Whole forward pass: chunk kernel (K1) then recurrence kernel (K2).
- * workspace: device buffer of at least kda_workspace_size(...) bytes, 256-byte
+ * workspace: device buffer of at least kda_workspace_size(...) bytes, 16-byte
  * aligned, or NULL, in which case libkda allocates it with cudaMallocAsync on
  * `stream` and frees it with cudaFreeAsync after the kernels.
  * scale: the read scale (1 / sqrt(D) in the pages); lower_bound in [-5, 0]:
