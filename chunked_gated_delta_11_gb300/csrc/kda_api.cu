@@ -24,7 +24,8 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
 cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, int32_t* cu_seg,
                             int32_t* blk, cudaStream_t stream);
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
-                               void* final_state, bool final_bf16, cudaStream_t stream);
+                               void* final_state, bool final_bf16, int sm_count,
+                               cudaStream_t stream);
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
                              cudaStream_t stream);
@@ -396,7 +397,7 @@ kda_status segmented_forward(FwdOpts opts, const void* q, const void* k, const v
     e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
                      cu_seg, T_total, H, Nseg, out, xs, opts, SegArgs{P, y, ms}, info.err, st);
   if (e == cudaSuccess)
-    e = launch_affine_scan(xs, ms, N, P, H, final_state, opts.state_bf16 != 0, st);
+    e = launch_affine_scan(xs, ms, N, P, H, final_state, opts.state_bf16 != 0, info.sm_count, st);
   if (e == cudaSuccess)
     e = launch_seg_fixup(cu_seg, blk, Nseg, H, xs, y, out, info.sm_count, st);
   if (!workspace) cudaFreeAsync(ws, st);

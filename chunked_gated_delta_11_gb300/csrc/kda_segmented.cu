@@ -65,82 +65,98 @@ __global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total,
 
 // ---------------------------------------------------------------------------
 // The scan.  Rows of S M + X depend only on the same rows of S, so each
-// (sequence, head) is split over SC_SPLIT CTAs of SC_ROWS value rows.  256
-// threads, each owning a 4 x 4 block of the CTA's 32 x 128 rows.  The rows are
-// kept transposed in shared memory (St[k][v], row stride SC_LD floats) so
-// that a thread's 4 values of one key column are one float4 load; M_j is
-// staged row-major.  xs holds the X role's final states [N P, H, V, K]; for
-// every later segment j its entry is replaced by that segment's starting state
-// S_0 (read by the fix-up).
+// (sequence, head) is split over 128 / ROWS CTAs of ROWS value rows (the
+// launcher takes the smallest ROWS whose grid fits one CTA per SM: few units,
+// more CTAs per unit and shorter steps).  256 threads, each owning a
+// (ROWS / 8) x 4 block of the CTA's rows.  The rows are kept transposed in
+// shared memory (St[k][v], row stride ROWS + 4 floats) so that a thread's
+// values of one key column are contiguous.  M_j is staged row-major in one of
+// two buffers by cp.async, M_{j+1} arriving while step j computes.  xs holds
+// the X role's final states [N P, H, V, K]; for every later segment j its
+// entry is replaced by that segment's starting state S_0 (read by the fix-up).
 // ---------------------------------------------------------------------------
 constexpr int SC_THREADS = 256;
-constexpr int SC_SPLIT = 4;
-constexpr int SC_ROWS = kDim / SC_SPLIT;  // 32
-constexpr int SC_LD = SC_ROWS + 4;
-constexpr int SC_SMEM = (kDim * SC_LD + kDim * kDim) * 4;
 
+template <int ROWS>
+constexpr int sc_smem() { return (kDim * (ROWS + 4) + 2 * kDim * kDim) * 4; }
+
+__device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) {
+#pragma unroll 4
+  for (int i = t; i < kDim * kDim / 4; i += SC_THREADS)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 4 * i)),
+                 "l"(src + 4 * i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int ROWS>
 __global__ void __launch_bounds__(SC_THREADS)
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
                    void* __restrict__ final_state, bool final_bf16) {
+  constexpr int SPLIT = kDim / ROWS, LD = ROWS + 4, RA = ROWS / 8;
   extern __shared__ float4 sc_smem4[];
   float* St = reinterpret_cast<float*>(sc_smem4);
-  float* Ms = St + kDim * SC_LD;
-  const int unit = blockIdx.x / SC_SPLIT, part = blockIdx.x - unit * SC_SPLIT;
+  float* Mbuf = St + kDim * LD;  // two [128][128] buffers
+  const int unit = blockIdx.x / SPLIT, part = blockIdx.x - unit * SPLIT;
   const int n = unit / H, h = unit - (unit / H) * H;
   const int t = threadIdx.x;
-  const int rv = (t >> 5) * 4, ck = (t & 31) * 4;  // local value rows rv.., key columns ck..
-  const int64_t row0 = static_cast<int64_t>(part) * SC_ROWS * kDim;  // first row of the part
+  const int rv = (t >> 5) * RA, ck = (t & 31) * 4;  // local value rows rv.., key columns ck..
+  const int64_t row0 = static_cast<int64_t>(part) * ROWS * kDim;  // first row of the part
   auto base = [&](int64_t s) { return (s * H + h) * kDim * kDim; };
   const int64_t s0 = static_cast<int64_t>(n) * P;
+  if (P > 1) sc_stage_m(Mbuf, ms + base(s0 + 1), t);
   {
     const float* x0 = xs + base(s0) + row0;
-    for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) St[(i & 127) * SC_LD + (i >> 7)] = x0[i];
+    for (int i = t; i < ROWS * kDim; i += SC_THREADS) St[(i & 127) * LD + (i >> 7)] = x0[i];
   }
-  __syncthreads();
   for (int j = 1; j < P; ++j) {
+    const float* Ms = Mbuf + ((j - 1) & 1) * kDim * kDim;
     float* xj = xs + base(s0 + j) + row0;
-    const float4* mj = reinterpret_cast<const float4*>(ms + base(s0 + j));
-    for (int i = t; i < kDim * kDim / 4; i += SC_THREADS) reinterpret_cast<float4*>(Ms)[i] = mj[i];
-    float acc[4][4];
+    float acc[RA][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < RA; ++a) {
       const float4 x = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck);
       acc[a][0] = x.x; acc[a][1] = x.y; acc[a][2] = x.z; acc[a][3] = x.w;
     }
-    __syncthreads();  // M_j staged
+    // M_j has arrived; its other buffer was last read in step j - 1, which
+    // every thread has finished (barrier at the end of the previous step)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    if (j + 1 < P) sc_stage_m(Mbuf + (j & 1) * kDim * kDim, ms + base(s0 + j + 1), t);
 #pragma unroll 4
     for (int kk = 0; kk < kDim; ++kk) {
-      const float4 sa = *reinterpret_cast<const float4*>(St + kk * SC_LD + rv);
+      float sv[RA];
+#pragma unroll
+      for (int a = 0; a < RA; ++a) sv[a] = St[kk * LD + rv + a];
       const float4 ma = *reinterpret_cast<const float4*>(Ms + kk * kDim + ck);
-      const float sv[4] = {sa.x, sa.y, sa.z, sa.w};
       const float mv[4] = {ma.x, ma.y, ma.z, ma.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < RA; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
     }
     // segment j starts from the S before this step (X_j was read above)
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < RA; ++a)
       *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
-          make_float4(St[ck * SC_LD + rv + a], St[(ck + 1) * SC_LD + rv + a],
-                      St[(ck + 2) * SC_LD + rv + a], St[(ck + 3) * SC_LD + rv + a]);
-    __syncthreads();  // every read of St and Ms is done
+          make_float4(St[ck * LD + rv + a], St[(ck + 1) * LD + rv + a],
+                      St[(ck + 2) * LD + rv + a], St[(ck + 3) * LD + rv + a]);
+    __syncthreads();  // every read of St and of this M buffer is done
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < RA; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) St[(ck + b) * SC_LD + rv + a] = acc[a][b];
-    __syncthreads();
+      for (int b = 0; b < 4; ++b) St[(ck + b) * LD + rv + a] = acc[a][b];
   }
+  __syncthreads();
   if (final_state) {
     const int64_t f0 = (static_cast<int64_t>(n) * H + h) * kDim * kDim + row0;
     if (final_bf16) {
       __nv_bfloat16* f = static_cast<__nv_bfloat16*>(final_state) + f0;
-      for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS)
-        f[i] = __float2bfloat16_rn(St[(i & 127) * SC_LD + (i >> 7)]);
+      for (int i = t; i < ROWS * kDim; i += SC_THREADS)
+        f[i] = __float2bfloat16_rn(St[(i & 127) * LD + (i >> 7)]);
     } else {
       float* f = static_cast<float*>(final_state) + f0;
-      for (int i = t; i < SC_ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * SC_LD + (i >> 7)];
+      for (int i = t; i < ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * LD + (i >> 7)];
     }
   }
 }
@@ -271,20 +287,38 @@ cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
-                               void* final_state, bool final_bf16, cudaStream_t stream) {
+template <int ROWS>
+cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H,
+                                 void* final_state, bool final_bf16, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     const cudaError_t e = cudaFuncSetAttribute(
-        affine_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM);
+        affine_scan_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, sc_smem<ROWS>());
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int64_t units = static_cast<int64_t>(N) * H * SC_SPLIT;
-  if (units == 0) return cudaSuccess;
-  affine_scan_kernel<<<static_cast<unsigned>(units), SC_THREADS, SC_SMEM, stream>>>(
+  const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
+  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), SC_THREADS, sc_smem<ROWS>(), stream>>>(
       xs, ms, N, P, H, final_state, final_bf16);
   return cudaGetLastError();
+}
+
+cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
+                               void* final_state, bool final_bf16, int sm_count,
+                               cudaStream_t stream) {
+  const int64_t units = static_cast<int64_t>(N) * H;
+  if (units == 0) return cudaSuccess;
+  // the most CTAs per (sequence, head) that still fit one per SM
+  const int64_t slots = sm_count;
+  if (units * 16 <= slots)
+    return launch_affine_scan_t<8>(xs, ms, N, P, H, final_state, final_bf16, stream);
+  if (units * 8 <= slots)
+    return launch_affine_scan_t<16>(xs, ms, N, P, H, final_state, final_bf16, stream);
+  if (units * 4 <= slots)
+    return launch_affine_scan_t<32>(xs, ms, N, P, H, final_state, final_bf16, stream);
+  if (units * 2 <= slots)
+    return launch_affine_scan_t<64>(xs, ms, N, P, H, final_state, final_bf16, stream);
+  return launch_affine_scan_t<128>(xs, ms, N, P, H, final_state, final_bf16, stream);
 }
 
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,

@@ -169,3 +169,17 @@ def test_segmented_schedule_options_bf16_states(per_head):
     ro, rs = oracle_case(ref)
     assert_close(f64(out), ro, "segmented schedule out (bf16 states)")
     assert_close(f64(fs), rs, "segmented schedule final_state (bf16 states)")
+
+
+@pytest.mark.parametrize("n_seq,H", [(24, 2), (40, 2)])
+def test_segmented_many_units(n_seq, H):
+    # 48 and 80 (sequence, head) units: the scan runs with 64 and 128 value
+    # rows per CTA (one CTA per SM), the shapes few-unit cases never reach
+    import random
+    rng = random.Random(n_seq)
+    lengths = [rng.randint(60, 400) for _ in range(n_seq)]
+    inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=66, init_std=0.02))
+    out, fs = segmented(inp, 2)
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, f"segmented, {n_seq * H} units, out")
+    assert_close(f64(fs), rs, f"segmented, {n_seq * H} units, final_state")
