@@ -68,8 +68,8 @@ MEASURED_TRAFFIC = {
     ("b8", "fused"): 4 * (538.057216e6 + 120.378624e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
     # the whole kda_fwd_segmented step: its four launches on the long workload
-    ("long", "segmented"): 16.384e3 + (4728.619520e6 + 1910.813184e6) + 18.883584e6
-                           + (1734.418432e6 + 813.688576e6),
+    ("long", "segmented"): 15.872e3 + (4745.593856e6 + 1911.234304e6) + 18.883840e6
+                           + (1734.559744e6 + 814.011904e6),
 }
 
 
