@@ -1,7 +1,9 @@
 // kda_fused.cu -- the single-kernel forward path.  One CTA per (sequence,
 // head) builds each chunk record in shared memory and runs the recurrence on
 // it, so the records never travel through HBM: HBM traffic is the algorithmic
-// q, k, v, g_raw, beta_raw in and out out (plus the states).
+// q, k, v, g_raw and beta_raw in, `out` out (plus the states).  Packed
+// sequences start longest first (seq_by_rank in kda_common.cuh).  A segmented
+// launch (SegArgs, kda_common.cuh) runs two CTA roles per (segment, head).
 //
 // Roles (256 threads, two CTAs per SM):
 //   warps 0-3  state threads (tensor-memory lanes 0-127); thread 0 also
