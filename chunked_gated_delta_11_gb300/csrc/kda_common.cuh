@@ -34,6 +34,7 @@
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -72,6 +73,21 @@ __host__ __device__ constexpr int u_offset(int c, int i) {
   return OFF_U + c * 64 + (((i >> 2) ^ u_piece_swz(c)) << 4) + ((i & 3) << 2);
 }
 __host__ __device__ constexpr int aqk_offset(int i, int j) { return ka_offset(128 + i, j); }
+
+// A kernel's dynamic shared-memory limit, set once per device: the attribute
+// belongs to the function in the current device's context, so a process that
+// drives several GPUs sets it on each.  `done` is the launcher's mask of
+// devices already set (devices >= 64 set it on every call).
+inline cudaError_t ensure_smem_limit(const void* func, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Per-call options of the forward pass (uniform over the grid).
 struct FwdOpts {

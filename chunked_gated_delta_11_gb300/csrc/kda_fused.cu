@@ -206,18 +206,22 @@ cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const vo
                            const void* init, const int32_t* cu, int64_t T_total, int H, int N,
                            void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
                            cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    // the register split above is only safe if every thread starts with F_REGS
+  // the register split above is only safe if every thread starts with F_REGS
+  static std::atomic<uint64_t> checked{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev >= 64 || !(checked.load(std::memory_order_acquire) & (uint64_t{1} << dev))) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<kGateScalar>);
+    const cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<kGateScalar>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != F_REGS) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(fused_kernel<kGateScalar>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, F_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
+    if (dev < 64) checked.fetch_or(uint64_t{1} << dev, std::memory_order_release);
   }
+  static std::atomic<uint64_t> smem_set{0};
+  if (const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fused_kernel<kGateScalar>),
+                                              F_SMEM, smem_set);
+      e != cudaSuccess)
+    return e;
   const int64_t units = static_cast<int64_t>(N) * H * (seg.P > 0 ? 2 : 1);
   if (units == 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -87,15 +87,12 @@ cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const
                               int gate_scalar, int sm_count, cudaStream_t stream) {
   const int64_t n_items = slot_count(T_total, N) * H;
   const int smem = static_cast<int>(sizeof(PrepSmem));
-  static bool attr_done = false;  // per process; the attribute is per function
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e =
+      ensure_smem_limit(reinterpret_cast<const void*>(chunk_prep_kernel), smem, smem_set);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_prep_kernel, 128, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_prep_kernel, 128, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t grid = (n_items < static_cast<int64_t>(sm_count) * per_sm ? n_items : static_cast<int64_t>(sm_count) * per_sm);

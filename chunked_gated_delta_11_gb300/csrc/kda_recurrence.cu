@@ -102,13 +102,11 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
 cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
                               int64_t T_total, int H, int N, void* out, void* final_state,
                               FwdOpts opts, int* err, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(recurrence_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, K2_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (const cudaError_t e =
+          ensure_smem_limit(reinterpret_cast<const void*>(recurrence_kernel), K2_SMEM, smem_set);
+      e != cudaSuccess)
+    return e;
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units == 0) return cudaSuccess;
   recurrence_kernel<<<static_cast<unsigned>(units), K2_THREADS, K2_SMEM, stream>>>(

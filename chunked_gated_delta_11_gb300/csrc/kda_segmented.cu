@@ -290,13 +290,11 @@ cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, in
 template <int ROWS>
 cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H,
                                  void* final_state, bool final_bf16, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        affine_scan_kernel<ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, sc_smem<ROWS>());
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (const cudaError_t e = ensure_smem_limit(
+          reinterpret_cast<const void*>(affine_scan_kernel<ROWS>), sc_smem<ROWS>(), smem_set);
+      e != cudaSuccess)
+    return e;
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
   affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), SC_THREADS, sc_smem<ROWS>(), stream>>>(
       xs, ms, N, P, H, final_state, final_bf16);
@@ -324,13 +322,11 @@ cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
                              cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        seg_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FX_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (const cudaError_t e =
+          ensure_smem_limit(reinterpret_cast<const void*>(seg_fixup_kernel), FX_SMEM, smem_set);
+      e != cudaSuccess)
+    return e;
   if (Nseg == 0) return cudaSuccess;
   seg_fixup_kernel<<<static_cast<unsigned>(3 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
       cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(y),
