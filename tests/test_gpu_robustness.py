@@ -113,3 +113,63 @@ def test_random_packings_all_schedules(case):
         assert kda.kda_device_status() == 0, name
         assert_close(f64(out), ro, f"{name} out {lengths} H={H}")
         assert_close(f64(fs), rs, f"{name} final_state {lengths} H={H}")
+
+
+@pytest.mark.parametrize("schedule", ["fused", "split", "decode", "segmented"])
+def test_cuda_graph_capture_and_replay(schedule):
+    # every schedule is capturable (asynchronous, no host synchronisation, no
+    # allocation outside the stream-ordered kind) and replays to the same bits
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[300, 47, 129], seed=72, init_std=0.02))
+    N = inp["N"]
+    a = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+         inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"])
+    out = torch.empty_like(inp["q"])
+    fs = torch.empty((N, 2, 128, 128), dtype=torch.float32, device="cuda")
+    call = {"fused": lambda s: kda.kda_fwd_fused(*a, N=N, out=out, final_state=fs, stream=s),
+            "split": lambda s: kda.kda_fwd(*a, N=N, out=out, final_state=fs, stream=s),
+            "decode": lambda s: kda.kda_decode(*a, N=N, out=out, final_state=fs, stream=s),
+            "segmented": lambda s: kda.kda_fwd_segmented(*a, N=N, segments=3, out=out,
+                                                         final_state=fs, stream=s)}[schedule]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(side)                      # eager run (also warms the launchers up)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    o_ref, s_ref = out.clone(), fs.clone()
+    out.zero_()
+    fs.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        call(side)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert kda.kda_device_status() == 0
+        assert torch.equal(out, o_ref) and torch.equal(fs, s_ref), schedule
+
+
+def test_concurrent_streams_match_serial_calls():
+    # the library keeps no per-call state: two passes on two streams at once
+    # give the bits of the same passes run one after the other
+    cases = [to_dev(synth.make_inputs(0, 2, lengths=L, seed=73 + i, init_std=0.02))
+             for i, L in enumerate(([500, 33], [17, 260, 90]))]
+
+    def run(inp, stream):
+        return kda.kda_fwd_fused(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                                 inp["scale"], inp["lower_bound"], inp["initial_state"],
+                                 inp["cu_seqlens"], N=inp["N"], stream=stream)
+    ref = [run(c, torch.cuda.current_stream()) for c in cases]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cases]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    got = []
+    for c, st in zip(cases, streams):
+        with torch.cuda.stream(st):
+            got.append(run(c, st))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    for (o1, s1), (o2, s2) in zip(ref, got):
+        assert torch.equal(o1, o2) and torch.equal(s1, s2)
