@@ -394,20 +394,107 @@ def kda_selftest_tcgen05(device="cuda"):
     return out1, out2, int(status.item())
 
 
+def _host_workspace(schedule, T, H, N, device):
+    """Workspace of a split or segmented pass from torch's caching allocator
+    (reused across calls), or None for the schedules that need none."""
+    nbytes = {"split": lambda: kda_workspace_size(T, H, N),
+              "segmented": lambda: kda_segmented_workspace_size(T, H, N)}.get(schedule,
+                                                                            lambda: 0)()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+
+
+def _forward_host_sliced(fwd, schedule, q, k, v, g_raw, beta_raw, scale, lower_bound,
+                         initial_state, N, device, out, final_state, stream, slices):
+    """kda_forward_host for N equal sequences: every sequence is cut in time
+    into `slices` chunk-aligned slices.  Slice g of all sequences goes
+    host->device (one copy per sequence and tensor, into a slice-major device
+    layout), runs as one pass over all (sequence, head) units starting from the
+    state the previous slice left (updated in place), and goes back while later
+    slices are copied in."""
+    T_total, H, D = q.shape
+    L = T_total // N
+    chunks = (L + CHUNK - 1) // CHUNK
+    G = max(1, min(int(slices), chunks))
+    cuts = [min(L, CHUNK * ((chunks * g) // G)) for g in range(G)] + [L]
+    ins = (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw))
+    dev = {name: torch.empty(t.shape, dtype=t.dtype, device=device) for name, t in ins}
+    out_d = torch.empty((T_total, H, D), dtype=torch.bfloat16, device=device)
+    state_d = torch.empty((N, H, D, D), dtype=torch.float32, device=device)
+    copy_in, copy_out, work = (torch.cuda.Stream(device), torch.cuda.Stream(device),
+                               torch.cuda.Stream(device))
+    start = torch.cuda.Event()
+    start.record(stream)
+    for st in (copy_in, copy_out, work):
+        st.wait_event(start)
+    if initial_state is not None:
+        with torch.cuda.stream(copy_in):
+            state_d.copy_(initial_state, non_blocking=True)
+    ws = None
+    with torch.cuda.stream(work):
+        ws = _host_workspace(schedule, N * max(b - a for a, b in zip(cuts, cuts[1:])), H, N,
+                             device)
+    started = initial_state is not None
+    for a, b in zip(cuts, cuts[1:]):
+        n = b - a
+        if n == 0:
+            continue
+        base = N * a
+        with torch.cuda.stream(copy_in):
+            for name, t in ins:
+                dst = dev[name]
+                for s in range(N):
+                    dst[base + s * n:base + (s + 1) * n].copy_(t[s * L + a:s * L + b],
+                                                               non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(copy_in)
+        work.wait_event(arrived)
+        with torch.cuda.stream(work):
+            sl = slice(base, base + N * n)
+            extra = {} if ws is None else {"workspace": ws}
+            fwd(dev["q"][sl], dev["k"][sl], dev["v"][sl], dev["g_raw"][sl], dev["beta_raw"][sl],
+                scale, lower_bound, state_d if started else None, None, N=N, out=out_d[sl],
+                final_state=state_d, stream=work, **extra)
+            done = torch.cuda.Event()
+            done.record(work)
+        started = True
+        copy_out.wait_event(done)
+        with torch.cuda.stream(copy_out):
+            for s in range(N):
+                out[s * L + a:s * L + b].copy_(out_d[base + s * n:base + (s + 1) * n],
+                                               non_blocking=True)
+    if not started:  # no tokens: the final state is the initial one (zeros here)
+        with torch.cuda.stream(work):
+            state_d.zero_()
+            done = torch.cuda.Event()
+            done.record(work)
+        copy_out.wait_event(done)
+    with torch.cuda.stream(copy_out):
+        final_state.copy_(state_d, non_blocking=True)
+    finished = torch.cuda.Event()
+    finished.record(copy_out)
+    stream.wait_event(finished)
+    for t in list(dev.values()) + [out_d, state_d] + ([ws] if ws is not None else []):
+        for st in (copy_in, copy_out, work):
+            t.record_stream(st)
+    return out, final_state
+
+
 def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
                      cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
                      stream=None, schedule="fused", groups=8):
     """Forward pass on host (CPU, ideally pinned) tensors; returns (out, final_state)
     as host tensors (allocated pinned if not given), ready once `stream` is.
 
-    The sequences are split into up to `groups` contiguous groups.  Group p's
-    inputs go host->device on a copy stream; its forward pass (`schedule`:
-    "fused" = kda_fwd_fused, "split" = kda_fwd, "decode" = kda_decode,
-    "segmented" = kda_fwd_segmented) runs on a stream of its own once they have
-    arrived,
-    so it overlaps the copies of the later groups; its outputs go device->host on
-    a third stream, overlapping the remaining input copies (the link carries
-    both directions at once).  `stream` (default: the current stream) orders the
+    The pass (`schedule`: "fused" = kda_fwd_fused, "split" = kda_fwd,
+    "decode" = kda_decode, "segmented" = kda_fwd_segmented) overlaps the copies:
+    - the sequences are split into up to `groups` contiguous groups, each run
+      on a stream of its own once its inputs have arrived;
+    - fewer than `groups` equal sequences (no cu_seqlens) are instead cut in
+      time into up to `groups` chunk-aligned slices; slice p runs over all
+      sequences once its inputs have arrived, from the state slice p - 1 left.
+    Inputs go host->device on one copy stream and outputs device->host on
+    another, overlapping the remaining input copies (the link carries both
+    directions at once).  `stream` (default: the current stream) orders the
     whole call: nothing starts before work already queued on it, and it waits
     for the last copy."""
     stream = torch.cuda.current_stream(device) if stream is None else stream
@@ -415,17 +502,20 @@ def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state
            "segmented": kda_fwd_segmented}[schedule]
     T_total, H, D, N = _geometry(q, None, N) if cu_seqlens is None else (
         q.shape[0], q.shape[1], q.shape[2], cu_seqlens.shape[0] - 1)
-    if cu_seqlens is not None:
-        bounds = [int(x) for x in cu_seqlens.tolist()]
-    else:
-        if T_total % max(N, 1):
-            raise ValueError("T_total must be a multiple of N without cu_seqlens")
-        L = T_total // max(N, 1)
-        bounds = [n * L for n in range(N + 1)]
+    if cu_seqlens is None and T_total % max(N, 1):
+        raise ValueError("T_total must be a multiple of N without cu_seqlens")
     if out is None:
         out = torch.empty((T_total, H, D), dtype=torch.bfloat16, pin_memory=True)
     if final_state is None:
         final_state = torch.empty((N, H, D, D), dtype=torch.float32, pin_memory=True)
+    if cu_seqlens is None and N < groups:
+        # too few sequences to form the groups: slices in time
+        return _forward_host_sliced(fwd, schedule, q, k, v, g_raw, beta_raw, scale, lower_bound,
+                                    initial_state, N, device, out, final_state, stream, groups)
+    if cu_seqlens is None:
+        bounds = [n * (T_total // N) for n in range(N + 1)]
+    else:
+        bounds = [int(x) for x in cu_seqlens.tolist()]
     dev = {name: torch.empty(t.shape, dtype=t.dtype, device=device)
            for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw))}
     init_d = None if initial_state is None else torch.empty(initial_state.shape,
@@ -462,12 +552,8 @@ def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state
             # the split and segmented schedules get their workspace from torch's
             # caching allocator (reused across calls) rather than the library's
             # per-call stream-ordered allocation
-            extra = {}
-            nbytes = {"split": lambda: kda_workspace_size(t1 - t0, H, n1 - n0),
-                      "segmented": lambda: kda_segmented_workspace_size(t1 - t0, H, n1 - n0)
-                      }.get(schedule, lambda: 0)()
-            if nbytes > 0:
-                extra["workspace"] = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            ws = _host_workspace(schedule, t1 - t0, H, n1 - n0, device)
+            extra = {} if ws is None else {"workspace": ws}
             fwd(dev["q"][t0:t1], dev["k"][t0:t1], dev["v"][t0:t1], dev["g_raw"][t0:t1],
                 dev["beta_raw"][t0:t1], scale, lower_bound,
                 None if init_d is None else init_d[n0:n1], cu_g, N=n1 - n0,

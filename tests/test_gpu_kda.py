@@ -344,3 +344,20 @@ def test_zero_query_and_key_rows(path):
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, "out")
     assert_close(f64(fs), rs, "final_state")
+
+
+@pytest.mark.parametrize("schedule", ["fused", "split", "decode", "segmented"])
+def test_host_buffer_entry_point_time_slices(schedule):
+    # equal sequences with initial states: the host-buffer entry point cuts
+    # them in time into chunk-aligned slices chained through the state
+    inp = synth.make_inputs(3 * 500, 2, 3, seed=12, init_std=0.02)
+    pin = {key: (inp[key].pin_memory() if inp[key] is not None else None)
+           for key in ("q", "k", "v", "g_raw", "beta_raw", "initial_state")}
+    out, fs = kda.kda_forward_host(pin["q"], pin["k"], pin["v"], pin["g_raw"], pin["beta_raw"],
+                                   inp["scale"], inp["lower_bound"], pin["initial_state"],
+                                   N=3, schedule=schedule, groups=5)
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, f"{schedule} host slices out")
+    assert_close(f64(fs), rs, f"{schedule} host slices final_state")
