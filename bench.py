@@ -253,7 +253,7 @@ def main():
                          "otherwise")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-units", type=int, default=0,
-                    help="oracle sample size for cpu_baseline (0 = one unit per core)")
+                    help="oracle sample size for cpu_baseline (0 = up to 16 units per core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -424,7 +424,9 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        n_units = args.cpu_units or min(2 * cores, units)
+        # about 10-100 s of CPU work: the whole step when it has at most
+        # 16 units per core (b8 on 16 cores), else 16 units per core
+        n_units = args.cpu_units or min(16 * cores, units)
         secs, th = oracle_sample(inp, n_units, cores)
         line["cpu_baseline"] = {
             "value": th / H / secs, "unit": "tokens/s", "cores": min(cores, n_units),
