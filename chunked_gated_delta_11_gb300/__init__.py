@@ -32,7 +32,7 @@ CHUNK = 16
 HEAD_DIM = 128
 REC_BYTES = 26112
 
-SCHEDULES = {"split": 0, "fused": 1, "decode": 2, "segmented": 3}
+SCHEDULES = {"split": 0, "fused": 1, "decode": 2, "segmented": 3, "auto": 4}
 
 
 class _Options(ctypes.Structure):
@@ -245,7 +245,9 @@ def kda_forward(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None
     the tensors: states fp32 or bf16 (both the same; the final state is allocated
     with the initial state's dtype), g_raw [T_total, H, 128] (per channel) or
     [T_total, H] (one gate per token and head).  schedule: "fused", "split",
-    "decode" or "segmented" (automatic piece count).  Returns (out, final_state)."""
+    "decode", "segmented" (automatic piece count) or "auto" (decode for at most
+    8 tokens per sequence, segmented when the units are too few for the SMs,
+    fused otherwise).  Returns (out, final_state)."""
     T_total, H, D, N = _geometry(q, cu_seqlens, N)
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name, torch.bfloat16, (T_total, H, D))

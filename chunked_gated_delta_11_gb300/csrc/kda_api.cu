@@ -253,6 +253,7 @@ extern "C" kda_status kda_decode(const void* q, const void* k, const void* v, co
 }
 
 namespace {
+int32_t auto_segments(int64_t T_total, int32_t H, int32_t N, int sms);
 kda_status segmented_forward(FwdOpts opts, const void* q, const void* k, const void* v,
                              const void* g_raw, const void* beta_raw, float scale,
                              float lower_bound, const void* initial_state,
@@ -270,17 +271,31 @@ extern "C" kda_status kda_forward(const kda_options* opts, const void* q, const 
   if (!opts) return KDA_ERR_INVALID_ARG;
   const int32_t sc = opts->schedule, sd = opts->state_dtype, gt = opts->gate;
   if (sc != KDA_SCHEDULE_SPLIT && sc != KDA_SCHEDULE_FUSED && sc != KDA_SCHEDULE_DECODE &&
-      sc != KDA_SCHEDULE_SEGMENTED)
+      sc != KDA_SCHEDULE_SEGMENTED && sc != KDA_SCHEDULE_AUTO)
     return KDA_ERR_INVALID_ARG;
   if ((sd != KDA_STATE_F32 && sd != KDA_STATE_BF16) ||
       (gt != KDA_GATE_PER_CHANNEL && gt != KDA_GATE_PER_HEAD))
     return KDA_ERR_INVALID_ARG;
-  if (sc == KDA_SCHEDULE_SEGMENTED)
+  int32_t sched = sc;
+  if (sc == KDA_SCHEDULE_AUTO) {
+    kda_status s = check_sizes(T_total, H, N, D, cu_seqlens);
+    if (s != KDA_OK) return s;
+    DeviceInfo info;
+    if ((s = device_info(info)) != KDA_OK) return s;
+    if (T_total <= 8 * static_cast<int64_t>(N))
+      sched = KDA_SCHEDULE_DECODE;  // serving steps: the state traffic dominates
+    else if (T_total < (static_cast<int64_t>(1) << 31) &&
+             auto_segments(T_total, H, N, info.sm_count) > 1)
+      sched = KDA_SCHEDULE_SEGMENTED;  // too few units for the SMs
+    else
+      sched = KDA_SCHEDULE_FUSED;
+  }
+  if (sched == KDA_SCHEDULE_SEGMENTED)
     return segmented_forward(FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
                              g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens,
                              T_total, H, N, D, out, final_state, 0, workspace, workspace_bytes,
                              stream);
-  const int schedule = sc == KDA_SCHEDULE_SPLIT ? 0 : sc == KDA_SCHEDULE_FUSED ? 1 : 2;
+  const int schedule = sched == KDA_SCHEDULE_SPLIT ? 0 : sched == KDA_SCHEDULE_FUSED ? 1 : 2;
   return forward(schedule, FwdOpts{sd == KDA_STATE_BF16, gt == KDA_GATE_PER_HEAD}, q, k, v,
                  g_raw, beta_raw, scale, lower_bound, initial_state, cu_seqlens, T_total, H, N,
                  D, out, final_state, workspace, workspace_bytes, stream);

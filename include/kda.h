@@ -113,12 +113,15 @@ kda_status kda_decode(const void* q, const void* k, const void* v, const void* g
 
 /* Options of kda_forward. */
 enum { KDA_SCHEDULE_SPLIT = 0, KDA_SCHEDULE_FUSED = 1, KDA_SCHEDULE_DECODE = 2,
-       KDA_SCHEDULE_SEGMENTED = 3 };
+       KDA_SCHEDULE_SEGMENTED = 3, KDA_SCHEDULE_AUTO = 4 };
 enum { KDA_STATE_F32 = 0, KDA_STATE_BF16 = 1 };
 enum { KDA_GATE_PER_CHANNEL = 0, KDA_GATE_PER_HEAD = 1 };
 typedef struct {
   int32_t schedule;     /* KDA_SCHEDULE_*: kda_fwd (split), kda_fwd_fused, kda_decode,
-                           kda_fwd_segmented (automatic piece count) */
+                           kda_fwd_segmented (automatic piece count), or AUTO:
+                           decode for at most 8 tokens per sequence on average,
+                           segmented when kda_segments_auto() > 1 (too few
+                           (sequence, head) units for the SMs), fused otherwise */
   int32_t state_dtype;  /* KDA_STATE_*: dtype of initial_state and final_state (both) */
   int32_t gate;         /* KDA_GATE_*: g_raw [T_total, H, D] or [T_total, H] */
 } kda_options;
@@ -135,8 +138,9 @@ typedef struct {
  *   Have Come Up with Kimi Delta Attention", sec. 3), with the same gate map
  *   log alpha = lower_bound * sigmoid(g_raw).
  * workspace / workspace_bytes are used by KDA_SCHEDULE_SPLIT (as in kda_fwd)
- * and KDA_SCHEDULE_SEGMENTED (kda_segmented_workspace_size with segments = 0;
- * NULL = allocated on the stream); the segmented schedule keeps every piece's
+ * and KDA_SCHEDULE_SEGMENTED or an AUTO choice of it
+ * (kda_segmented_workspace_size with segments = 0; NULL = allocated on the
+ * stream); the segmented schedule keeps every piece's
  * states in fp32 and converts only initial_state and final_state.  Everything
  * else is as in kda_fwd; a null `opts` or an unknown option value returns
  * KDA_ERR_INVALID_ARG. */

@@ -111,7 +111,7 @@ def test_forward_rejects_bad_options(lib):
     P = ctypes.c_void_p
     args = [P(FAKE)] * 5 + [0.1, -5.0, None, None, 64, 1, 1, 128, P(FAKE), P(FAKE), None, 0, None]
     assert lib.kda_forward(None, *args) == 1                      # no options
-    for bad in ((4, 0, 0), (1, 2, 0), (1, 0, 2), (-1, 0, 0)):
+    for bad in ((5, 0, 0), (1, 2, 0), (1, 0, 2), (-1, 0, 0)):
         opts = kda._Options(*bad)
         assert lib.kda_forward(ctypes.byref(opts), *args) == 1, bad
     opts = kda._Options(1, 0, 0)

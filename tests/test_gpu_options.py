@@ -10,7 +10,7 @@ from kda_testlib import assert_close, f64, oracle_case
 
 pytestmark = pytest.mark.gpu
 
-SCHEDULES = ["fused", "split", "decode", "segmented"]
+SCHEDULES = ["fused", "split", "decode", "segmented", "auto"]
 
 
 def to_dev(inp):
@@ -65,3 +65,16 @@ def test_forward_split_with_workspace_and_fp32_states_matches_kda_fwd():
     o2, s2 = kda.kda_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
                          inp["scale"], inp["lower_bound"], inp["initial_state"], None, N=1)
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("lengths,H", [
+    ([1] * 48, 2),          # serving step: decode
+    ([8192], 2),            # one long sequence, few units: segmented
+    ([64] * 80, 4),         # many units: fused
+])
+def test_auto_schedule(lengths, H):
+    inp = to_dev(synth.make_inputs(0, H, lengths=lengths, seed=81, init_std=0.02))
+    out, fs = forward(inp, "auto")
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, f"auto out {len(lengths)} x {lengths[0]}")
+    assert_close(f64(fs), rs, f"auto final_state {len(lengths)} x {lengths[0]}")
