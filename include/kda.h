@@ -25,7 +25,9 @@
  *   beta_raw         bf16 [T_total, H]
  *   out              bf16 [T_total, H, D]
  *   initial_state    fp32 [N, H, V, K] or NULL (= zeros), V = K = D
- *   final_state      fp32 [N, H, V, K] or NULL (= not written)
+ *   final_state      fp32 [N, H, V, K] or NULL (= not written); it may be the
+ *                    initial_state buffer (updated in place) on every
+ *                    schedule
  *   cu_seqlens       int32 [N + 1] on the device, or NULL.  With it, sequence
  *                    n is tokens [cu_seqlens[n], cu_seqlens[n+1]); it must
  *                    start at 0, be non-decreasing and end at T_total (not

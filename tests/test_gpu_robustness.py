@@ -173,3 +173,39 @@ def test_concurrent_streams_match_serial_calls():
     assert kda.kda_device_status() == 0
     for (o1, s1), (o2, s2) in zip(ref, got):
         assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("schedule", ["fused", "split", "decode"])
+def test_no_final_state_requested(schedule):
+    # final_state = NULL: the pass writes only `out`, which matches the oracle
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[200, 31], seed=74, init_std=0.02))
+    a = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+         inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"])
+    fn = {"fused": kda.kda_fwd_fused, "split": kda.kda_fwd, "decode": kda.kda_decode}[schedule]
+    out, fs = fn(*a, N=inp["N"], output_final_state=False)
+    assert fs is None
+    assert kda.kda_device_status() == 0
+    ro, _ = oracle_case(inp)
+    assert_close(f64(out), ro, f"{schedule} out without a final state")
+
+
+@pytest.mark.parametrize("schedule", ["fused", "split", "segmented"])
+def test_state_updated_in_place(schedule):
+    # final_state may be the initial_state buffer: each (sequence, head) reads
+    # its initial state before it writes its final state
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[300, 70], seed=75, init_std=0.02))
+    ro, rs = oracle_case(inp)
+    state = inp["initial_state"].clone()
+    a = (inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+         inp["lower_bound"], state, inp["cu_seqlens"])
+    kw = dict(N=inp["N"], final_state=state)
+    if schedule == "fused":
+        out, fs = kda.kda_fwd_fused(*a, **kw)
+    elif schedule == "split":
+        out, fs = kda.kda_fwd(*a, **kw)
+    else:
+        out, fs = kda.kda_fwd_segmented(*a, segments=3, **kw)
+    assert kda.kda_device_status() == 0
+    assert fs.data_ptr() == state.data_ptr()
+    assert_close(f64(out), ro, f"{schedule} out (state in place)")
+    assert_close(f64(state), rs, f"{schedule} final_state (in place)")
