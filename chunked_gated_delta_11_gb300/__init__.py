@@ -30,7 +30,7 @@ __all__ = [
 
 CHUNK = 16
 HEAD_DIM = 128
-REC_BYTES = 26112
+REC_BYTES = 26176
 
 SCHEDULES = {"split": 0, "fused": 1, "decode": 2, "segmented": 3, "auto": 4}
 

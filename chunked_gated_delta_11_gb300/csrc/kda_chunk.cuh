@@ -16,11 +16,11 @@
 // The normalisation is applied to the 16 x 16 matrices and the 16 per-token
 // rows instead of the 128-channel factors, so the factor pass needs no norm:
 // with D = diag(rk), the record holds
-//   Qdec = diag(rq) qP,  Kend' = kQ (= D^-1 Kend),  Aqk' = lower(diag(rq) Mqk)
-//   (= Aqk D^-1),  W' = D W,  U' = D U,
+//   Qdec = qP,  Kend' = kQ (= D^-1 Kend),  Aqk' = lower(Mqk) (= diag(rq)^-1 Aqk D^-1),
+//   W' = D W,  U' = D U,  and rq,
 // and the recurrence computes E'^T = U' - W' S^T = D E^T, S += E' Kend' and
-// O = Qdec S^T + Aqk' E'^T, which equal the unscaled products (rho and chi of
-// sec. 6.3/6.5 and the state update of sec. 6.4).  W' and U' come from
+// O = diag(rq) (Qdec S^T + Aqk' E'^T), which equal the unscaled products (rho
+// and chi of sec. 6.3/6.5 and the state update of sec. 6.4).  W' and U' come from
 //   R' = D R D^-1 = strictly-lower(diag(beta rk^2) Mkk),  A' = (I + R')^-1 = D A D^-1
 //   W' = A' diag(beta rk^2) kP,   U' = A' diag(beta rk) V.
 // Decay factors are prefix/suffix products of per-token retention factors, so
@@ -309,7 +309,11 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     if ((w & 1) == 0 && l < 16) {
       const float s2 = S.g2[w][l] + S.g2[w + 1][l];
       if (nx == RAW_Q)
-        S.rq[l] = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
+      {
+        const float r = scale * rsqrtf(s2 + eps);  // the read scale is folded into q's norm
+        S.rq[l] = r;
+        *reinterpret_cast<float*>(rec + OFF_RQ + 4 * l) = r;
+      }
       else
         S.rk[l] = rsqrtf(s2 + eps);
     }
@@ -318,7 +322,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   const float2 Hh = Pl[7];
   const float2 Ho = make_float2(__shfl_xor_sync(0xffffffffu, Hh.x, 1),
                                 __shfl_xor_sync(0xffffffffu, Hh.y, 1));
-  float2 Qu[8];  // q P of this thread's tokens (normalised once rq is known)
+  float2 Qu[8];  // q P of this thread's tokens (Qdec; rq is applied to the outputs)
   {
     const float2 one = make_float2(1.f, 1.f);
     const float2 dl = hf ? __fmul2_rn(Ho, Hh) : __fmul2_rn(Hh, Ho);  // same product in both lanes
@@ -386,13 +390,10 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
       ldsm_x2_t_at(br, bbase + kk * 512);
       mma16816(acc2[kk & 1], ar, br[0], br[1]);
     }
-    // Qdec = diag(rq) qP, bf16 rows 0..15 of [Qdec ; W'] (this thread's pairs)
+    // Qdec = qP, bf16 rows 0..15 of [Qdec ; W'] (this thread's pairs)
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = hf * 8 + ii;
-      const float r = S.rq[i];
-      *reinterpret_cast<uint32_t*>(rec + b1_offset(i, d0)) = pack_bf16(Qu[ii].x * r, Qu[ii].y * r);
-    }
+    for (int ii = 0; ii < 8; ++ii)
+      *reinterpret_cast<uint32_t*>(rec + b1_offset(hf * 8 + ii, d0)) = pack_bf16(Qu[ii].x, Qu[ii].y);
     float acc[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) acc[e] = acc2[0][e] + acc2[1][e];
@@ -409,11 +410,10 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
           S.Rt[m][i] = m < i ? f * acc[2 * h2 + o] : 0.f;
         }
       } else {
-        const float f = S.rq[i];
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
           const int j = c0 + o;
-          *reinterpret_cast<float*>(rec + aqk_offset(i, j)) = j <= i ? f * acc[2 * h2 + o] : 0.f;
+          *reinterpret_cast<float*>(rec + aqk_offset(i, j)) = j <= i ? acc[2 * h2 + o] : 0.f;
         }
       }
     }

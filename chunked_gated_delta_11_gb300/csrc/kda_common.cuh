@@ -31,6 +31,9 @@
 //                      row c; its four 16-byte pieces (4 tokens each) in the
 //                      order p ^ (2 ((c >> 1) & 1) + ((c >> 2) & 1)).
 //   [OFF_DL, +512)     dlast fp32 [128] = diagonal of D_{0:C-1}.
+//   [OFF_RQ, +64)      rq fp32 [16]: the query factors s / |q_i| that Qdec and
+//                      Aqk' leave out; the recurrence scales each output row
+//                      by them.
 // Rows of tokens past a ragged sequence end are zero, which makes them no-ops.
 #pragma once
 
@@ -49,9 +52,10 @@ constexpr int OFF_KA = 8192;
 constexpr int KA_TILE = 4608;  // one K=8 tile of [Kend ; Aqk]: 144 rows x 32 B
 constexpr int OFF_U = OFF_KA + 2 * KA_TILE;
 constexpr int OFF_DL = OFF_U + 8192;
-constexpr int REC_BYTES = OFF_DL + 512;  // 26112
+constexpr int OFF_RQ = OFF_DL + 512;
+constexpr int REC_BYTES = OFF_RQ + 64;  // 26176
 constexpr int REC_STRIDE_SMEM = 26624;   // 1024-aligned stage stride in smem
-static_assert(REC_BYTES == 26112 && REC_STRIDE_SMEM >= REC_BYTES, "record layout");
+static_assert(REC_BYTES == 26176 && REC_STRIDE_SMEM >= REC_BYTES, "record layout");
 
 __host__ __device__ constexpr int b1_offset(int n, int d) {
   // byte offset of bf16 element (row n, channel d) of the [Qdec ; W] tile

@@ -38,7 +38,7 @@ constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
 constexpr int F_RAW_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 127) & ~127);
 constexpr int F_V_OFF = F_RAW_OFF + 2 * QKG_BYTES;  // q, k, g_raw double-buffered
 constexpr int F_OST_OFF = F_V_OFF + V_BYTES;
-constexpr int F_CTL_OFF = F_OST_OFF + 4096;
+constexpr int F_CTL_OFF = F_OST_OFF + 4096 + 256;  // output staging, then rq slots
 constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
 static_assert(2 * (F_SMEM + 1024) <= 228 * 1024, "fused kernel must fit two CTAs per SM");

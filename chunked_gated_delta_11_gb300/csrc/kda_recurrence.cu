@@ -14,7 +14,7 @@ namespace kda {
 constexpr int K2_NST = 4;
 constexpr int K2_THREADS = 128;
 constexpr int K2_OST_OFF = K2_NST * REC_STRIDE_SMEM;
-constexpr int K2_CTL_OFF = K2_OST_OFF + 4096;
+constexpr int K2_CTL_OFF = K2_OST_OFF + 4096 + 256;  // output staging, then rq slots
 constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 1024 + 64;
 static_assert(2 * (K2_SMEM + 1024) <= 228 * 1024, "recurrence kernel must fit two CTAs per SM");
 

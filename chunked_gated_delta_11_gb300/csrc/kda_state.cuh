@@ -17,8 +17,8 @@
 //        E'^T -> tensor memory (fp32; the MMA reads its tf32 part)
 //   MMA2 (kind::tf32, M=128 N=144 K=16, 2 instructions), D = [S | D1 cols 0-15]:
 //        S[v][d]    += sum_j E'^T[v][j] Kend'[j][d]        (write, sec. 6.4)
-//        D1[v][i]   += sum_j E'^T[v][j] Aqk'[i][j]  -> o[i][v] (read, sec. 6.5)
-//   state threads: o read out; then, once record c+1 is there,
+//        D1[v][i]   += sum_j E'^T[v][j] Aqk'[i][j]  -> o[i][v] / rq_i (read, sec. 6.5)
+//   state threads: o read out and scaled by the record's rq; then, once record c+1 is there,
 //        Sb = bf16(S) (= bf16(S_{c+1})),  S *= dlast_{c+1}   (forget, sec. 6.4)
 //   while MMA1 of chunk c+1 runs: o -> bf16 -> out.
 //
@@ -175,7 +175,8 @@ __device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* b
 // `final_dst` is thread v's row of the final state (fp32, or bf16 if
 // `state_bf16`; null = not written).
 // `ostage` is 4 KB of shared memory (1 KB per state warp) that turns each
-// warp's 16 x 32 output tile into 16-byte stores.  u_zero: the records carry
+// warp's 16 x 32 output tile into 16-byte stores, followed by 256 B (64 B per
+// state warp) that hold the chunk's rq between the U' read and the output.  u_zero: the records carry
 // no U' (v is zero), which is taken as zero.
 template <int NST, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
@@ -184,6 +185,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
                                            __nv_bfloat16* __restrict__ out, void* final_dst,
                                            bool state_bf16, int* err, uint8_t* ostage,
                                            StageFree&& stage_free, bool u_zero = false) {
+  float* rqstage = reinterpret_cast<float*>(ostage + 4096) + (v >> 5) * 16;
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
   // chunk 0: snapshot the initial state and apply chunk 0's decay
@@ -228,10 +230,14 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
         pk[i4 * 4 + 3] = __float_as_uint(e1.y);
       }
       tmem_st16(tb + TM_E + lane_off, pk);
+      // the query factors the record's Qdec and Aqk' leave out: copied with U'
+      // to this warp's slot, since the stage may be released once MMA2 is done
+      if ((v & 31) < 4)
+        reinterpret_cast<float4*>(rqstage)[v & 3] = reinterpret_cast<const float4*>(st + OFF_RQ)[v & 3];
       tmem_wait_st();
       tc_fence_before();
     }
-    // every state thread has written E^T and finished reading U
+    // every state thread has written E^T and finished reading U' and rq
     if (!state_all(ok)) { ok = false; break; }
     if (v == 0) {
       tc_fence_after();
@@ -244,6 +250,15 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       tc_fence_after();
       tmem_ld16(tb + TM_D1 + lane_off, o);
       tmem_wait_ld();
+      const float4* rq4 = reinterpret_cast<const float4*>(rqstage);
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 r = rq4[i4];
+        o[4 * i4 + 0] = __float_as_uint(__uint_as_float(o[4 * i4 + 0]) * r.x);
+        o[4 * i4 + 1] = __float_as_uint(__uint_as_float(o[4 * i4 + 1]) * r.y);
+        o[4 * i4 + 2] = __float_as_uint(__uint_as_float(o[4 * i4 + 2]) * r.z);
+        o[4 * i4 + 3] = __float_as_uint(__uint_as_float(o[4 * i4 + 3]) * r.w);
+      }
     }
     if (ok && v == 0) stage_free(c, s);
     if (c + 1 < nchunks) {

@@ -66,7 +66,7 @@ typedef enum kda_status {
 #define KDA_HEAD_DIM 128
 
 /* Bytes of device workspace kda_fwd / kda_chunk_prep / kda_chunk_recurrence
- * need for these sizes: one chunk record (26112 bytes) per (chunk slot, head),
+ * need for these sizes: one chunk record (26176 bytes) per (chunk slot, head),
  * with T_total / 16 + N + 1 chunk slots, enough for any split of T_total
  * tokens into N sequences.  Returns 0 for invalid sizes. */
 size_t kda_workspace_size(int64_t T_total, int32_t H, int32_t N, int32_t D);
@@ -164,7 +164,7 @@ kda_status kda_forward(const kda_options* opts, const void* q, const void* k, co
  * loads the library's device code holds until the process exits.
  * Limit: kda_workspace_size(T_total, H, N, D) must not exceed
  * KDA_NOALLOC_WORKSPACE_BYTES (e.g. T_total + 16 (N + 1) <= 1280 tokens at
- * H = 32, <= 41,120 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
+ * H = 32, <= 41,008 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
  * anything is launched.
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (once per device, with that device current), so make
@@ -183,20 +183,23 @@ kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const vo
 /* K1 alone: the token-parallel chunk kernel.  Writes one record per (chunk,
  * head) into `workspace` (same size rule as kda_fwd; must not be NULL).  For
  * chunk c (0-based) of sequence n and head h the record starts at byte
- *   ((floor(bos_n / 16) + n + c) * H + h) * 26112
+ *   ((floor(bos_n / 16) + n + c) * H + h) * 26176
  * with bos_n the first token of sequence n, and holds, for the chunk's tokens
  * i < 16 (rows past the sequence end are zero), in this order:
- *   [Qdec ; W'] bf16 32 x 128, 128-byte-swizzled K-major tiles;
+ *   [Qdec' ; W'] bf16 32 x 128, 128-byte-swizzled K-major tiles;
  *   [Kend' ; Aqk'] fp32 144 x 16 (Kend'^T rows 0-127, Aqk' rows 128-143), two
  *   32-byte-swizzled K=8 tiles;  U'^T fp32 [128][16];  dlast fp32 [128];
+ *   rq fp32 [16];
  * where (sec. 6.1-6.6 of "You Could Have Come Up with Kimi Delta Attention")
  *   Qdec_i = scale q^_i D_{0:i},  Kend_i = k^_i D_{i+1:last},
  *   Akk = (I + R)^-1 with R_ij = beta_i <k^_j|D_{j+1:i}|k^_i> (j < i),
  *   W = Akk diag(beta) [k^_i D_{0:i}],  U = Akk diag(beta) V,
  *   Aqk_ij = scale <k^_j|D_{j+1:i}|q^_i> (j <= i),  dlast = diag(D_{0:last}),
- * stored with the per-token key norms rk_j = 1 / |k_j| moved between factors
- * (the products the recurrence forms are unchanged):  W'_i = rk_i W_i,
- * U'_i = rk_i U_i,  Kend'_j = Kend_j / rk_j,  Aqk'_ij = Aqk_ij / rk_j.
+ * stored with the per-token norms rk_j = 1 / |k_j| and rq_i = scale / |q_i|
+ * moved between factors (the products the recurrence forms are unchanged):
+ * W'_i = rk_i W_i,  U'_i = rk_i U_i,  Kend'_j = Kend_j / rk_j,
+ * Qdec'_i = Qdec_i / rq_i,  Aqk'_ij = Aqk_ij / (rq_i rk_j), and rq itself, by
+ * which the recurrence scales each output row.
  * The byte layout of each tile is given in chunked_gated_delta_11_gb300/csrc/
  * kda_common.cuh. */
 kda_status kda_chunk_prep(const void* q, const void* k, const void* v, const void* g_raw,

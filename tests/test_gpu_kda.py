@@ -92,18 +92,21 @@ def decode_record(rec):
     uoff = 17408 + cc * 64 + (((ii_ >> 2) ^ swz) << 4) + ((ii_ & 3) << 2)
     U = rec.view(np.float32)[uoff // 4].T
     dl = rec[25600:26112].view(np.float32)
+    rq = rec[26112:26176].view(np.float32)
     return {"Qdec": b1[:16].astype(np.float64), "W": b1[16:].astype(np.float64),
             "Kend": ka[:, :128].astype(np.float64), "Aqk": ka[:, 128:].T.astype(np.float64),
-            "U": U, "dlast": dl}
+            "U": U, "dlast": dl, "rq": rq}
 
 
-def record_convention(f, rk):
+def record_convention(f, rk, rq):
     """The oracle's chunk factors in the record's convention: with D = diag(rk),
-    rk_j = 1 / |k_j| (the key norm of token j), the record holds W' = D W,
-    U' = D U, Kend' = D^-1 Kend and Aqk' = Aqk D^-1, whose products in the
-    recurrence equal the unscaled ones."""
-    return {"Qdec": f["Qdec"], "W": rk[:, None] * f["W"], "U": rk[:, None] * f["U"],
-            "Kend": f["Kend"] / rk[:, None], "Aqk": f["Aqk"] / rk[None, :], "dlast": f["dlast"]}
+    rk_j = 1 / |k_j|, and rq_i = scale / |q_i|, the record holds W' = D W,
+    U' = D U, Kend' = D^-1 Kend, Qdec' = diag(rq)^-1 Qdec and
+    Aqk' = diag(rq)^-1 Aqk D^-1, plus rq; the recurrence's products, with each
+    output row scaled by rq_i, equal the unscaled ones."""
+    return {"Qdec": f["Qdec"] / rq[:, None], "W": rk[:, None] * f["W"],
+            "U": rk[:, None] * f["U"], "Kend": f["Kend"] / rk[:, None],
+            "Aqk": f["Aqk"] / (rq[:, None] * rk[None, :]), "dlast": f["dlast"], "rq": rq}
 
 
 @pytest.mark.parametrize("lengths,H", [([64], 1), ([45], 2), ([7, 0, 33, 16], 2)])
@@ -119,8 +122,9 @@ def test_chunk_records_match_oracle_factors(lengths, H):
                                       f64(inp["beta_raw"]), inp["lower_bound"])
     cu = inp["cu_seqlens"].cpu().numpy()
     f = oracle.chunk_factors(qh, kh, f64(inp["v"]), la, beta, inp["scale"], cu_seqlens=cu)
-    kraw = f64(inp["k"])
+    kraw, qraw = f64(inp["k"]), f64(inp["q"])
     got = {k_: [] for k_ in f if k_ != "Akk"}
+    got["rq"] = []
     ref = {k_: [] for k_ in got}
     chunk = 0
     for n in range(N):
@@ -130,10 +134,13 @@ def test_chunk_records_match_oracle_factors(lengths, H):
                 slot = bos // 16 + n + c
                 r = decode_record(wsh[(slot * H + h) * kda.REC_BYTES:][:kda.REC_BYTES])
                 kc = np.zeros((16, 128))
+                qc = np.zeros((16, 128))
                 t0 = bos + 16 * c
                 kc[:min(16, eos - t0)] = kraw[t0:min(t0 + 16, eos), h]
+                qc[:min(16, eos - t0)] = qraw[t0:min(t0 + 16, eos), h]
                 rk = 1.0 / np.sqrt((kc * kc).sum(-1) + oracle.DEFAULT_EPS)
-                fr = record_convention({k_: f[k_][chunk, h] for k_ in got}, rk)
+                rq = inp["scale"] / np.sqrt((qc * qc).sum(-1) + oracle.DEFAULT_EPS)
+                fr = record_convention({k_: f[k_][chunk, h] for k_ in got if k_ != "rq"}, rk, rq)
                 for key in got:
                     got[key].append(r[key].reshape(-1))
                     ref[key].append(fr[key].reshape(-1))

@@ -104,11 +104,11 @@ def model_forward(inp):
             Au_hi = bf16(Au)
             W = mm(bf16(Aw), bf16(Ku))
             U = mm(Au_hi, vv) + mm(bf16(Au - Au_hi), vv)
-            Qd = rq[..., None] * Qu
-            Aqk = np.tril(rq[..., None] * Mqk)
+            Qd = Qu                 # the record leaves rq out of Qdec and Aqk'
+            Aqk = np.tril(Mqk)
             D1 = mm(bf16(S), bf16(np.concatenate([W, Qd], 1)).transpose(0, 2, 1))
             E = tf32_trunc(U - D1[:, :, :16].transpose(0, 2, 1))
-            O = D1[:, :, 16:].transpose(0, 2, 1) + mm(tf32_trunc(Aqk), E)
+            O = rq[..., None] * (D1[:, :, 16:].transpose(0, 2, 1) + mm(tf32_trunc(Aqk), E))
             S = S * dl[:, None, :] + mm(E.transpose(0, 2, 1), tf32_trunc(Ke))
             out[sl] = bf16(O[:, :nc]).transpose(1, 0, 2)
         fs[n] = S

@@ -40,7 +40,7 @@ def test_noalloc_matches_kda_fwd_on_two_calls():
 
 def test_noalloc_rejects_sizes_beyond_its_array():
     kda.load()
-    T, H = 4096, 32   # needs (4096/16 + 2) slots x 32 heads x 26112 B > 64 MiB
+    T, H = 4096, 32   # needs (4096/16 + 2) slots x 32 heads x 26176 B > 64 MiB
     assert kda.kda_workspace_size(T, H, 1) > kda.NOALLOC_WORKSPACE_BYTES
     x = torch.zeros((T, H, 128), dtype=torch.bfloat16, device="cuda")
     b = torch.zeros((T, H), dtype=torch.bfloat16, device="cuda")
