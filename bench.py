@@ -46,6 +46,12 @@ WORKLOAD_TEXT = {
            "segmented path)",
     "decode": "one serving step: 256 sequences x 1 token, H=32, D=128, bf16, fp32 states "
               "0.02*N(0,1) in and out",
+    "fk96": "FlashKDA benchmark row shape: 1 sequence x 8192 tokens, H=96, D=128, bf16, zero state",
+    "fk64": "FlashKDA benchmark row shape: 1 sequence x 8192 tokens, H=64, D=128, bf16, zero state",
+    "fk96p": "FlashKDA benchmark row shape '1024x8': 8 packed sequences x 1024 tokens (cu_seqlens), "
+             "H=96, D=128, bf16, zero states",
+    "fk64p": "FlashKDA benchmark row shape '1024x8': 8 packed sequences x 1024 tokens (cu_seqlens), "
+             "H=64, D=128, bf16, zero states",
 }
 PATH_TEXT = {
     "fused": "kda_fwd_fused = fused_kernel (chunk math + tcgen05 recurrence, one launch)",

@@ -23,6 +23,11 @@ Workloads (all D = d_k = d_v = 128, lower_bound = -5, scale = 128 ** -0.5):
  b2      profiling size: 2 sequences of 8192 tokens, H = 32
  decode  one serving step: 256 sequences of 1 token, H = 32, initial states
          ~ 0.02 N(0, 1) (the decode regime: moving the states dominates)
+ fk96    the shapes of FlashKDA's published benchmark rows ("FlashKDA v1: A
+ fk64    Deep Dive", benchmark section; T = 8192, D = 128): 1 sequence of 8192
+         tokens, H = 96 or 64; zero initial state
+ fk96p   the same rows' "1024 x 8" form: 8 sequences of 1024 tokens, H = 96
+ fk64p   or 64, passed packed with cu_seqlens; zero initial states
 ======  =====================================================================
 
 Draw order is q, k, v, g_raw, beta_raw, initial_state; sequence lengths come
@@ -52,6 +57,7 @@ class Workload:
     g_mean: float = 0.0
     max_len: int = 0         # variable lengths: upper bound
     seed: int = 0
+    packed: bool = False     # equal lengths T, passed with cu_seqlens
 
 
 WORKLOADS = {
@@ -67,6 +73,10 @@ WORKLOADS = {
     "l32": Workload("l32", H=32, N=1, T=32768, init_std=None, g_mean=2.0, seed=8),
     # one decode step of a serving batch: 256 sequences x 1 new token, states in/out
     "decode": Workload("decode", H=32, N=256, T=1, init_std=0.02, seed=7),
+    "fk96": Workload("fk96", H=96, N=1, T=8192, init_std=None, seed=9),
+    "fk64": Workload("fk64", H=64, N=1, T=8192, init_std=None, seed=10),
+    "fk96p": Workload("fk96p", H=96, N=8, T=1024, init_std=None, seed=11, packed=True),
+    "fk64p": Workload("fk64p", H=64, N=8, T=1024, init_std=None, seed=12, packed=True),
 }
 
 
@@ -134,8 +144,8 @@ def workload_inputs(name: str, device="cpu", seed: int | None = None) -> dict:
     """Inputs of one named workload (see the module docstring)."""
     w = WORKLOADS[name]
     seed = w.seed if seed is None else seed
-    if w.T is None:
-        lengths = varlen_lengths(w.N, w.max_len, seed)
+    if w.T is None or w.packed:
+        lengths = [w.T] * w.N if w.packed else varlen_lengths(w.N, w.max_len, seed)
         return make_inputs(0, w.H, lengths=lengths, seed=seed, init_std=w.init_std,
                            g_mean=w.g_mean, device=device)
     return make_inputs(w.T * w.N, w.H, w.N, seed=seed, init_std=w.init_std,

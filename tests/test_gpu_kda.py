@@ -211,6 +211,10 @@ def test_fwd_empty_input_returns_initial_state(path):
     ("b8", [(0, 0), (3, 17), (7, 31)]),
     ("long", [(0, 0), (0, 31)]),
     ("slow", [(0, 5)]),
+    ("fk96", [(0, 0), (0, 95)]),      # the shapes of FlashKDA's benchmark rows
+    ("fk64", [(0, 63)]),
+    ("fk96p", [(0, 0), (7, 95)]),
+    ("fk64p", [(3, 10)]),
 ])
 @pytest.mark.parametrize("path", PATHS)
 def test_fwd_full_size_sampled_units(name, units, path):

@@ -78,3 +78,18 @@ def test_auto_schedule(lengths, H):
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, f"auto out {len(lengths)} x {lengths[0]}")
     assert_close(f64(fs), rs, f"auto final_state {len(lengths)} x {lengths[0]}")
+
+
+@pytest.mark.parametrize("name,units", [
+    ("fk96", [(0, 0), (0, 95)]),
+    ("fk64", [(0, 7)]),
+    ("fk96p", [(5, 40)]),
+    ("fk64p", [(7, 63)]),
+])
+def test_auto_schedule_on_benchmark_row_shapes(name, units):
+    # FlashKDA's benchmark row shapes: the automatic choice (segmented for the
+    # single sequences, fused for the packed ones) against the oracle
+    from kda_testlib import compare_units
+    inp = synth.workload_inputs(name, device="cuda")
+    out, fs = forward(inp, "auto")
+    compare_units(inp, out, fs, units)
