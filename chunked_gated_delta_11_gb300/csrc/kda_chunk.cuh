@@ -10,9 +10,16 @@
 //   a_i[d] = 2^(lower_bound * log2(e) * sigma(g_raw_i[d]))      (= alpha_i[d])
 //   P_i = prod_{m<=i} a_m = D_{0:i},   Q_i = prod_{i<m<16} a_m = D_{i+1:last}
 //   rq_i = s / |q_i|, rk_i = 1 / |k_i|  (tensor-core Gram diagonals of the raw rows)
-//   the decayed factors of the unnormalised rows:
-//     qP_i = q_i P_i,  kP_i = k_i P_i,  kQ_i = k_i Q_i,  kI_i = k_i Q_i / dlast
-//   Mkk = kP kI^T, Mqk = qP kI^T                         (16 x 16, K = 128)
+//   the decayed factors of the unnormalised rows, taken relative to the
+//   middle of the chunk, m = P_7 (the product over tokens 0-7):
+//     qM_i = q_i P_i / m,  kM_i = k_i P_i / m,  kI_i = k_i m / P_i = k_i Q_i / Q_7,
+//     and kQ_i = k_i Q_i (Kend')
+//   Mkk = kM kI^T, Mqk = qM kI^T                         (16 x 16, K = 128)
+// (m cancels in both products.)  With the midpoint, P_i / m and m / P_i stay
+// within 2^(+-7.3 * 8) at lower_bound = -5, where P_i and 1 / P_i alone reach
+// 2^(+-115.4): a key row k / P_i would overflow fp32 and bf16 for raw
+// |k_d| above about 2^12.6, and k P_i would lose small rows below the normal
+// range, while the midpoint form keeps raw rows up to about 2^60 finite.
 // The normalisation is applied to the 16 x 16 matrices and the 16 per-token
 // rows instead of the 128-channel factors, so the factor pass needs no norm:
 // with D = diag(rk), the record holds
@@ -22,7 +29,7 @@
 // O = diag(rq) (Qdec S^T + Aqk' E'^T), which equal the unscaled products (rho
 // and chi of sec. 6.3/6.5 and the state update of sec. 6.4).  W' and U' come from
 //   R' = D R D^-1 = strictly-lower(diag(beta rk^2) Mkk),  A' = (I + R')^-1 = D A D^-1
-//   W' = A' diag(beta rk^2) kP,   U' = A' diag(beta rk) V.
+//   W' = A' diag(beta rk^2) kP = (A' diag(beta rk^2) kM) Diag(m),   U' = A' diag(beta rk) V.
 // Decay factors are prefix/suffix products of per-token retention factors, so
 // their range is that of D_{0:i} itself: with lower_bound >= -5 and 16 tokens
 // every factor and its inverse stays a normal fp32 number.
@@ -67,12 +74,13 @@ constexpr int V_BYTES = RAW_TILE;            // one chunk's v tile
 // 16-byte halves); drv_off's swizzle keeps the ldmatrix reads and the factor
 // pass's stores conflict-free.
 struct ChunkSmem {
-  uint8_t kd[4096];  // kP
-  uint8_t ki[4096];  // kI
-  uint8_t qd[4096];  // qP
+  uint8_t kd[4096];  // kM = k P / m
+  uint8_t ki[4096];  // kI = k m / P
+  uint8_t qd[4096];  // qM = q P / m
   float Rt[16][RS];  // Rt[m][i] = -R'[i][m] for m < i, 0 otherwise
   float Aw[16][AS];  // A' diag(beta rk^2)
   float Au[16][AS];  // A' diag(beta rk)
+  float pm[128];     // m = P_7 per key channel (the W' columns are scaled by it)
   float rq[16], rk[16], beta[16];
   float g2[4][16];  // partial squared norms (warp w: q for w < 2, k otherwise)
 };
@@ -328,31 +336,40 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     const float2 dl = hf ? __fmul2_rn(Ho, Hh) : __fmul2_rn(Hh, Ho);  // same product in both lanes
     const float2 pre = hf ? Ho : one;  // prod over tokens before the half
     float2 sfx = hf ? one : Ho;        // prod over the tokens after the one being processed
-    const float2 inv_dl = make_float2(rcp_approx(dl.x), rcp_approx(dl.y));
-    if (hf == 0) *reinterpret_cast<float2*>(rec + OFF_DL + d0 * 4) = dl;
+    // midpoint m = P_7 (first half's product) and Q_7 = dlast / m (second half's):
+    // P_i / m = Pl_i / Hh in the first half and Pl_i in the second
+    const float2 h1 = hf ? Ho : Hh, h2 = hf ? Hh : Ho;
+    const float2 rel = hf ? one : make_float2(rcp_approx(Hh.x), rcp_approx(Hh.y));
+    const float2 inv_q7 = make_float2(rcp_approx(h2.x), rcp_approx(h2.y));
+    if (hf == 0) {
+      *reinterpret_cast<float2*>(rec + OFF_DL + d0 * 4) = dl;
+      *reinterpret_cast<float2*>(&S.pm[d0]) = h1;
+    }
     // packed bf16 words, [token pair m] for channel d0 (x) and d0+1 (y)
     uint32_t qx[4], qy[4], kx[4], ky[4], ix[4], iy[4];
     float ex[8], ey[8];  // kQ of channels d0, d0 + 1
 #pragma unroll
     for (int m = 3; m >= 0; --m) {
-      float2 Kd[2], Ki[2];
+      float2 Kd[2], Ki[2], Qm[2];
 #pragma unroll
       for (int o = 1; o >= 0; --o) {
         const int ii = 2 * m + o;
         const float2 Q = sfx;
         sfx = __fmul2_rn(sfx, a[ii]);
         const float2 P = __fmul2_rn(pre, Pl[ii]);
+        const float2 Pm = __fmul2_rn(Pl[ii], rel);  // P_i / m
         const float2 qv = bf2_at(raw + RAW_Q * RAW_TILE + roff(ii));
         const float2 kv = bf2_at(raw + RAW_K * RAW_TILE + roff(ii));
         Qu[ii] = __fmul2_rn(qv, P);
-        Kd[o] = __fmul2_rn(kv, P);
+        Qm[o] = __fmul2_rn(qv, Pm);
+        Kd[o] = __fmul2_rn(kv, Pm);
         const float2 Ke = __fmul2_rn(kv, Q);
-        Ki[o] = __fmul2_rn(Ke, inv_dl);
+        Ki[o] = __fmul2_rn(Ke, inv_q7);
         ex[ii] = Ke.x;
         ey[ii] = Ke.y;
       }
-      qx[m] = pack_bf16(Qu[2 * m].x, Qu[2 * m + 1].x);
-      qy[m] = pack_bf16(Qu[2 * m].y, Qu[2 * m + 1].y);
+      qx[m] = pack_bf16(Qm[0].x, Qm[1].x);
+      qy[m] = pack_bf16(Qm[0].y, Qm[1].y);
       kx[m] = pack_bf16(Kd[0].x, Kd[1].x);
       ky[m] = pack_bf16(Kd[0].y, Kd[1].y);
       ix[m] = pack_bf16(Ki[0].x, Ki[1].x);
@@ -460,7 +477,8 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   {
     const int mi = l >> 3, g = l >> 2, q2 = (l & 3) * 2;
     auto ld2 = [](const float* p) { return *reinterpret_cast<const float2*>(p); };
-    // W' [i][c]: A = A' diag(beta rk^2) [i][j] (bf16), B = kP^T tile [c][j] ([n][k] order)
+    // W' [i][c] = m_c (A' diag(beta rk^2) kM)[i][c]: A = A' diag(beta rk^2) [i][j]
+    // (bf16), B = kM^T tile [c][j] ([n][k] order)
     uint32_t ah[4];
     {
       const float2 f0 = ld2(&S.Aw[g][q2]), f1 = ld2(&S.Aw[g + 8][q2]);
@@ -480,8 +498,11 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
         float wacc[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816(wacc, ah, bk[2 * half], bk[2 * half + 1]);
         const int c = n0 + half * 8 + q2;
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + g, c)) = pack_bf16(wacc[0], wacc[1]);
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + g, c)) = pack_bf16(wacc[2], wacc[3]);
+        const float2 mc = *reinterpret_cast<const float2*>(&S.pm[c]);
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + g, c)) =
+            pack_bf16(wacc[0] * mc.x, wacc[1] * mc.y);
+        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + g, c)) =
+            pack_bf16(wacc[2] * mc.x, wacc[3] * mc.y);
       }
     }
     // U'^T [c][i] = V^T (A' diag(beta rk))^T: A = V^T from the raw v tile
