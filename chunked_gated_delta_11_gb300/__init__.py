@@ -23,6 +23,7 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
+    "kda_selftest_timeout",
     "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc",
     "kda_fwd_segmented", "kda_segments_auto", "kda_segmented_workspace_size",
     "kda_validate_cu_seqlens", "REC_BYTES", "CHUNK", "HEAD_DIM",
@@ -100,6 +101,8 @@ def load(build_if_missing: bool = False):
         lib.kda_segments_auto.restype = i32
         lib.kda_validate_cu_seqlens.argtypes = [P, i32, i64, P]
         lib.kda_validate_cu_seqlens.restype = ctypes.c_int
+        lib.kda_selftest_timeout.argtypes = [i64, P]
+        lib.kda_selftest_timeout.restype = ctypes.c_int
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]
         lib.kda_selftest_tcgen05.restype = ctypes.c_int
         _lib = lib
@@ -383,6 +386,13 @@ def kda_validate_cu_seqlens(cu_seqlens, T_total: int, stream=None):
 def kda_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the device error word: 0 or a status."""
     return int(load().kda_device_status(_stream(stream)))
+
+
+def kda_selftest_timeout(limit_cycles: int = 100_000, stream=None):
+    """Queue the diagnostic whose bounded wait runs out after `limit_cycles`
+    SM cycles; kda_device_status() then reports KDA_ERR_TIMEOUT (5) once."""
+    _check(load().kda_selftest_timeout(int(limit_cycles), _stream(stream)),
+           "kda_selftest_timeout")
 
 
 def kda_selftest_tcgen05(device="cuda"):

@@ -29,6 +29,7 @@ cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
                              cudaStream_t stream);
+cudaError_t launch_selftest_timeout(long long limit, int* err, cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* g,
                           const void* beta_raw, float scale, float lower_bound, float eps,
                           const void* init, const int32_t* cu, int64_t T_total, int H, int N,
@@ -465,6 +466,17 @@ extern "C" kda_status kda_validate_cu_seqlens(const int32_t* cu_seqlens, int32_t
   validate_cu_kernel<<<static_cast<unsigned>(blocks < 1024 ? blocks : 1024), threads, 0,
                        static_cast<cudaStream_t>(stream)>>>(cu_seqlens, N, T_total, info.err);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_selftest_timeout(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles) return KDA_ERR_INVALID_ARG;
+  DeviceInfo info;
+  const kda_status s = device_info(info);
+  if (s != KDA_OK) return s;
+  return launch_selftest_timeout(limit_cycles, info.err, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_LAUNCH;
 }
 
 extern "C" const char* kda_status_string(kda_status status) {

@@ -12,7 +12,7 @@
 //
 // Every smem address the descriptors can form stays inside the 17 KB record
 // area, so a wrong convention gives wrong numbers only.
-#include "kda_common.cuh"
+#include "kda_state.cuh"
 
 namespace kda {
 
@@ -121,6 +121,40 @@ selftest_tcgen05_kernel(float* __restrict__ out1, float* __restrict__ out2,
   tc_fence_before();
   __syncthreads();
   if (w == 0) tmem_dealloc(tbase, 512);
+}
+
+// The timeout path of the bounded waits, exercised on purpose: one CTA of 128
+// threads holds tensor memory, as the state threads of the forward kernels do,
+// and waits with wait_or_abort on an mbarrier that nothing arrives at.  Each
+// wait gives up after `limit` cycles, sets the CTA's abort flag and the device
+// error word; the CTA agrees to stop through the same barrier reduction the
+// recurrence uses (state_all), frees its tensor memory and exits.
+__global__ void __launch_bounds__(128, 1) selftest_timeout_kernel(long long limit, int* err) {
+  __shared__ StateCtl<1> ctl;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    mbar_init(&ctl.full[0], 1);  // one arrival expected, none ever made
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (t < 32) {
+    tmem_alloc(&ctl.tmem, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const bool ok = wait_or_abort(&ctl.full[0], 0, &ctl, err, limit);
+  const bool all_ok = state_all(ok);  // false: every thread leaves together
+  (void)all_ok;
+  tc_fence_before();
+  __syncthreads();
+  if (t < 32) tmem_dealloc(ctl.tmem, 32);
+}
+
+cudaError_t launch_selftest_timeout(long long limit, int* err, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 128, 0, stream>>>(limit, err);
+  return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -48,13 +48,18 @@ struct StateCtl {
   int abort;
 };
 
+// Wait for phase `parity` of `bar`; false if the CTA's abort flag is set or if
+// `limit` cycles pass first, in which case this thread sets the abort flag and
+// the error word (KDA_ERR_TIMEOUT).  The kernels use the default limit
+// (about a second); kda_selftest_timeout passes a short one.
 template <class Ctl>
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl, int* err) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl, int* err,
+                                              long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (*reinterpret_cast<volatile int*>(&ctl->abort)) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
       atomicExch(err, 5);
       return false;

@@ -41,7 +41,10 @@
  * stream); nothing synchronises inside.  Argument errors are reported before
  * anything is launched; errors found on the device (a bounded wait that ran
  * out) are latched in a device error word that kda_device_status() returns.
- * libkda keeps no state between calls other than that error word.
+ * libkda keeps two things between calls: that error word, and the fixed
+ * scratch array of kda_fwd_noalloc, which holds the last kda_fwd_noalloc
+ * call's chunk records (see the race note of kda_fwd_noalloc below).  The
+ * other entry points keep nothing.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -160,8 +163,9 @@ kda_status kda_forward(const kda_options* opts, const void* q, const void* k, co
  * memory and offers no allocator).  The pages have no counterpart to this
  * entry point; it exists for such callers only.
  * Same arguments and results as kda_fwd, minus the workspace: the K1->K2
- * records go to a fixed 64 MiB device array inside libkda, which every GPU that
- * loads the library's device code holds until the process exits.
+ * records go to a fixed 64 MiB device array inside libkda.  A GPU holds that
+ * array from the first kda_fwd_noalloc call on it (or from library load under
+ * eager module loading, CUDA_MODULE_LOADING=EAGER) until the process exits.
  * Limit: kda_workspace_size(T_total, H, N, D) must not exceed
  * KDA_NOALLOC_WORKSPACE_BYTES (e.g. T_total + 16 (N + 1) <= 1280 tokens at
  * H = 32, <= 41,008 at H = 1); larger sizes return KDA_ERR_WORKSPACE before
@@ -290,6 +294,17 @@ const char* kda_status_string(kda_status status);
  * launch error.  The expected values are closed-form small dyadic numbers
  * (see the kernel source), exact in fp32. */
 int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream);
+
+/* Diagnostic of the device-side timeout path (the failure detection of the
+ * bounded waits): one CTA holds tensor memory and waits on an mbarrier that
+ * nothing arrives at, with the forward kernels' wait routine but a limit of
+ * `limit_cycles` SM cycles (1 .. 2^31; the forward kernels use 2^31, about a
+ * second).  When the wait runs out the CTA latches KDA_ERR_TIMEOUT in the
+ * device error word, frees its tensor memory and exits, exactly as a forward
+ * kernel does; kda_device_status() then returns KDA_ERR_TIMEOUT once and clears
+ * it.  Asynchronous on `stream`.  Returns KDA_ERR_INVALID_ARG for a limit
+ * outside that range and KDA_ERR_LAUNCH if the launch fails. */
+kda_status kda_selftest_timeout(int64_t limit_cycles, void* stream);
 
 #ifdef __cplusplus
 }

@@ -209,3 +209,28 @@ def test_state_updated_in_place(schedule):
     assert fs.data_ptr() == state.data_ptr()
     assert_close(f64(out), ro, f"{schedule} out (state in place)")
     assert_close(f64(state), rs, f"{schedule} final_state (in place)")
+
+
+def test_bounded_wait_timeout_is_reported_and_recovers():
+    # the failure-detection path of every device wait, made to run out on purpose:
+    # a CTA waits on an mbarrier nothing arrives at, with a 1e5-cycle limit
+    assert kda.kda_device_status() == 0
+    kda.kda_selftest_timeout(100_000)
+    assert kda.kda_device_status() == 5          # KDA_ERR_TIMEOUT, latched once
+    assert kda.kda_device_status() == 0          # and cleared by the read
+    # the context is intact: the next forward pass is correct
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[70, 33], seed=91, init_std=0.02))
+    out, fs = kda.kda_fwd_fused(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                                inp["scale"], inp["lower_bound"], inp["initial_state"],
+                                inp["cu_seqlens"], N=inp["N"])
+    assert kda.kda_device_status() == 0
+    ro, rs = oracle_case(inp)
+    assert_close(f64(out), ro, "out after a timeout")
+    assert_close(f64(fs), rs, "final_state after a timeout")
+
+
+def test_timeout_limit_is_checked_on_the_host():
+    for bad in (0, -1, (1 << 31) + 1):
+        with pytest.raises(kda.KdaError) as e:
+            kda.kda_selftest_timeout(bad)
+        assert e.value.status == 1
