@@ -35,7 +35,8 @@ def sources():
 
 
 def _deps():
-    deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
+    deps = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                        if f.endswith((".cuh", ".h"))]
     deps.append(os.path.join(INCLUDE, "kda.h"))
     deps.append(os.path.abspath(__file__))
     return deps

@@ -42,6 +42,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "kda_bounds.h"
+
 namespace kda {
 
 constexpr int kChunk = 16;
@@ -389,13 +391,16 @@ __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
 // ---------------------------------------------------------------------------
 // sequence geometry.  Chunk records of sequence n live at record slots
 // slot0(n) .. slot0(n) + nchunks(n) - 1 with slot0(n) = floor(bos_n / 16) + n,
-// which never overlap and stay below T_total / 16 + N + 1.
+// which never overlap and stay below T_total / 16 + N + 1.  The bounds read
+// from cu_seqlens are clamped (kda_bounds.h): a malformed cu_seqlens gives
+// wrong results (and kda_validate_cu_seqlens reports it) but every access stays
+// inside the tensors and the workspace, since the last slot of a sequence is
+// below eos / 16 + n + 1 for any 0 <= bos <= eos <= T_total.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void seq_bounds(const int32_t* cu, int64_t T_total, int N, int n,
                                            int64_t& bos, int64_t& eos) {
   if (cu) {
-    bos = __ldg(cu + n);
-    eos = __ldg(cu + n + 1);
+    clamp_seq_bounds(__ldg(cu + n), __ldg(cu + n + 1), T_total, bos, eos);
   } else {
     const int64_t L = T_total / N;
     bos = static_cast<int64_t>(n) * L;
