@@ -10,8 +10,11 @@
 // takes it from g_noalloc_ws instead.
 //
 // Cost of the array: KDA_NOALLOC_WORKSPACE_BYTES (64 MiB) of device memory on
-// every GPU where the library's device code is loaded, held until the process
-// exits.
+// each GPU that uses it, from the first kda_fwd_noalloc call on that device
+// (or from library load, under eager module loading) until the process
+// exits.  Under CUDA's default lazy module loading the module that holds the
+// array is loaded, and the memory taken, when the first call looks up its
+// address.
 #include <mutex>
 
 #include "kda.h"

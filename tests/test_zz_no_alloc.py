@@ -38,6 +38,29 @@ def test_noalloc_matches_kda_fwd_on_two_calls():
         assert_close(f64(fs), f64(ref_fs), "noalloc final_state")
 
 
+def test_noalloc_at_its_size_limit():
+    # H = 32, N = 1: T_total = 1248 needs 80 record slots x 32 heads x 26176 B,
+    # just under the 64 MiB array; T_total = 1264 needs 81 slots, just over
+    H = 32
+    assert kda.kda_workspace_size(1248, H, 1) <= kda.NOALLOC_WORKSPACE_BYTES
+    assert kda.kda_workspace_size(1264, H, 1) > kda.NOALLOC_WORKSPACE_BYTES
+    inp = _dev(synth.make_inputs(1248, H, 1, seed=23, init_std=0.02))
+    ref_out, ref_fs = kda.kda_fwd(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                                  inp["scale"], inp["lower_bound"], inp["initial_state"], N=1)
+    out = torch.full_like(ref_out, float("nan"))
+    fs = torch.full_like(ref_fs, float("nan"))
+    kda.kda_fwd_noalloc(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"],
+                        inp["scale"], inp["lower_bound"], out, fs, inp["initial_state"], N=1)
+    assert kda.kda_device_status() == 0
+    assert_close(f64(out), f64(ref_out), "noalloc out at the limit")
+    assert_close(f64(fs), f64(ref_fs), "noalloc final_state at the limit")
+    x = torch.zeros((1264, H, 128), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((1264, H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_fwd_noalloc(x, x, x, x, b, 0.1, -5.0, torch.empty_like(x))
+    assert e.value.status == 3
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
     kda.load()
     T, H = 4096, 32   # needs (4096/16 + 2) slots x 32 heads x 26176 B > 64 MiB
