@@ -247,8 +247,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed loops of --steps steps each; the line reports their median")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="b8")
     ap.add_argument("--path", choices=["fused", "split", "decode", "segmented"], default=None,
@@ -312,19 +314,23 @@ def main():
         step()
     torch.cuda.synchronize()
     assert kda.kda_device_status() == 0
-    barrier(world)
     sampler = ClockSampler(local)
     sampler.start()
-    torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    rep_ms = []
+    for _ in range(max(1, args.repeats)):
+        # each repeat: exactly --steps steps between a barrier + synchronize on both sides
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        rep_ms.append(max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world))
     clocks = sampler.stop()
-    barrier(world)
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    ms = statistics.median(rep_ms)
     assert kda.kda_device_status() == 0
 
     # the other path, and the split path's per-kernel durations, on the same stream
@@ -361,11 +367,17 @@ def main():
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = out_h.numel() * out_h.element_size() + fs_h.numel() * fs_h.element_size()
 
+    ws_host = torch.empty(kda.kda_fwd_host_workspace_size(T, H, N, host["cu_seqlens"],
+                                                          schedule=args.path),
+                          dtype=torch.uint8, device="cuda")
+
     def e2e_step():
+        # kda_fwd_host through the C ABI: host buffers in, copies and passes
+        # pipelined inside libkda, host buffers out
         kda.kda_forward_host(host["q"], host["k"], host["v"], host["g_raw"], host["beta_raw"],
                              inp["scale"], inp["lower_bound"], host["initial_state"],
                              host["cu_seqlens"], N=N, out=out_h, final_state=fs_h, stream=stream,
-                             schedule=args.path)
+                             schedule=args.path, workspace=ws_host)
 
     e2e_ms = None
     if args.e2e_steps > 0:
@@ -393,6 +405,8 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "repeats": {"n": len(rep_ms), "ms_per_step": rep_ms, "median": ms, "min": min(rep_ms),
+                    "max": max(rep_ms), "spread": (max(rep_ms) - min(rep_ms)) / ms},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {
@@ -425,8 +439,9 @@ def main():
         "clocks": clocks,
         "e2e": None if e2e_ms is None else {
             "value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s",
-            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": PATH_LAUNCHES[args.path] * args.steps,
+            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "kda_fwd_host (C ABI, pinned host buffers)", "copies_declared": True},
+        "gpu_launches": PATH_LAUNCHES[args.path] * args.steps * len(rep_ms),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1

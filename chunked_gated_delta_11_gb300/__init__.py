@@ -23,7 +23,7 @@ from .build import build as _build
 __all__ = [
     "KdaError", "load", "kda_workspace_size", "kda_fwd", "kda_chunk_prep",
     "kda_chunk_recurrence", "kda_device_status", "kda_status_string", "kda_selftest_tcgen05",
-    "kda_selftest_timeout",
+    "kda_selftest_timeout", "kda_fwd_host_workspace_size",
     "kda_forward_host", "kda_fwd_fused", "kda_decode", "kda_forward", "kda_fwd_noalloc",
     "kda_fwd_segmented", "kda_segments_auto", "kda_segmented_workspace_size",
     "kda_validate_cu_seqlens", "REC_BYTES", "CHUNK", "HEAD_DIM",
@@ -101,6 +101,11 @@ def load(build_if_missing: bool = False):
         lib.kda_segments_auto.restype = i32
         lib.kda_validate_cu_seqlens.argtypes = [P, i32, i64, P]
         lib.kda_validate_cu_seqlens.restype = ctypes.c_int
+        lib.kda_fwd_host.argtypes = [P, P, P, P, P, P, f32, f32, P, P, i64, i32, i32, i32, P, P,
+                                     i32, P, sz, P]
+        lib.kda_fwd_host.restype = ctypes.c_int
+        lib.kda_fwd_host_workspace_size.argtypes = [P, i64, i32, i32, i32, P, i32]
+        lib.kda_fwd_host_workspace_size.restype = sz
         lib.kda_selftest_timeout.argtypes = [i64, P]
         lib.kda_selftest_timeout.restype = ctypes.c_int
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]
@@ -406,181 +411,72 @@ def kda_selftest_tcgen05(device="cuda"):
     return out1, out2, int(status.item())
 
 
-def _host_workspace(schedule, T, H, N, device):
-    """Workspace of a split or segmented pass from torch's caching allocator
-    (reused across calls), or None for the schedules that need none."""
-    nbytes = {"split": lambda: kda_workspace_size(T, H, N),
-              "segmented": lambda: kda_segmented_workspace_size(T, H, N)}.get(schedule,
-                                                                            lambda: 0)()
-    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+def kda_fwd_host_workspace_size(T_total: int, H: int, N: int, cu_seqlens=None,
+                                schedule: str = "fused", state_bf16: bool = False,
+                                per_head_gate: bool = False, groups: int = 8) -> int:
+    """Device workspace bytes of kda_fwd_host (cu_seqlens: host int32 tensor or None)."""
+    opts = _Options(SCHEDULES[schedule], 1 if state_bf16 else 0, 1 if per_head_gate else 0)
+    return int(load().kda_fwd_host_workspace_size(ctypes.byref(opts), int(T_total), int(H),
+                                                  int(N), HEAD_DIM, _hptr(cu_seqlens),
+                                                  int(groups)))
 
 
-def _forward_host_sliced(fwd, schedule, q, k, v, g_raw, beta_raw, scale, lower_bound,
-                         initial_state, N, device, out, final_state, stream, slices):
-    """kda_forward_host for N equal sequences: every sequence is cut in time
-    into `slices` chunk-aligned slices.  Slice g of all sequences goes
-    host->device (one copy per sequence and tensor, into a slice-major device
-    layout), runs as one pass over all (sequence, head) units starting from the
-    state the previous slice left (updated in place), and goes back while later
-    slices are copied in."""
-    T_total, H, D = q.shape
-    L = T_total // N
-    chunks = (L + CHUNK - 1) // CHUNK
-    G = max(1, min(int(slices), chunks))
-    cuts = [min(L, CHUNK * ((chunks * g) // G)) for g in range(G)] + [L]
-    ins = (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw))
-    dev = {name: torch.empty(t.shape, dtype=t.dtype, device=device) for name, t in ins}
-    out_d = torch.empty((T_total, H, D), dtype=torch.bfloat16, device=device)
-    state_d = torch.empty((N, H, D, D), dtype=torch.float32, device=device)
-    copy_in, copy_out, work = (torch.cuda.Stream(device), torch.cuda.Stream(device),
-                               torch.cuda.Stream(device))
-    start = torch.cuda.Event()
-    start.record(stream)
-    for st in (copy_in, copy_out, work):
-        st.wait_event(start)
-    if initial_state is not None:
-        with torch.cuda.stream(copy_in):
-            state_d.copy_(initial_state, non_blocking=True)
-    ws = None
-    with torch.cuda.stream(work):
-        ws = _host_workspace(schedule, N * max(b - a for a, b in zip(cuts, cuts[1:])), H, N,
-                             device)
-    started = initial_state is not None
-    for a, b in zip(cuts, cuts[1:]):
-        n = b - a
-        if n == 0:
-            continue
-        base = N * a
-        with torch.cuda.stream(copy_in):
-            for name, t in ins:
-                dst = dev[name]
-                for s in range(N):
-                    dst[base + s * n:base + (s + 1) * n].copy_(t[s * L + a:s * L + b],
-                                                               non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(copy_in)
-        work.wait_event(arrived)
-        with torch.cuda.stream(work):
-            sl = slice(base, base + N * n)
-            extra = {} if ws is None else {"workspace": ws}
-            fwd(dev["q"][sl], dev["k"][sl], dev["v"][sl], dev["g_raw"][sl], dev["beta_raw"][sl],
-                scale, lower_bound, state_d if started else None, None, N=N, out=out_d[sl],
-                final_state=state_d, stream=work, **extra)
-            done = torch.cuda.Event()
-            done.record(work)
-        started = True
-        copy_out.wait_event(done)
-        with torch.cuda.stream(copy_out):
-            for s in range(N):
-                out[s * L + a:s * L + b].copy_(out_d[base + s * n:base + (s + 1) * n],
-                                               non_blocking=True)
-    if not started:  # no tokens: the final state is the initial one (zeros here)
-        with torch.cuda.stream(work):
-            state_d.zero_()
-            done = torch.cuda.Event()
-            done.record(work)
-        copy_out.wait_event(done)
-    with torch.cuda.stream(copy_out):
-        final_state.copy_(state_d, non_blocking=True)
-    finished = torch.cuda.Event()
-    finished.record(copy_out)
-    stream.wait_event(finished)
-    for t in list(dev.values()) + [out_d, state_d] + ([ws] if ws is not None else []):
-        for st in (copy_in, copy_out, work):
-            t.record_stream(st)
-    return out, final_state
+def _hptr(t):
+    if t is None:
+        return None
+    if t.device.type != "cpu":
+        raise ValueError("kda_forward_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError("host tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def kda_forward_host(q, k, v, g_raw, beta_raw, scale, lower_bound, initial_state=None,
                      cu_seqlens=None, N=None, device="cuda", out=None, final_state=None,
-                     stream=None, schedule="fused", groups=8):
-    """Forward pass on host (CPU, ideally pinned) tensors; returns (out, final_state)
-    as host tensors (allocated pinned if not given), ready once `stream` is.
-
-    The pass (`schedule`: "fused" = kda_fwd_fused, "split" = kda_fwd,
-    "decode" = kda_decode, "segmented" = kda_fwd_segmented) overlaps the copies:
-    - the sequences are split into up to `groups` contiguous groups, each run
-      on a stream of its own once its inputs have arrived;
-    - fewer than `groups` equal sequences (no cu_seqlens) are instead cut in
-      time into up to `groups` chunk-aligned slices; slice p runs over all
-      sequences once its inputs have arrived, from the state slice p - 1 left.
-    Inputs go host->device on one copy stream and outputs device->host on
-    another, overlapping the remaining input copies (the link carries both
-    directions at once).  `stream` (default: the current stream) orders the
-    whole call: nothing starts before work already queued on it, and it waits
-    for the last copy."""
-    stream = torch.cuda.current_stream(device) if stream is None else stream
-    fwd = {"fused": kda_fwd_fused, "split": kda_fwd, "decode": kda_decode,
-           "segmented": kda_fwd_segmented}[schedule]
-    T_total, H, D, N = _geometry(q, None, N) if cu_seqlens is None else (
-        q.shape[0], q.shape[1], q.shape[2], cu_seqlens.shape[0] - 1)
-    if cu_seqlens is None and T_total % max(N, 1):
-        raise ValueError("T_total must be a multiple of N without cu_seqlens")
+                     stream=None, schedule="fused", groups=8, workspace=None):
+    """Forward pass on host (CPU, ideally pinned) tensors through kda_fwd_host:
+    libkda copies the inputs in, runs the pass and copies the outputs back in a
+    pipeline of `groups` pieces (groups of whole sequences, or chunk-aligned
+    time slices of few equal sequences).  Returns (out, final_state) as host
+    tensors (allocated pinned if not given), complete once `stream` (default:
+    the current stream of `device`) is.  The device workspace comes from
+    torch's caching allocator on that stream unless `workspace` is given."""
+    dev = torch.device(device)
+    stream = torch.cuda.current_stream(dev) if stream is None else stream
+    T_total, H, D = q.shape
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        N = cu_seqlens.shape[0] - 1
+    elif N is None:
+        N = 1
+    per_head = g_raw.dim() == 2
+    sdt = initial_state.dtype if initial_state is not None else (
+        final_state.dtype if final_state is not None else torch.float32)
+    if sdt not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"states must be float32 or bfloat16, got {sdt}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
     if out is None:
         out = torch.empty((T_total, H, D), dtype=torch.bfloat16, pin_memory=True)
     if final_state is None:
-        final_state = torch.empty((N, H, D, D), dtype=torch.float32, pin_memory=True)
-    if cu_seqlens is None and N < groups:
-        # too few sequences to form the groups: slices in time
-        return _forward_host_sliced(fwd, schedule, q, k, v, g_raw, beta_raw, scale, lower_bound,
-                                    initial_state, N, device, out, final_state, stream, groups)
-    if cu_seqlens is None:
-        bounds = [n * (T_total // N) for n in range(N + 1)]
-    else:
-        bounds = [int(x) for x in cu_seqlens.tolist()]
-    dev = {name: torch.empty(t.shape, dtype=t.dtype, device=device)
-           for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw))}
-    init_d = None if initial_state is None else torch.empty(initial_state.shape,
-                                                            dtype=initial_state.dtype,
-                                                            device=device)
-    out_d = torch.empty((T_total, H, D), dtype=torch.bfloat16, device=device)
-    fs_d = torch.empty((N, H, D, D), dtype=torch.float32, device=device)
-    G = max(1, min(int(groups), N))
-    edges = [round(i * N / G) for i in range(G + 1)]
-    copy_in, copy_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    work = [torch.cuda.Stream(device) for _ in range(G)]
-    start = torch.cuda.Event()
-    start.record(stream)
-    copy_in.wait_event(start)
-    copy_out.wait_event(start)
-    for gi in range(G):
-        n0, n1 = edges[gi], edges[gi + 1]
-        t0, t1 = bounds[n0], bounds[n1]
-        with torch.cuda.stream(copy_in):
-            for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw)):
-                dev[name][t0:t1].copy_(t[t0:t1], non_blocking=True)
-            if init_d is not None:
-                init_d[n0:n1].copy_(initial_state[n0:n1], non_blocking=True)
-            cu_g = None
-            if cu_seqlens is not None:
-                cu_g = torch.tensor([b - t0 for b in bounds[n0:n1 + 1]], dtype=torch.int32,
-                                    pin_memory=True).to(device, non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(copy_in)
-        work[gi].wait_event(arrived)
-        with torch.cuda.stream(work[gi]):
-            if cu_g is not None:
-                cu_g.record_stream(work[gi])
-            # the split and segmented schedules get their workspace from torch's
-            # caching allocator (reused across calls) rather than the library's
-            # per-call stream-ordered allocation
-            ws = _host_workspace(schedule, t1 - t0, H, n1 - n0, device)
-            extra = {} if ws is None else {"workspace": ws}
-            fwd(dev["q"][t0:t1], dev["k"][t0:t1], dev["v"][t0:t1], dev["g_raw"][t0:t1],
-                dev["beta_raw"][t0:t1], scale, lower_bound,
-                None if init_d is None else init_d[n0:n1], cu_g, N=n1 - n0,
-                out=out_d[t0:t1], final_state=fs_d[n0:n1], stream=work[gi], **extra)
-            done = torch.cuda.Event()
-            done.record(work[gi])
-        copy_out.wait_event(done)
-        with torch.cuda.stream(copy_out):
-            out[t0:t1].copy_(out_d[t0:t1], non_blocking=True)
-            final_state[n0:n1].copy_(fs_d[n0:n1], non_blocking=True)
-    finished = torch.cuda.Event()
-    finished.record(copy_out)
-    stream.wait_event(finished)
-    # the device buffers stay alive until the streams that use them are done
-    for t in list(dev.values()) + [out_d, fs_d] + ([init_d] if init_d is not None else []):
-        for st in [copy_in, copy_out] + work:
-            t.record_stream(st)
+        final_state = torch.empty((N, H, D, D), dtype=sdt, pin_memory=True)
+    opts = _Options(SCHEDULES[schedule], 1 if sdt == torch.bfloat16 else 0, 1 if per_head else 0)
+    cu = None if cu_seqlens is None else cu_seqlens.cpu().contiguous()
+    nbytes = int(load().kda_fwd_host_workspace_size(ctypes.byref(opts), T_total, H, N, D,
+                                                    _hptr(cu), int(groups)))
+    if nbytes == 0:
+        raise KdaError(1, "kda_fwd_host_workspace_size")
+    if workspace is None:
+        with torch.cuda.stream(stream):
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8)
+    with torch.cuda.device(dev):
+        st = load().kda_fwd_host(ctypes.byref(opts), _hptr(q), _hptr(k), _hptr(v), _hptr(g_raw),
+                                 _hptr(beta_raw), float(scale), float(lower_bound),
+                                 _hptr(initial_state), _hptr(cu), T_total, H, N, D, _hptr(out),
+                                 _hptr(final_state), int(groups), _ptr(workspace),
+                                 workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    _check(st, "kda_fwd_host")
     return out, final_state

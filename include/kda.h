@@ -155,6 +155,44 @@ kda_status kda_forward(const kda_options* opts, const void* q, const void* k, co
                        int32_t H, int32_t N, int32_t D, void* out, void* final_state,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* The forward pass on HOST buffers: q, k, v, g_raw, beta_raw, initial_state,
+ * cu_seqlens, out and final_state are host pointers (pinned memory lets the
+ * copies overlap; pageable memory works, with copies that stage through the
+ * driver).  Layouts, options and results are those of kda_forward; cu_seqlens
+ * is a host int32 [N + 1], checked here (0 first, non-decreasing, T_total
+ * last; otherwise KDA_ERR_INVALID_ARG before anything is queued).
+ * The call pipelines the host-to-device copies, the passes and the
+ * device-to-host copies in `groups` pieces (1 .. 16; 0 = 8):
+ *   - G groups of whole sequences, each copied in, run (one kda_forward over
+ *     its own sequences) and copied out on streams of its own;
+ *   - for N equal sequences without cu_seqlens, fewer than `groups` of them,
+ *     and fp32 states: each sequence cut in time into up to G chunk-aligned
+ *     slices; slice p of all sequences runs once its rows have arrived,
+ *     starting from the fp32 state slice p - 1 left in device memory (exact:
+ *     the recurrence is a left-to-right scan).
+ * Every copy is one cudaMemcpyAsync (or one cudaMemcpy2DAsync for the rows of
+ * all N sequences of a slice) on library-owned copy streams, ordered after
+ * the work already queued on `stream`; `stream` waits for the last copy, so
+ * the host outputs are complete once `stream` is.  The host inputs must stay
+ * unchanged, and the outputs untouched, until then.
+ * workspace: device memory of kda_fwd_host_workspace_size() bytes, 256-byte
+ * aligned (the inputs, outputs, states and each piece's kda_forward
+ * workspace), or NULL (= cudaMallocAsync / cudaFreeAsync on `stream`).
+ * Concurrent calls are serialised while they queue their work.
+ * Errors: those of kda_forward; KDA_ERR_WORKSPACE for a small or misaligned
+ * workspace; KDA_ERR_LAUNCH if a copy or launch fails. */
+kda_status kda_fwd_host(const kda_options* opts, const void* q, const void* k, const void* v,
+                        const void* g_raw, const void* beta_raw, float scale, float lower_bound,
+                        const void* initial_state, const int32_t* cu_seqlens, int64_t T_total,
+                        int32_t H, int32_t N, int32_t D, void* out, void* final_state,
+                        int32_t groups, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes of kda_fwd_host for these arguments (cu_seqlens is
+ * the host array, or NULL); 0 for invalid arguments. */
+size_t kda_fwd_host_workspace_size(const kda_options* opts, int64_t T_total, int32_t H,
+                                   int32_t N, int32_t D, const int32_t* cu_seqlens,
+                                   int32_t groups);
+
 /* Size of the fixed workspace array used by kda_fwd_noalloc (64 MiB). */
 #define KDA_NOALLOC_WORKSPACE_BYTES (64 * 1024 * 1024)
 

@@ -151,3 +151,44 @@ def test_validate_cu_seqlens_rejects_bad_arguments(lib):
     assert lib.kda_validate_cu_seqlens(P(FAKE), 0, 10, None) == 1        # no sequences
     assert lib.kda_validate_cu_seqlens(P(FAKE + 2), 2, 10, None) == 1    # misaligned
     assert lib.kda_validate_cu_seqlens(P(FAKE), 2, 1 << 31, None) == 1   # int32 range
+
+
+def _host_call(lib, cu=None, T=64, H=1, N=1, groups=0, lb=-5.0, schedule=1, sd=0, gate=0, ws=None,
+               ws_bytes=0):
+    P = ctypes.c_void_p
+    opts = kda._Options(schedule, sd, gate)
+    buf = (ctypes.c_uint8 * 64)()
+    hp = ctypes.cast(buf, P)
+    cu_arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
+    return lib.kda_fwd_host(ctypes.byref(opts), hp, hp, hp, hp, hp, 0.1, lb, None, cu_arr, T, H, N,
+                            128, hp, None, groups, P(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cu=[0, 5, 3, 64], N=3), 1),        # decreasing host cu_seqlens
+    (dict(cu=[1, 64], N=1), 1),              # does not start at 0
+    (dict(cu=[0, 60], N=1), 1),              # does not end at T_total
+    (dict(groups=17), 1),                    # more pieces than the pipeline has streams
+    (dict(groups=-1), 1),
+    (dict(schedule=9), 1),
+    (dict(sd=3), 1),
+    (dict(lb=0.5), 2),
+    (dict(T=63, N=2), 1),                    # T_total not a multiple of N without cu_seqlens
+    (dict(ws=FAKE + 16, ws_bytes=1 << 30), 3),  # workspace not 256-byte aligned
+])
+def test_fwd_host_rejects_bad_arguments_on_the_host(lib, kw, status):
+    # all of these are found before any CUDA call (no GPU needed)
+    assert _host_call(lib, **kw) == status
+
+
+def test_fwd_host_workspace_size_is_the_device_layout(lib):
+    opts = kda._Options(1, 0, 0)
+    r = lambda x: (x + 255) // 256 * 256
+    T, H, N = 64, 2, 2
+    rows = T * H
+    state = N * H * 128 * 128 * 4
+    cu_words = N + 2          # the groups' rebased cu_seqlens: 2 groups of 1 sequence
+    want = (4 * r(rows * 256) + r(rows * 2) + r(rows * 256) + 2 * r(state) + r(cu_words * 4 + 4))
+    got = lib.kda_fwd_host_workspace_size(ctypes.byref(opts), T, H, N, 128, None, 2)
+    assert got == want
+    assert lib.kda_fwd_host_workspace_size(ctypes.byref(opts), T, H, N, 64, None, 2) == 0
