@@ -439,7 +439,8 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
 
   // ---- A' = (I + R')^-1 by fp32 forward substitution in warp 0: lane j (and
   // j + 16, which repeats it) carries column j; after column m of R' has been
-  // applied, entry m is final.  Writes A' diag(beta rk^2) and A' diag(beta rk). ----
+  // applied, entry m is final.  Writes A' diag(beta rk^2) (lanes 0-15) and
+  // A' diag(beta rk) (lanes 16-31). ----
   if (w == 0) {
     const int j = l & 15;
     float x[16];
@@ -458,12 +459,13 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
     }
     const float rkj = S.rk[j];
     const float cu = S.beta[j] * rkj, cw = cu * rkj;
-    if (l < 16) {
+    // lanes 0-15 write column j of A' diag(beta rk^2), lanes 16-31 (which
+    // computed the same column) that of A' diag(beta rk)
+    {
+      float* dst = l < 16 ? &S.Aw[0][j] : &S.Au[0][j];
+      const float f = l < 16 ? cw : cu;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        S.Aw[i][j] = x[i] * cw;
-        S.Au[i][j] = x[i] * cu;
-      }
+      for (int i = 0; i < 16; ++i) dst[i * AS] = x[i] * f;
     }
   }
   // this chunk's v tile (the older of at most two pending groups)
