@@ -106,6 +106,9 @@ def load(build_if_missing: bool = False):
         lib.kda_fwd_host.restype = ctypes.c_int
         lib.kda_fwd_host_workspace_size.argtypes = [P, i64, i32, i32, i32, P, i32]
         lib.kda_fwd_host_workspace_size.restype = sz
+        lib.kda_profile_phases.argtypes = [i32, P, P, P, P, P, f32, f32, i64, i32, i32, i32, P,
+                                           P, P, sz, P, i32, P]
+        lib.kda_profile_phases.restype = ctypes.c_int
         lib.kda_selftest_timeout.argtypes = [i64, P]
         lib.kda_selftest_timeout.restype = ctypes.c_int
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]

@@ -30,6 +30,15 @@ cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg
                              const float* sstart, const void* y, void* out, int sm_count,
                              cudaStream_t stream);
 cudaError_t launch_selftest_timeout(long long limit, int* err, cudaStream_t stream);
+cudaError_t launch_recurrence_timed(const void* ws, const void* init, const int32_t* cu,
+                                    int64_t T_total, int H, int N, void* out, void* final_state,
+                                    FwdOpts opts, int* err, long long* stamps, int max_chunks,
+                                    cudaStream_t stream);
+cudaError_t launch_fused_timed(const void* q, const void* k, const void* v, const void* g,
+                               const void* beta_raw, float scale, float lower_bound, float eps,
+                               const int32_t* cu, int64_t T_total, int H, int N, void* out,
+                               void* final_state, int* err, long long* stamps, int max_chunks,
+                               cudaStream_t stream);
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* g,
                           const void* beta_raw, float scale, float lower_bound, float eps,
                           const void* init, const int32_t* cu, int64_t T_total, int H, int N,
@@ -477,6 +486,41 @@ extern "C" kda_status kda_selftest_timeout(int64_t limit_cycles, void* stream) {
                  cudaSuccess
              ? KDA_OK
              : KDA_ERR_LAUNCH;
+}
+
+extern "C" kda_status kda_profile_phases(int32_t kernel, const void* q, const void* k,
+                                         const void* v, const void* g_raw, const void* beta_raw,
+                                         float scale, float lower_bound, int64_t T_total,
+                                         int32_t H, int32_t N, int32_t D, void* out,
+                                         float* final_state, void* workspace,
+                                         size_t workspace_bytes, long long* stamps,
+                                         int32_t max_chunks, void* stream) {
+  if (kernel != 0 && kernel != 1) return KDA_ERR_INVALID_ARG;
+  kda_status s = check_sizes(T_total, H, N, D, nullptr);
+  if (s != KDA_OK) return s;
+  if ((s = check_inputs(q, k, v, g_raw, beta_raw, scale, lower_bound, T_total)) != KDA_OK) return s;
+  if ((s = check_outputs(out, nullptr, final_state, T_total)) != KDA_OK) return s;
+  if (!stamps || max_chunks < 0 || (reinterpret_cast<uintptr_t>(stamps) & 7u) != 0)
+    return KDA_ERR_INVALID_ARG;
+  DeviceInfo info;
+  if ((s = device_info(info)) != KDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (kernel == 1) {
+    e = launch_fused_timed(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, nullptr,
+                           T_total, H, N, out, final_state, info.err, stamps, max_chunks, st);
+  } else {
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < kda_workspace_size(T_total, H, N, D))
+      return KDA_ERR_WORKSPACE;
+    e = T_total > 0 ? launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
+                                        nullptr, T_total, H, N, workspace, 0, info.sm_count, st)
+                    : cudaSuccess;
+    if (e == cudaSuccess)
+      e = launch_recurrence_timed(workspace, nullptr, nullptr, T_total, H, N, out, final_state,
+                                  FwdOpts{0, 0}, info.err, stamps, max_chunks, st);
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 extern "C" const char* kda_status_string(kda_status status) {

@@ -120,6 +120,14 @@ __device__ __forceinline__ void ldsm_x2_t_at(uint32_t (&r)[2], uint32_t a) {
                : "=r"(r[0]), "=r"(r[1])
                : "r"(a));
 }
+// four 8 x 8 b16 tiles from mma fragments (lane l: row l / 4, elements
+// 2 (l % 4), + 1 of each) to 16-byte rows of shared memory; lane l gives the
+// address of row (l & 7) of tile l >> 3
+__device__ __forceinline__ void stsm_x4(void* p, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(p)),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -240,7 +248,10 @@ __device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
 //                whether it issued them.
 // Returns may_write().  With u_zero (v known to be zero) U' is zero and is
 // neither formed nor written; the reader must take it as zero.
-template <class MayWrite, class LoadV, class NextQKG>
+// kRecShared: `rec` is in shared memory (the fused kernel's ring), so W' goes
+// out through stmatrix, which addresses shared memory only; a global record
+// (K1) takes plain 4-byte stores.
+template <bool kRecShared, class MayWrite, class LoadV, class NextQKG>
 __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, uint8_t* vt,
                                                    bool newer_qkg, uint32_t beta_raw_bits,
                                                    int nc, float scale,
@@ -334,8 +345,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   {
     const float2 one = make_float2(1.f, 1.f);
     const float2 dl = hf ? __fmul2_rn(Ho, Hh) : __fmul2_rn(Hh, Ho);  // same product in both lanes
-    const float2 pre = hf ? Ho : one;  // prod over tokens before the half
-    float2 sfx = hf ? one : Ho;        // prod over the tokens after the one being processed
+    float2 sfx = hf ? one : Ho;  // prod over the tokens after the one being processed
     // midpoint m = P_7 (first half's product) and Q_7 = dlast / m (second half's):
     // P_i / m = Pl_i / Hh in the first half and Pl_i in the second
     const float2 h1 = hf ? Ho : Hh, h2 = hf ? Hh : Ho;
@@ -356,12 +366,11 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
         const int ii = 2 * m + o;
         const float2 Q = sfx;
         sfx = __fmul2_rn(sfx, a[ii]);
-        const float2 P = __fmul2_rn(pre, Pl[ii]);
         const float2 Pm = __fmul2_rn(Pl[ii], rel);  // P_i / m
         const float2 qv = bf2_at(raw + RAW_Q * RAW_TILE + roff(ii));
         const float2 kv = bf2_at(raw + RAW_K * RAW_TILE + roff(ii));
-        Qu[ii] = __fmul2_rn(qv, P);
         Qm[o] = __fmul2_rn(qv, Pm);
+        Qu[ii] = __fmul2_rn(Qm[o], h1);  // q P_i = (q P_i / m) m
         Kd[o] = __fmul2_rn(kv, Pm);
         const float2 Ke = __fmul2_rn(kv, Q);
         Ki[o] = __fmul2_rn(Ke, inv_q7);
@@ -493,18 +502,28 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
 #pragma unroll
     for (int pair = 0; pair < 2; ++pair) {
       const int n0 = w * 32 + pair * 16;
-      uint32_t bk[4];
+      uint32_t bk[4], wf[4];
       ldsm_x4(bk, S.kd + drv_off(n0 + (l & 7) + (mi >> 1) * 8, mi & 1));
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float wacc[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816(wacc, ah, bk[2 * half], bk[2 * half + 1]);
-        const int c = n0 + half * 8 + q2;
-        const float2 mc = *reinterpret_cast<const float2*>(&S.pm[c]);
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + g, c)) =
-            pack_bf16(wacc[0] * mc.x, wacc[1] * mc.y);
-        *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + g, c)) =
-            pack_bf16(wacc[2] * mc.x, wacc[3] * mc.y);
+        const float2 mc = *reinterpret_cast<const float2*>(&S.pm[n0 + half * 8 + q2]);
+        wf[2 * half] = pack_bf16(wacc[0] * mc.x, wacc[1] * mc.y);      // rows g
+        wf[2 * half + 1] = pack_bf16(wacc[2] * mc.x, wacc[3] * mc.y);  // rows g + 8
+      }
+      if constexpr (kRecShared) {
+        // the four 8 x 8 bf16 tiles (W' rows 0-7 / 8-15 x channels n0.. /
+        // n0+8..) in one stmatrix: lane l gives the address of row (l & 7) of
+        // tile l >> 3, a 16-byte piece of the swizzled [Qdec ; W'] tile
+        stsm_x4(rec + b1_offset(16 + (l & 7) + 8 * (mi & 1), n0 + 8 * (mi >> 1)), wf);
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c = n0 + half * 8 + q2;
+          *reinterpret_cast<uint32_t*>(rec + b1_offset(16 + g, c)) = wf[2 * half];
+          *reinterpret_cast<uint32_t*>(rec + b1_offset(24 + g, c)) = wf[2 * half + 1];
+        }
       }
     }
     // U'^T [c][i] = V^T (A' diag(beta rk))^T: A = V^T from the raw v tile

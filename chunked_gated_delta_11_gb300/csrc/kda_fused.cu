@@ -57,14 +57,16 @@ __device__ __forceinline__ bool chunk_all(bool pred) {
   return r != 0;
 }
 
-template <bool kGateScalar>
+// kTimed: the diagnostic instantiation of kda_profile_phases, in which thread
+// 0 of CTA 0 records the state side's phase stamps (state_rows).
+template <bool kGateScalar, bool kTimed>
 __global__ void __launch_bounds__(F_THREADS, 2)
 fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
              const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e, float eps,
              const void* init, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
              __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts, SegArgs seg,
-             int* __restrict__ err) {
+             int* __restrict__ err, long long* stamps, int max_chunks) {
   constexpr int NST = F_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -173,7 +175,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
         return true;
       };
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
-      if (!build_chunk_record(CS, rawbuf(c), vt, c + 1 < nchunks, bbits[0], nc, scale,
+      if (!build_chunk_record<true>(CS, rawbuf(c), vt, c + 1 < nchunks, bbits[0], nc, scale,
                               lb_log2e, eps, rec, tc, may_write, load_v, next_qkg, mrole))
         break;
       // every thread's record stores -> async proxy, then one arrival per warp
@@ -190,46 +192,50 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
     // a segmented launch writes every piece's final state to its fp32 workspace
     const bool final_bf16 = opts.state_bf16 && seg.P == 0;
-    state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, mrole ? seg.y : out,
-               state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
-                        state_base + static_cast<int64_t>(t) * kDim, final_bf16),
-               final_bf16, err, smem + F_OST_OFF, release, mrole);
+    // 16-column snapshot pieces: the state warps run under the 152-register cap
+    state_rows<NST, 16, kTimed>(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h,
+                            mrole ? seg.y : out,
+                            state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
+                                     state_base + static_cast<int64_t>(t) * kDim, final_bf16),
+                            final_bf16, err, smem + F_OST_OFF, release, mrole,
+                            blockIdx.x == 0 ? stamps : nullptr, max_chunks);
   }
   tc_fence_before();
   __syncthreads();
   if (w == 0) tmem_dealloc(tb, TM_COLS);
 }
 
-template <bool kGateScalar>
+template <bool kGateScalar, bool kTimed = false>
 cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const void* g,
                            const void* beta_raw, float scale, float lower_bound, float eps,
                            const void* init, const int32_t* cu, int64_t T_total, int H, int N,
                            void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, long long* stamps = nullptr, int max_chunks = 0) {
   // the register split above is only safe if every thread starts with F_REGS
   static std::atomic<uint64_t> checked{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   if (dev >= 64 || !(checked.load(std::memory_order_acquire) & (uint64_t{1} << dev))) {
     cudaFuncAttributes fa;
-    const cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<kGateScalar>);
+    const cudaError_t e = cudaFuncGetAttributes(&fa, fused_kernel<kGateScalar, kTimed>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != F_REGS) return cudaErrorInvalidConfiguration;
     if (dev < 64) checked.fetch_or(uint64_t{1} << dev, std::memory_order_release);
   }
   static std::atomic<uint64_t> smem_set{0};
-  if (const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fused_kernel<kGateScalar>),
+  if (const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fused_kernel<kGateScalar, kTimed>),
                                               F_SMEM, smem_set);
       e != cudaSuccess)
     return e;
   const int64_t units = static_cast<int64_t>(N) * H * (seg.P > 0 ? 2 : 1);
   if (units == 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  fused_kernel<kGateScalar><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
+  fused_kernel<kGateScalar, kTimed><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
       static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err);
+      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err,
+      stamps, max_chunks);
   return cudaGetLastError();
 }
 
@@ -243,6 +249,18 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
                                     T_total, H, N, out, final_state, opts, seg, err, stream)
              : launch_fused_t<false>(q, k, v, g, beta_raw, scale, lower_bound, eps, init, cu,
                                      T_total, H, N, out, final_state, opts, seg, err, stream);
+}
+
+// The diagnostic instantiation (per-channel gate, fp32 states, no segments).
+cudaError_t launch_fused_timed(const void* q, const void* k, const void* v, const void* g,
+                               const void* beta_raw, float scale, float lower_bound, float eps,
+                               const int32_t* cu, int64_t T_total, int H, int N, void* out,
+                               void* final_state, int* err, long long* stamps, int max_chunks,
+                               cudaStream_t stream) {
+  return launch_fused_t<false, true>(q, k, v, g, beta_raw, scale, lower_bound, eps, nullptr, cu,
+                                     T_total, H, N, out, final_state, FwdOpts{0, 0},
+                                     SegArgs{0, nullptr, nullptr}, err, stream, stamps,
+                                     max_chunks);
 }
 
 }  // namespace kda

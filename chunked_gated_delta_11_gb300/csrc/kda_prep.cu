@@ -62,7 +62,7 @@ chunk_prep_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   while (have) {
     bool have_next = false;
     uint32_t next_bits = 0u;
-    build_chunk_record(
+    build_chunk_record<false>(
         P.chunk, P.raw, P.vt, false, bbits, cur.nc, scale, lb_log2e, eps,
         ws + static_cast<int64_t>(cur.item) * REC_BYTES, t,
         [] {

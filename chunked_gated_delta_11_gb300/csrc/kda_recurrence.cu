@@ -18,11 +18,12 @@ constexpr int K2_CTL_OFF = K2_OST_OFF + 4096 + 256;  // output staging, then rq 
 constexpr int K2_SMEM = K2_CTL_OFF + static_cast<int>(sizeof(StateCtl<K2_NST>)) + 1024 + 64;
 static_assert(2 * (K2_SMEM + 1024) <= 228 * 1024, "recurrence kernel must fit two CTAs per SM");
 
+template <bool kTimed>
 __global__ void __launch_bounds__(K2_THREADS, 2)
 recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
                   const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
                   __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts,
-                  int* __restrict__ err) {
+                  int* __restrict__ err, long long* stamps, int max_chunks) {
   constexpr int NST = K2_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -86,9 +87,11 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
       ++issued;
     }
   };
-  state_rows(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
-             state_at(final_state, state_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
-             opts.state_bf16, err, smem + K2_OST_OFF, refill);
+  state_rows<NST, 32, kTimed>(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
+                          state_at(final_state, state_base + static_cast<int64_t>(t) * kDim,
+                                   opts.state_bf16),
+                          opts.state_bf16, err, smem + K2_OST_OFF, refill, false,
+                          blockIdx.x == 0 ? stamps : nullptr, max_chunks);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory
     for (int p = issued > NST ? issued - NST : 0; p < issued; ++p)
@@ -99,20 +102,39 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
   if (w == 0) tmem_dealloc(tb, TM_COLS);
 }
 
-cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
-                              int64_t T_total, int H, int N, void* out, void* final_state,
-                              FwdOpts opts, int* err, cudaStream_t stream) {
+template <bool kTimed>
+cudaError_t launch_recurrence_t(const void* ws, const void* init, const int32_t* cu,
+                                int64_t T_total, int H, int N, void* out, void* final_state,
+                                FwdOpts opts, int* err, long long* stamps, int max_chunks,
+                                cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
-  if (const cudaError_t e =
-          ensure_smem_limit(reinterpret_cast<const void*>(recurrence_kernel), K2_SMEM, smem_set);
+  if (const cudaError_t e = ensure_smem_limit(
+          reinterpret_cast<const void*>(recurrence_kernel<kTimed>), K2_SMEM, smem_set);
       e != cudaSuccess)
     return e;
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units == 0) return cudaSuccess;
-  recurrence_kernel<<<static_cast<unsigned>(units), K2_THREADS, K2_SMEM, stream>>>(
+  recurrence_kernel<kTimed><<<static_cast<unsigned>(units), K2_THREADS, K2_SMEM, stream>>>(
       static_cast<const uint8_t*>(ws), init, cu, T_total, H, N,
-      static_cast<__nv_bfloat16*>(out), final_state, opts, err);
+      static_cast<__nv_bfloat16*>(out), final_state, opts, err, stamps, max_chunks);
   return cudaGetLastError();
+}
+
+cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
+                              int64_t T_total, int H, int N, void* out, void* final_state,
+                              FwdOpts opts, int* err, cudaStream_t stream) {
+  return launch_recurrence_t<false>(ws, init, cu, T_total, H, N, out, final_state, opts, err,
+                                    nullptr, 0, stream);
+}
+
+// The diagnostic instantiation: thread 0 of CTA 0 records the phase stamps
+// of state_rows (kda_state.cuh) for its first max_chunks chunks.
+cudaError_t launch_recurrence_timed(const void* ws, const void* init, const int32_t* cu,
+                                    int64_t T_total, int H, int N, void* out, void* final_state,
+                                    FwdOpts opts, int* err, long long* stamps, int max_chunks,
+                                    cudaStream_t stream) {
+  return launch_recurrence_t<true>(ws, init, cu, T_total, H, N, out, final_state, opts, err,
+                                   stamps, max_chunks, stream);
 }
 
 }  // namespace kda

@@ -118,32 +118,47 @@ __device__ __forceinline__ void load_state(uint32_t tb, uint32_t lane_off, const
 }
 
 // Snapshot and forget: Sb = bf16(S), then S *= dlast (dlast of the next
-// chunk, fp32 [128] in shared memory).  Thread v's row, 32 columns at a time.
+// chunk, fp32 [128] in shared memory).  Thread v's row, kCols (32 or 16)
+// columns at a time: 16 keeps fewer values live (r, the bf16 pairs and the
+// dlast vectors of one piece), for state threads that run under a register
+// cap (the fused kernel's setmaxnreg split); 32 needs half the tensor-memory
+// round trips, for the recurrence kernel, which has registers to spare.
+template <int kCols>
 __device__ __forceinline__ void snapshot_and_decay(uint32_t tb, uint32_t lane_off,
                                                    const float* dlast) {
+  static_assert(kCols == 16 || kCols == 32, "piece width");
   const float4* dl4 = reinterpret_cast<const float4*>(dlast);
 #pragma unroll
-  for (int qd = 0; qd < 4; ++qd) {
-    uint32_t r[32], b[16];
-    tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+  for (int qd = 0; qd < 128 / kCols; ++qd) {
+    uint32_t r[kCols], b[kCols / 2];
+    if constexpr (kCols == 32)
+      tmem_ld32(tb + TM_S + lane_off + qd * 32, r);
+    else
+      tmem_ld16(tb + TM_S + lane_off + qd * 16, r);
     tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kCols / 2; ++i)
       b[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-    tmem_st16(tb + TM_SB + lane_off + qd * 16, b);
+    if constexpr (kCols == 32)
+      tmem_st16(tb + TM_SB + lane_off + qd * 16, b);
+    else
+      tmem_st8(tb + TM_SB + lane_off + qd * 8, b);
 #pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4) {
-      const float4 dv = dl4[qd * 8 + i4];
+    for (int i4 = 0; i4 < kCols / 4; ++i4) {
+      const float4 dv = dl4[qd * (kCols / 4) + i4];
       const float2 a = __fmul2_rn(make_float2(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1])),
                                   make_float2(dv.x, dv.y));
-      const float2 b = __fmul2_rn(make_float2(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3])),
+      const float2 c = __fmul2_rn(make_float2(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3])),
                                   make_float2(dv.z, dv.w));
       r[4 * i4 + 0] = __float_as_uint(a.x);
       r[4 * i4 + 1] = __float_as_uint(a.y);
-      r[4 * i4 + 2] = __float_as_uint(b.x);
-      r[4 * i4 + 3] = __float_as_uint(b.y);
+      r[4 * i4 + 2] = __float_as_uint(c.x);
+      r[4 * i4 + 3] = __float_as_uint(c.y);
     }
-    tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+    if constexpr (kCols == 32)
+      tmem_st32(tb + TM_S + lane_off + qd * 32, r);
+    else
+      tmem_st16(tb + TM_S + lane_off + qd * 16, r);
   }
   tmem_wait_st();
 }
@@ -183,13 +198,27 @@ __device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* b
 // warp's 16 x 32 output tile into 16-byte stores, followed by 256 B (64 B per
 // state warp) that hold the chunk's rq between the U' read and the output.  u_zero: the records carry
 // no U' (v is zero), which is taken as zero.
-template <int NST, class StageFree>
+//
+// kTimed (a diagnostic instantiation, kda_profile_phases): thread 0 writes
+// clock64() at the phase boundaries of chunk c to stamps[8 c + k] for
+// c < max_chunks (stamps null = not recorded):
+//   k = 0 MMA1 issued, 1 MMA1 complete, 2 E'^T written (MMA2 issued),
+//   3 MMA2 complete, 4 next record there, 5 snapshot and decay done (MMA1 of
+//   chunk c + 1 issued), 6 outputs stored.
+// kSnapCols: the column width of the snapshot pass (snapshot_and_decay).
+template <int NST, int kSnapCols, bool kTimed = false, class StageFree>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out, void* final_dst,
                                            bool state_bf16, int* err, uint8_t* ostage,
-                                           StageFree&& stage_free, bool u_zero = false) {
+                                           StageFree&& stage_free, bool u_zero = false,
+                                           long long* stamps = nullptr, int max_chunks = 0) {
+  auto stamp = [&](int c, int k) {
+    if constexpr (kTimed) {
+      if (v == 0 && stamps && c < max_chunks) stamps[8 * c + k] = clock64();
+    }
+  };
   float* rqstage = reinterpret_cast<float*>(ostage + 4096) + (v >> 5) * 16;
   bool ok = true;
   int n1 = 0, n2 = 0;  // MMA1 / MMA2 commits issued (thread 0)
@@ -197,7 +226,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
   if (nchunks > 0) {
     ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->full[0], 0, ctl, err));
     if (ok) {
-      snapshot_and_decay(tb, lane_off, reinterpret_cast<const float*>(ring + OFF_DL));
+      snapshot_and_decay<kSnapCols>(tb, lane_off, reinterpret_cast<const float*>(ring + OFF_DL));
       tc_fence_before();
     }
     ok = state_all(ok);
@@ -206,11 +235,13 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       issue_mma1(smem_u32(ring), tb, &ctl->mma1);
       ++n1;
     }
+    stamp(0, 0);
   }
   for (int c = 0; c < nchunks && ok; ++c) {
     const int s = c % NST;
     const uint8_t* st = ring + s * REC_STRIDE_SMEM;
     ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma1, c & 1, ctl, err));
+    stamp(c, 1);
     if (ok) {
       // corrected errors e[v][i] = U[i][v] - (W S^T)[i][v] -> tensor memory
       tc_fence_after();
@@ -249,7 +280,9 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       issue_mma2(smem_u32(st), tb, &ctl->mma2);
       ++n2;
     }
+    stamp(c, 2);
     ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->mma2, c & 1, ctl, err));
+    stamp(c, 3);
     uint32_t o[16];
     if (ok) {
       tc_fence_after();
@@ -270,9 +303,10 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       // snapshot S_{c+1} for MMA1 of chunk c+1 and apply that chunk's decay
       const int s1 = (c + 1) % NST;
       if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->full[s1], ((c + 1) / NST) & 1, ctl, err));
+      stamp(c, 4);
       if (ok) {
-        snapshot_and_decay(tb, lane_off,
-                           reinterpret_cast<const float*>(ring + s1 * REC_STRIDE_SMEM + OFF_DL));
+        snapshot_and_decay<kSnapCols>(
+            tb, lane_off, reinterpret_cast<const float*>(ring + s1 * REC_STRIDE_SMEM + OFF_DL));
         tc_fence_before();
       }
       // also: every thread has read this chunk's outputs out of D1
@@ -282,6 +316,8 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
         issue_mma1(smem_u32(ring + s1 * REC_STRIDE_SMEM), tb, &ctl->mma1);
         ++n1;
       }
+      stamp(c, 5);
+      stamp(c + 1, 0);
     }
     if (ok) {
       // warp tile [16 tokens][32 channels] bf16 through shared memory, then
@@ -304,6 +340,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       }
       __syncwarp();
     }
+    stamp(c, 6);
   }
   ok = state_all(ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
   if (!ok && v == 0) {

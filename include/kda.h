@@ -344,6 +344,28 @@ int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream);
  * outside that range and KDA_ERR_LAUNCH if the launch fails. */
 kda_status kda_selftest_timeout(int64_t limit_cycles, void* stream);
 
+/* Diagnostic: where the serial chain of the recurrence spends its time.
+ * Runs one forward pass over N equal sequences (no cu_seqlens, zero initial
+ * state, fp32 final state) with kernel 0 = the chunk kernel then a timed copy
+ * of the recurrence kernel (workspace as for kda_fwd, required), or kernel 1 =
+ * a timed copy of the fused kernel (workspace unused).  Thread 0 of the first
+ * (sequence, head) CTA writes the SM clock (clock64) at the phase boundaries
+ * of each of its first max_chunks chunks c to stamps[8 c + k] (device int64,
+ * 8-byte aligned, 8 max_chunks entries; entry 7 unused):
+ *   k = 0 first MMA issued, 1 first MMA complete, 2 corrected errors written
+ *   (second MMA issued), 3 second MMA complete, 4 next record available,
+ *   5 snapshot and decay of the state done, 6 outputs stored.
+ * The results (out, final_state) are those of kda_fwd.  The timed copies are
+ * separate instantiations; the other entry points do not record anything.
+ * There is no counterpart on the pages; it backs the per-phase analysis of the
+ * chain.  Errors as kda_fwd. */
+kda_status kda_profile_phases(int32_t kernel, const void* q, const void* k, const void* v,
+                              const void* g_raw, const void* beta_raw, float scale,
+                              float lower_bound, int64_t T_total, int32_t H, int32_t N,
+                              int32_t D, void* out, float* final_state, void* workspace,
+                              size_t workspace_bytes, long long* stamps, int32_t max_chunks,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -372,3 +372,18 @@ def test_host_buffer_entry_point_time_slices(schedule):
     ro, rs = oracle_case(inp)
     assert_close(f64(out), ro, f"{schedule} host slices out")
     assert_close(f64(fs), rs, f"{schedule} host slices final_state")
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_profile_phases_diagnostic(kernel):
+    # the timed copies give kda_fwd's results and stamps in phase order
+    from chunked_gated_delta_11_gb300 import phases
+    inp = to_dev(synth.make_inputs(2 * 640, 2, 2, seed=31))
+    st = phases.run(kernel, inp, 40)
+    o_ref, s_ref = run(inp, "split")
+    assert kda.kda_device_status() == 0
+    for c in range(40 - 1):
+        assert all(st[c, k] <= st[c, k + 1] for k in range(6)), (c, st[c])
+        assert st[c, 0] < st[c + 1, 0]
+    table = phases.table(st)
+    assert table["period"][0] > table["MMA1"][0] > 0
