@@ -109,6 +109,15 @@ def load(build_if_missing: bool = False):
         lib.kda_profile_phases.argtypes = [i32, P, P, P, P, P, f32, f32, i64, i32, i32, i32, P,
                                            P, P, sz, P, i32, P]
         lib.kda_profile_phases.restype = ctypes.c_int
+        lib.kda_piece_workspace_size.argtypes = [i64, i32]
+        lib.kda_piece_workspace_size.restype = sz
+        lib.kda_piece_forward.argtypes = [P, P, P, P, P, f32, f32, P, i64, i32, i32, P, P, P, P,
+                                          i32, P, sz, P]
+        lib.kda_piece_forward.restype = ctypes.c_int
+        lib.kda_pieces_scan.argtypes = [P, P, i32, i32, i32, P, P]
+        lib.kda_pieces_scan.restype = ctypes.c_int
+        lib.kda_piece_fixup.argtypes = [P, P, P, i64, i32, i32, P, sz, P]
+        lib.kda_piece_fixup.restype = ctypes.c_int
         lib.kda_selftest_timeout.argtypes = [i64, P]
         lib.kda_selftest_timeout.restype = ctypes.c_int
         lib.kda_selftest_tcgen05.argtypes = [P, P, P, P]

@@ -95,6 +95,19 @@ kda_status device_info(DeviceInfo& out) {
   return KDA_OK;
 }
 
+}  // namespace
+
+// The device error word of the current device, for the entry points in the
+// other translation units.
+kda_status error_word(int** out) {
+  DeviceInfo info;
+  const kda_status s = device_info(info);
+  if (s == KDA_OK) *out = info.err;
+  return s;
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 kda_status check_sizes(int64_t T_total, int32_t H, int32_t N, int32_t D,

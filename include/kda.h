@@ -344,6 +344,43 @@ int kda_selftest_tcgen05(float* out1, float* out2, int* status, void* stream);
  * outside that range and KDA_ERR_LAUNCH if the launch fails. */
 kda_status kda_selftest_timeout(int64_t limit_cycles, void* stream);
 
+/* Context parallelism: the pieces of one long sequence on different ranks.
+ * Each token step of the recurrence is an affine map of the state,
+ * S -> S A_t + beta_t v_t k^_t^T with A_t = Diag(alpha_t)(I - beta_t k^_t k^_t^T)
+ * ("You Could Have Come Up with Kimi Delta Attention", sec. 4.1), so the piece
+ * of rank r (tokens in order, all heads) maps its starting state S_0 to
+ * S_0 M_r + X_r, and inside it o_t = o^X_t + S_0 y_t, y_t = M_t (scale q^_t).
+ * A rank runs kda_piece_forward on its piece, the ranks exchange the (M_r, X_r)
+ * pairs (the only exchange step: 2 x H x 64 KiB per rank, gathered in rank
+ * order by the caller's collective library), each rank runs kda_pieces_scan
+ * over the gathered pairs and kda_piece_fixup on its own outputs.  Results
+ * agree with one pass over the whole sequence up to rounding (the fix-up adds
+ * S_0 y in bf16 with fp32 sums, as kda_fwd_segmented does).  All pointers are
+ * device pointers of the calling rank's GPU; states fp32 [H, V, K] per piece.
+ *
+ * kda_piece_forward: m_state == NULL: the first piece, a plain fused pass from
+ *   initial_state (NULL = zeros) writing `out` and its final state x_state.
+ *   m_state != NULL: a later piece (initial_state must be NULL): out = o^X
+ *   (from zero), x_state = X_r, m_state = M_r and y (bf16 [T_local, H, V]) =
+ *   the identity-start, v = 0 run's outputs (may be NULL for an empty
+ *   piece, T_local = 0, whose maps are X = 0 and M = I).  gate: KDA_GATE_*.  workspace:
+ *   kda_piece_workspace_size() bytes (needed with m_state).
+ * kda_pieces_scan: xs, ms fp32 [P, H, V, K] of the P pieces in order (ms[0] is
+ *   not read); replaces xs[j] (j >= 1) by piece j's starting state S_0 and
+ *   writes the state after the last piece to final_state (or NULL).
+ * kda_piece_fixup: out (bf16 [T_local, H, V]) += s0 (fp32 [H, V, K]) y; needs a
+ *   256-byte workspace. */
+size_t kda_piece_workspace_size(int64_t T_local, int32_t H);
+kda_status kda_piece_forward(const void* q, const void* k, const void* v, const void* g_raw,
+                             const void* beta_raw, float scale, float lower_bound,
+                             const float* initial_state, int64_t T_local, int32_t H, int32_t D,
+                             void* out, float* x_state, float* m_state, void* y, int32_t gate,
+                             void* workspace, size_t workspace_bytes, void* stream);
+kda_status kda_pieces_scan(float* xs, const float* ms, int32_t P, int32_t H, int32_t D,
+                           float* final_state, void* stream);
+kda_status kda_piece_fixup(void* out, const void* y, const float* s0, int64_t T_local, int32_t H,
+                           int32_t D, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Diagnostic: where the serial chain of the recurrence spends its time.
  * Runs one forward pass over N equal sequences (no cu_seqlens, zero initial
  * state, fp32 final state) with kernel 0 = the chunk kernel then a timed copy
