@@ -70,8 +70,8 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # is four times the b2 capture: b8 processes four times the units, and the
 # traffic is the per-unit inputs, outputs and states.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 538.057728e6 + 120.397056e6,
-    ("b8", "fused"): 4 * (538.057728e6 + 120.397056e6),
+    ("b2", "fused"): 538.522368e6 + 120.761088e6,
+    ("b8", "fused"): 4 * (538.522368e6 + 120.761088e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
     # the whole kda_fwd_segmented step: its four launches on the long workload
     ("long", "segmented"): 16.128e3 + (4559.290368e6 + 1910.622720e6) + 18.883072e6
