@@ -12,7 +12,7 @@ namespace kda {
 cudaError_t launch_chunk_prep(const void* q, const void* k, const void* v, const void* g,
                               const void* beta_raw, float scale, float lower_bound, float eps,
                               const int32_t* cu, int64_t T_total, int H, int N, void* ws,
-                              int gate_scalar, int sm_count, cudaStream_t stream);
+                              int gate_scalar, int sm_count, int* err, cudaStream_t stream);
 cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
                               int64_t T_total, int H, int N, void* out, void* final_state,
                               FwdOpts opts, int* err, cudaStream_t stream);
@@ -119,6 +119,8 @@ kda_status check_sizes(int64_t T_total, int32_t H, int32_t N, int32_t D,
   if (static_cast<int64_t>(N) * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
   if (T_total > (static_cast<int64_t>(1) << 40) / (static_cast<int64_t>(H) * KDA_HEAD_DIM))
     return KDA_ERR_INVALID_ARG;
+  // token coordinates of the tensor-map copies are int32
+  if (T_total >= (static_cast<int64_t>(1) << 31)) return KDA_ERR_INVALID_ARG;
   return KDA_OK;
 }
 
@@ -196,7 +198,7 @@ kda_status forward(int schedule, FwdOpts opts, const void* q, const void* k, con
     }
     if (T_total > 0)
       e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, cu_seqlens,
-                            T_total, H, N, ws, opts.gate_scalar, info.sm_count, st);
+                            T_total, H, N, ws, opts.gate_scalar, info.sm_count, info.err, st);
     if (e == cudaSuccess)
       e = launch_recurrence(ws, initial_state, cu_seqlens, T_total, H, N, out, final_state, opts,
                             info.err, st);
@@ -223,7 +225,7 @@ extern "C" kda_status kda_chunk_prep(const void* q, const void* k, const void* v
   if (T_total == 0) return KDA_OK;
   cudaError_t e = launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
                                     cu_seqlens, T_total, H, N, workspace, 0, info.sm_count,
-                                    static_cast<cudaStream_t>(stream));
+                                    info.err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
@@ -527,7 +529,8 @@ extern "C" kda_status kda_profile_phases(int32_t kernel, const void* q, const vo
         workspace_bytes < kda_workspace_size(T_total, H, N, D))
       return KDA_ERR_WORKSPACE;
     e = T_total > 0 ? launch_chunk_prep(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps,
-                                        nullptr, T_total, H, N, workspace, 0, info.sm_count, st)
+                                        nullptr, T_total, H, N, workspace, 0, info.sm_count,
+                                        info.err, st)
                     : cudaSuccess;
     if (e == cudaSuccess)
       e = launch_recurrence_timed(workspace, nullptr, nullptr, T_total, H, N, out, final_state,

@@ -46,17 +46,18 @@
 // their tf32 part).
 //
 // Raw input tiles (16 rows of 128 bf16) live in shared buffers of the caller:
-// q, k, g_raw of a chunk in one buffer (in that order), v in another; row r
-// (256 bytes) starts at r * 272 + 64 (r >> 3), so that 8 consecutive rows
-// fall on distinct banks (ldmatrix) and rows r and r + 8 on opposite halves of
-// the banks (the factor pass reads both at once), with plain row-linear
-// addressing.  They arrive as two cp.async
-// groups: q, k, g_raw (issued during an earlier build, once that build's
-// factor pass is done with its own buffer) and v (issued at the start of the
-// chunk's own build, once the previous U' products are done with the v buffer).
+// q, k, g_raw of a chunk in one buffer (in that order), v in another.  They
+// arrive by tensor-map (TMA) copies, two boxes per tile (layout in
+// kda_tma.cuh), issued by one thread onto an mbarrier: q, k, g_raw during an
+// earlier build, once that build's factor pass is done with its buffer, and
+// v at the start of the chunk's own build.  In a partial chunk the rows past
+// its end (whatever follows in the tensor) are overwritten once the tiles
+// are there: zeros for q, k, v and -inf for g_raw, so those tokens are no-ops
+// and their record rows are zero.
 #pragma once
 
 #include "kda_common.cuh"
+#include "kda_tma.cuh"
 
 namespace kda {
 
@@ -64,10 +65,8 @@ constexpr int RS = 20;  // float row stride of -R'^T (conflict-free accumulator 
 constexpr int AS = 24;  // float row stride of the A' tiles (conflict-free fragment loads)
 
 enum { RAW_Q = 0, RAW_K = 1, RAW_G = 2 };
-constexpr int RAW_ROW = 272;                 // padded row stride of a raw tile
-constexpr int RAW_TILE = 16 * RAW_ROW + 64;  // one raw tile (4416 B)
-constexpr int QKG_BYTES = 3 * RAW_TILE;      // one chunk's q, k, g_raw tiles
-constexpr int V_BYTES = RAW_TILE;            // one chunk's v tile
+constexpr int QKG_BYTES = 3 * RAW_TILE;  // one chunk's q, k, g_raw tiles
+constexpr int V_BYTES = RAW_TILE;        // one chunk's v tile
 
 // Per-group scratch.  Derived operand tiles are bf16, stored transposed,
 // [128 channels][16 tokens] (32 B per channel, tokens 0-7 and 8-15 in two
@@ -83,14 +82,9 @@ struct ChunkSmem {
   float pm[128];     // m = P_7 per key channel (the W' columns are scaled by it)
   float rq[16], rk[16], beta[16];
   float g2[4][16];  // partial squared norms (warp w: q for w < 2, k otherwise)
+  float2 hx[4][32];  // the half-chunk products of each thread's channel pair
 };
 
-__host__ __device__ __forceinline__ constexpr int raw_row_off(int i) {
-  return i * RAW_ROW + ((i >> 3) << 6);
-}
-__device__ __forceinline__ uint8_t* raw_row(uint8_t* raw, int x, int i) {
-  return raw + x * RAW_TILE + raw_row_off(i);
-}
 // byte offset of (channel d, token half h) in a derived tile: the eight
 // 16-byte slots of each 128-byte group of four channels are XOR-permuted by 3
 // in every other group
@@ -137,10 +131,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
 
 __device__ __forceinline__ float2 bf2_at(const uint8_t* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
@@ -159,93 +149,123 @@ __device__ __forceinline__ void split2(float2 x, uint32_t& hi, uint32_t& lo) {
 // larger CTA can run other warps beside them).
 __device__ __forceinline__ void chunk_sync() { named_bar(1, 128); }
 
-// The raw-tile loads of one thread, set up once: thread t copies 16-byte piece
-// (t & 15) of rows (t >> 4) and (t >> 4) + 8 of every tile with cp.async; rows
-// past a chunk's end get `fill` (two bf16 per word) by plain stores instead.
-struct TileLoader {
-  uint32_t soff0, soff1;  // shared offsets of the piece in rows (t >> 4) and (t >> 4) + 8
-  int64_t goff;           // element offset of the piece from the chunk's first token
-  int64_t rstride8;       // elements between a row and the row 8 further
-  int row;
-  __device__ __forceinline__ TileLoader(int t, int64_t row_stride) {
-    row = t >> 4;
-    const int c = t & 15;
-    soff0 = static_cast<uint32_t>(raw_row_off(row) + c * 16);
-    soff1 = static_cast<uint32_t>(raw_row_off(row + 8) + c * 16);
-    goff = row * row_stride + c * 8;
-    rstride8 = row_stride * 8;
-  }
-  // tile: shared base of one 16-row tile; src: the chunk's first token, head h
-  __device__ __forceinline__ void load(uint8_t* tile, const __nv_bfloat16* src, int nc,
-                                       uint32_t fill) const {
-    const __nv_bfloat16* s0 = src + goff;
-    if (row < nc)
-      cp_async16(tile + soff0, s0);
-    else
-      *reinterpret_cast<uint4*>(tile + soff0) = make_uint4(fill, fill, fill, fill);
-    if (row + 8 < nc)
-      cp_async16(tile + soff1, s0 + rstride8);
-    else
-      *reinterpret_cast<uint4*>(tile + soff1) = make_uint4(fill, fill, fill, fill);
-  }
-};
-// Scalar gate (one g_raw per token and head, broadcast over the key channels):
-// the g tile is written with plain stores.  gs points at the chunk's first
-// token, head h; its token stride is `gstride` elements.
-__device__ __forceinline__ void broadcast_gate_tile(const TileLoader& L, uint8_t* tile,
-                                                    const __nv_bfloat16* gs, int64_t gstride,
-                                                    int nc) {
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int row = L.row + 8 * half;
-    uint32_t w = 0xFF80FF80u;
-    if (row < nc) {
-      const uint32_t b = __bfloat16_as_ushort(gs[row * gstride]);
-      w = b | (b << 16);
-    }
-    *reinterpret_cast<uint4*>(tile + (half ? L.soff1 : L.soff0)) = make_uint4(w, w, w, w);
-  }
-}
-// q, k and g_raw of one chunk (pointers at its first token, head h): the first
-// cp.async group of its raw tiles.  gstride > 0: g_raw is one value per token
-// and head (token stride gstride), broadcast over the key channels.
-__device__ __forceinline__ void issue_qkg_loads(const TileLoader& L, uint8_t* raw,
-                                                const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                                const __nv_bfloat16* g, int nc,
-                                                int64_t gstride = 0) {
-  L.load(raw + RAW_Q * RAW_TILE, q, nc, 0u);
-  L.load(raw + RAW_K * RAW_TILE, k, nc, 0u);
-  // g_raw rows past the end hold -inf: sigma(-inf) = 0 gives a = 2^0 = 1 exactly,
-  // so those tokens neither decay nor change the running products
-  if (gstride > 0)
-    broadcast_gate_tile(L, raw + RAW_G * RAW_TILE, g, gstride, nc);
-  else
-    L.load(raw + RAW_G * RAW_TILE, g, nc, 0xFF80FF80u);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// v of one chunk into a v buffer: the second group
-__device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
-                                              const __nv_bfloat16* v, int nc) {
-  L.load(vt, v, nc, 0u);
-  asm volatile("cp.async.commit_group;" ::: "memory");
+// AND of `pred` over the 128 chunk threads (named barrier 1).
+__device__ __forceinline__ bool chunk_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
 }
 
+// q, k and g_raw of one chunk (first token t0, head h) into the buffer `raw`,
+// completing on `bar` (initialised for one arrival): one thread issues them.
+// With the scalar gate only q and k are copied; broadcast_gate_tile writes g.
+__device__ __forceinline__ void issue_qkg_tma(const RawMaps& maps, uint8_t* raw, int h,
+                                              int64_t t0, bool gate_scalar, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, (gate_scalar ? 2 : 3) * RAW_TILE);
+  const int t = static_cast<int>(t0);
+  tma_tile(raw + RAW_Q * RAW_TILE, &maps.q, h, t, bar);
+  tma_tile(raw + RAW_K * RAW_TILE, &maps.k, h, t, bar);
+  if (!gate_scalar) tma_tile(raw + RAW_G * RAW_TILE, &maps.g, h, t, bar);
+}
+// v of one chunk into the v buffer, completing on `bar`: one thread.
+__device__ __forceinline__ void issue_v_tma(const RawMaps& maps, uint8_t* vt, int h, int64_t t0,
+                                            uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, RAW_TILE);
+  tma_tile(vt, &maps.v, h, static_cast<int>(t0), bar);
+}
+// Scalar gate (one g_raw per token and head, broadcast over the key channels):
+// the g tile written with plain stores by the 128 threads, thread t the
+// 16-byte pieces (t & 7) of row t >> 3 in both boxes.  gs points at the
+// chunk's first token, head h, with token stride `gstride`; rows past the end
+// hold -inf (sigma(-inf) = 0, so a = 2^0 = 1).
+__device__ __forceinline__ void broadcast_gate_tile(uint8_t* tile, const __nv_bfloat16* gs,
+                                                    int64_t gstride, int nc, int t) {
+  const int r = t >> 3, pc = t & 7;
+  uint32_t w = 0xFF80FF80u;
+  if (r < nc) {
+    const uint32_t b = __bfloat16_as_ushort(gs[r * gstride]);
+    w = b | (b << 16);
+  }
+  const uint4 x = make_uint4(w, w, w, w);
+  *reinterpret_cast<uint4*>(tile + r * RAW_ROW + pc * 16) = x;
+  *reinterpret_cast<uint4*>(tile + RAW_BOX + r * RAW_ROW + pc * 16) = x;
+}
+
+// Rows nc .. 15 of a raw tile that arrived by TMA hold whatever follows the
+// chunk in the tensor: in a partial chunk the 128 threads overwrite them with
+// `fill` (two bf16 per word), thread t the 16-byte pieces (t & 7) of row
+// t >> 3 in both boxes.  Zero rows of q, k and v, and -inf rows of g_raw
+// (retention 2^0 = 1), make those tokens no-ops, as the record format states.
+__device__ __forceinline__ void fill_rows_past_end(uint8_t* tile, int nc, uint32_t fill, int t) {
+  const int r = t >> 3, pc = t & 7;
+  if (r < nc) return;
+  const uint4 x = make_uint4(fill, fill, fill, fill);
+  *reinterpret_cast<uint4*>(tile + r * RAW_ROW + pc * 16) = x;
+  *reinterpret_cast<uint4*>(tile + RAW_BOX + r * RAW_ROW + pc * 16) = x;
+}
+
+// Bounded wait of the chunk threads on a raw-tile barrier: false once
+// *abort is set or the wait runs out (then *abort is set and the error word
+// latches KDA_ERR_TIMEOUT), as every wait of libkda.
+__device__ __forceinline__ bool raw_wait(uint64_t* bar, uint32_t parity, int* abort, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
+    if (*reinterpret_cast<volatile int*>(abort)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *reinterpret_cast<volatile int*>(abort) = 1;
+      atomicExch(err, 5);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Where the raw tiles of the chunk being built arrive: the q/k/g_raw barrier
+// and phase, and (unless the record's U' is known to be zero) the v barrier
+// and phase; `abort` and `err` as in raw_wait.  Optionally the q/k/g_raw
+// barrier and phase of the next chunk the thread builds, which the build
+// tests without waiting (at its v wait) and reports in *next_ready; a later
+// build given qkg_ready = that result skips its own wait.  A parity test is
+// only exact once the barrier's previous phase is known complete: true for
+// the next chunk of a double buffer whose previous use this thread waited on.
+struct RawSync {
+  uint64_t* qkg_bar;
+  uint32_t qkg_parity;
+  uint64_t* v_bar;
+  uint32_t v_parity;
+  int* abort;
+  int* err;
+  bool qkg_ready = false;
+  uint64_t* next_qkg_bar = nullptr;
+  uint32_t next_qkg_parity = 0;
+  bool* next_ready = nullptr;
+};
+
 // Build the record of one chunk whose q, k, g_raw tiles were issued into `raw`
-// with issue_qkg_loads (this call waits for them; `newer_qkg` says whether the
-// q, k, g_raw group of a later chunk was issued after them, and may still be
-// pending).  Its v tile goes to `vt`.  All 128 threads of the group must call
-// it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
+// with issue_qkg_tma (this call waits for them on rs.qkg_bar).  Its v tile
+// goes to `vt` (waited on rs.v_bar; issued by load_v, or by the caller before
+// the call).  All 128 threads of the
+// group must call it.  beta_raw_bits: thread t < 16 holds the bf16 bits of token t's
 // beta_raw (any value for t >= nc).  `rec` is the record base (global or
 // shared memory).  Hooks, each run by
 // all 128 threads:
-//   may_write()  before the first write to the record; returns, uniformly,
-//                whether to go on (the fused kernel waits there until the
-//                previous record of this stage is consumed).  Includes a
-//                barrier of the group.  On false nothing is written.
-//   load_v()     right after may_write: issue this chunk's v tile (issue_v_loads).
+//   may_write(ok)  before the first write to the record, with ok = whether
+//                the raw tiles arrived; returns, uniformly, whether to go on
+//                (the fused kernel also waits there until the previous record
+//                of this stage is consumed).  Includes a barrier of the group.
+//                On false nothing is written.
+//   load_v()     right after may_write: issue this chunk's v tile (issue_v_tma),
+//                unless the caller issued it earlier.
 //   next_qkg()   once the factor pass is done with `raw`: issue a later chunk's
-//                q, k, g_raw tiles (into `raw` or another buffer); returns
-//                whether it issued them.
+//                q, k, g_raw tiles (into `raw` or another buffer).
 // Returns may_write().  With u_zero (v known to be zero) U' is zero and is
 // neither formed nor written; the reader must take it as zero.
 // kRecShared: `rec` is in shared memory (the fused kernel's ring), so W' goes
@@ -253,29 +273,35 @@ __device__ __forceinline__ void issue_v_loads(const TileLoader& L, uint8_t* vt,
 // (K1) takes plain 4-byte stores.
 template <bool kRecShared, class MayWrite, class LoadV, class NextQKG>
 __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, uint8_t* vt,
-                                                   bool newer_qkg, uint32_t beta_raw_bits,
+                                                   const RawSync& rs, uint32_t beta_raw_bits,
                                                    int nc, float scale,
                                                    float lb_log2e, float eps, uint8_t* rec, int t,
                                                    MayWrite&& may_write, LoadV&& load_v,
                                                    NextQKG&& next_qkg, bool u_zero = false) {
   const int w = t >> 5, l = t & 31;
-  if (newer_qkg)
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  const bool arrived = rs.qkg_ready || raw_wait(rs.qkg_bar, rs.qkg_parity, rs.abort, rs.err);
+  if (nc < kChunk) {
+    fill_rows_past_end(raw + RAW_Q * RAW_TILE, nc, 0u, t);
+    fill_rows_past_end(raw + RAW_K * RAW_TILE, nc, 0u, t);
+    fill_rows_past_end(raw + RAW_G * RAW_TILE, nc, 0xFF80FF80u, t);
+  }
   if (t < 16) {
     const float br = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(beta_raw_bits)));
     S.beta[t] = (t < nc) ? sigmoid_fast(br) : 0.f;
   }
-  if (!may_write()) return false;  // includes a barrier of the 128 threads
+  if (!may_write(arrived)) return false;  // includes a barrier of the 128 threads
   load_v();
 
   // ---- factor pass: norms (tensor cores), retention factors, decayed factors ----
-  // Thread (p, hf): key channels d0 = 2p, 2p + 1, tokens 8 hf .. 8 hf + 7; the
-  // two halves of a channel pair sit in neighbouring lanes.
-  const int p = 16 * w + (l >> 1), hf = l & 1, d0 = 2 * p;
+  // Thread (w, l): token half hf = l & 1 (tokens 8 hf .. 8 hf + 7) and key
+  // channels d0, d0 + 1 of the 32-channel group (w & 1) ^ hf of box w >> 1.
+  // The two half-warps of one load thus read rows ii and 8 + ii in opposite
+  // 64-byte halves of the banks (conflict-free); the thread with the same
+  // channels and the other token half is lane l ^ 1 of warp w ^ 1.
+  const int hf = l & 1;
+  const int d0 = 64 * (w >> 1) + 32 * ((w & 1) ^ hf) + 2 * (l >> 1);
   // byte offset of the thread's bf16 pair in raw row 8 hf + ii
-  const int rbase = raw_row_off(8 * hf) + d0 * 2;
+  const int rbase = raw_off(8 * hf, d0);
   auto roff = [&](int ii) { return rbase + ii * RAW_ROW; };
 
   // Warp w: the 16 x 16 Gram matrix G = X X^T of X = q (w < 2) or k over the
@@ -287,7 +313,8 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   float gacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // column tiles 0, 1
   {
     const int mi = l >> 3;
-    const uint8_t* pa = raw_row(raw, nx, (l & 7) + (mi & 1) * 8) + (mi >> 1) * 16 + (w & 1) * 128;
+    const uint8_t* pa = raw + nx * RAW_TILE + raw_off((l & 7) + (mi & 1) * 8, 64 * (w & 1)) +
+                        (mi >> 1) * 16;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t a[4];
@@ -312,6 +339,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
       Pl[ii] = ii ? __fmul2_rn(Pl[ii - 1], a[ii]) : a[ii];
     }
   }
+  S.hx[w][l] = Pl[7];  // read by the other token half after the pair barrier
   {
     // diagonal: lane (g = l >> 2, c = l & 3) holds columns 8 nt + 2c, +1 of
     // rows g (acc 0, 1) and g + 8 (acc 2, 3) of column tile nt; the two warps
@@ -337,10 +365,10 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
         S.rk[l] = rsqrtf(s2 + eps);
     }
   }
-  // products over the other half from the neighbouring lane
+  // products over the other half, from lane l ^ 1 of warp w ^ 1 (written
+  // before the pair barrier above)
   const float2 Hh = Pl[7];
-  const float2 Ho = make_float2(__shfl_xor_sync(0xffffffffu, Hh.x, 1),
-                                __shfl_xor_sync(0xffffffffu, Hh.y, 1));
+  const float2 Ho = S.hx[w ^ 1][l ^ 1];
   float2 Qu[8];  // q P of this thread's tokens (Qdec; rq is applied to the outputs)
   {
     const float2 one = make_float2(1.f, 1.f);
@@ -399,7 +427,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
   }
   chunk_sync();
   // q, k and g_raw of this chunk are no longer read
-  const bool prefetched = next_qkg();
+  next_qkg();
 
   // ---- Mkk (warps 0,1) -> -R'^T, Mqk (warps 2,3) -> Aqk'; Qdec -> record ----
   {
@@ -477,11 +505,14 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
       for (int i = 0; i < 16; ++i) dst[i * AS] = x[i] * f;
     }
   }
-  // this chunk's v tile (the older of at most two pending groups)
-  if (prefetched)
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  // this chunk's v tile (a timeout latches the error and the record is
+  // finished on whatever is there; the caller sees the error word)
+  if (rs.next_ready)
+    *rs.next_ready = rs.next_qkg_bar && mbar_test_wait(rs.next_qkg_bar, rs.next_qkg_parity);
+  if (!u_zero) {
+    raw_wait(rs.v_bar, rs.v_parity, rs.abort, rs.err);
+    if (nc < kChunk) fill_rows_past_end(vt, nc, 0u, t);
+  }
   chunk_sync();
 
   // ---- W' = A' diag(beta rk^2) kP, U' = A' diag(beta rk) V (warp w: channels 32w..32w+31) ----
@@ -540,7 +571,7 @@ __device__ __forceinline__ bool build_chunk_record(ChunkSmem& S, uint8_t* raw, u
       const int m0 = w * 32 + mt * 16;
       const int j = (l & 7) + (mi >> 1) * 8;
       uint32_t av[4];
-      ldsm_x4_t(av, raw_row(vt, 0, j) + ((m0 >> 3) + (mi & 1)) * 16);
+      ldsm_x4_t(av, vt + raw_off(j, m0 + 8 * (mi & 1)));
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         float u[4] = {0.f, 0.f, 0.f, 0.f};

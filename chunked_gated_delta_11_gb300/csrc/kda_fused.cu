@@ -21,6 +21,7 @@
 // recurrence of chunk c inside every CTA instead.
 #include "kda_chunk.cuh"
 #include "kda_state.cuh"
+#include "kda_tma.cuh"
 
 namespace kda {
 
@@ -39,30 +40,24 @@ constexpr int F_RAW_OFF = F_CHUNK_OFF + ((static_cast<int>(sizeof(ChunkSmem)) + 
 constexpr int F_V_OFF = F_RAW_OFF + 2 * QKG_BYTES;  // q, k, g_raw double-buffered
 constexpr int F_OST_OFF = F_V_OFF + V_BYTES;
 constexpr int F_CTL_OFF = F_OST_OFF + 4096 + 256;  // output staging, then rq slots
-constexpr int F_SMEM = F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 1024 + 64;
+// the raw tiles' barriers (q/k/g_raw buffers 0 and 1, v) and how many copy
+// groups each has had (read after an abort, to let the last ones land)
+struct RawBars {
+  uint64_t qkg[2];
+  uint64_t v;
+  int qkg_n, v_n;
+};
+constexpr int F_RB_OFF = (F_CTL_OFF + static_cast<int>(sizeof(StateCtl<F_NST>)) + 7) & ~7;
+constexpr int F_SMEM = F_RB_OFF + static_cast<int>(sizeof(RawBars)) + 1024 + 64;
+static_assert(F_RAW_OFF % 128 == 0 && F_V_OFF % 128 == 0, "TMA destinations are 128-byte aligned");
 // two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA
 static_assert(2 * (F_SMEM + 1024) <= 228 * 1024, "fused kernel must fit two CTAs per SM");
-
-// AND of `pred` over the 128 chunk threads (named barrier 1).
-__device__ __forceinline__ bool chunk_all(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, 1, 128, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred))
-      : "memory");
-  return r != 0;
-}
 
 // kTimed: the diagnostic instantiation of kda_profile_phases, in which thread
 // 0 of CTA 0 records the state side's phase stamps (state_rows).
 template <bool kGateScalar, bool kTimed>
 __global__ void __launch_bounds__(F_THREADS, 2)
-fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-             const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restrict__ g,
              const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e, float eps,
              const void* init, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
              __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts, SegArgs seg,
@@ -72,6 +67,7 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   uint8_t* smem = align1024(smem_raw);
   ChunkSmem& CS = *reinterpret_cast<ChunkSmem*>(smem + F_CHUNK_OFF);
   auto* ctl = reinterpret_cast<StateCtl<NST>*>(smem + F_CTL_OFF);
+  auto* rb = reinterpret_cast<RawBars*>(smem + F_RB_OFF);
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   int unit = blockIdx.x;
   const bool mrole = seg.P > 0 && unit >= N * H;  // segmented launch, M role (SegArgs)
@@ -99,6 +95,11 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
     }
     mbar_init(&ctl->mma1, 1);
     mbar_init(&ctl->mma2, 1);
+    mbar_init(&rb->qkg[0], 1);  // one arrive.expect_tx per copy group
+    mbar_init(&rb->qkg[1], 1);
+    mbar_init(&rb->v, 1);
+    rb->qkg_n = 0;
+    rb->v_n = 0;
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -120,63 +121,78 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
   __syncthreads();
   tc_fence_after();
 
+  // Raw input tiles: q, k, g_raw double-buffered, v single.  One state
+  // thread issues each copy group (kda_tma.cuh): those of chunks 0 and 1 (v:
+  // chunk 0) at the start, then each as soon as record j is there
+  // (on_record): chunk j is done with its q, k, g_raw buffer, which takes
+  // chunk j + 2, and with the v buffer, which takes chunk j + 1.  So the
+  // copies cost the chunk threads nothing, and q, k, g_raw have a whole
+  // build to arrive, v the first part of one.
+  auto rawbuf = [&](int c) { return smem + F_RAW_OFF + (c & 1) * QKG_BYTES; };
+  uint8_t* vt = smem + F_V_OFF;
+  auto chunk_t0 = [&](int c) { return bos + static_cast<int64_t>(c) * kChunk; };
+  auto issue_qkg = [&](int c) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    issue_qkg_tma(maps, rawbuf(c), h, chunk_t0(c), kGateScalar, &rb->qkg[c & 1]);
+    ++rb->qkg_n;
+  };
+  // M role: v = 0, nothing to load (the record's U' is taken as zero)
+  auto issue_v = [&](int c) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    issue_v_tma(maps, vt, h, chunk_t0(c), &rb->v);
+    ++rb->v_n;
+  };
+
   if (w >= 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_CHUNK_REGS));
     // ---------------- chunk threads ----------------
-    // q, k, g_raw tiles are double-buffered: those of chunk c+2 load into
-    // chunk c's buffer as soon as chunk c's gate phase is done with them, so
-    // they have a whole build to arrive; v of chunk c loads at the start of
-    // its own build.
     const int tc = t - 128;
-    auto rawbuf = [&](int c) { return smem + F_RAW_OFF + (c & 1) * QKG_BYTES; };
-    uint8_t* vt = smem + F_V_OFF;
-    const int64_t row_stride = static_cast<int64_t>(H) * kDim;
-    const TileLoader loader(tc, row_stride);
-    // g_raw of head h: per channel [T, H, 128], or one value per token [T, H]
-    const int64_t gstride = kGateScalar ? H : row_stride;
-    const __nv_bfloat16* g0 = g + (kGateScalar ? h : static_cast<int64_t>(h) * kDim);
-    auto chunk_geom = [&](int c, int64_t& t0, int& nc) {
-      t0 = bos + static_cast<int64_t>(c) * kChunk;
-      nc = static_cast<int>((eos - t0) < kChunk ? (eos - t0) : kChunk);
+    // g_raw of head h as one value per token (the scalar gate, [T, H])
+    const __nv_bfloat16* g0 = g + h;
+    auto chunk_nc = [&](int c) {
+      const int64_t left = eos - chunk_t0(c);
+      return static_cast<int>(left < kChunk ? left : kChunk);
     };
-    auto start = [&](int c) -> uint32_t {
-      int64_t t0;
-      int nc;
-      chunk_geom(c, t0, nc);
-      const int64_t base = t0 * row_stride + static_cast<int64_t>(h) * kDim;
-      issue_qkg_loads(loader, rawbuf(c), q + base, k + base, g0 + t0 * gstride, nc,
-                      kGateScalar ? gstride : 0);
+    // beta_raw of chunk c (and, for the scalar gate, its g_raw tile, written
+    // once the buffer's previous chunk is done with it)
+    auto prepare = [&](int c) -> uint32_t {
+      const int64_t t0 = chunk_t0(c);
+      const int nc = chunk_nc(c);
+      if (kGateScalar) broadcast_gate_tile(rawbuf(c) + RAW_G * RAW_TILE, g0 + t0 * H, H, nc, tc);
       return (tc < nc) ? __bfloat16_as_ushort(beta_raw[(t0 + tc) * H + h]) : 0u;
     };
     uint32_t bbits[2] = {0u, 0u};  // beta_raw bits of chunks c and c+1
-    if (nchunks > 0) bbits[0] = start(0);
-    if (nchunks > 1) bbits[1] = start(1);
+    // whether an earlier test found the next chunk's q, k, g_raw there
+    bool qkg_ready = false;
+    if (nchunks > 0) bbits[0] = prepare(0);
+    if (nchunks > 1) bbits[1] = prepare(1);
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % NST;
-      int64_t t0;
-      int nc;
-      chunk_geom(c, t0, nc);
+      const int nc = chunk_nc(c);
       uint32_t next_bits = 0u;
-      // before writing record c into stage s: record c - NST there must be
-      // fully consumed (its MMAs read [Qdec ; W] and [Kend ; Aqk])
-      auto may_write = [&]() -> bool {
-        bool ok = c < NST || wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err);
+      // before writing record c into stage s: its raw tiles are there, and
+      // record c - NST in that stage is fully consumed (its MMAs read
+      // [Qdec ; W] and [Kend ; Aqk]).  The first chunk warp polls the empty
+      // barrier; all of them agree through the barrier reduction.
+      auto may_write = [&](bool arrived) -> bool {
+        bool ok = arrived && (c < NST || tc >= 32 ||
+                              wait_or_abort(&ctl->empty[s], ((c / NST) - 1) & 1, ctl, err));
         ok = ok && !*reinterpret_cast<volatile int*>(&ctl->abort);
         return chunk_all(ok);
       };
-      auto load_v = [&] {
-        // M role: v = 0, every row of the tile takes the zero fill
-        issue_v_loads(loader, vt, v + t0 * row_stride + static_cast<int64_t>(h) * kDim,
-                      mrole ? 0 : nc);
-      };
-      auto next_qkg = [&]() -> bool {
-        if (c + 2 >= nchunks) return false;
-        next_bits = start(c + 2);
-        return true;
+      auto next_qkg = [&] {
+        if (c + 2 < nchunks) next_bits = prepare(c + 2);
       };
       uint8_t* rec = smem + s * REC_STRIDE_SMEM;
-      if (!build_chunk_record<true>(CS, rawbuf(c), vt, c + 1 < nchunks, bbits[0], nc, scale,
-                              lb_log2e, eps, rec, tc, may_write, load_v, next_qkg, mrole))
+      // chunk c is the (c >> 1)-th use of its q, k, g_raw buffer and the
+      // c-th v copy
+      const bool has_next = c + 1 < nchunks;
+      const RawSync rs{&rb->qkg[c & 1], static_cast<uint32_t>((c >> 1) & 1), &rb->v,
+                       static_cast<uint32_t>(c & 1), &ctl->abort, err, qkg_ready,
+                       has_next ? &rb->qkg[(c + 1) & 1] : nullptr,
+                       static_cast<uint32_t>(((c + 1) >> 1) & 1), &qkg_ready};
+      if (!build_chunk_record<true>(CS, rawbuf(c), vt, rs, bbits[0], nc, scale, lb_log2e, eps,
+                                    rec, tc, may_write, [] {}, next_qkg, mrole))
         break;
       // every thread's record stores -> async proxy, then one arrival per warp
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -185,11 +201,22 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
       bbits[0] = bbits[1];
       bbits[1] = next_bits;
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_STATE_REGS));
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
+    // the first copies: q, k, g_raw of chunks 0 and 1 (state warp 1), v of
+    // chunk 0 (state warp 2); then, once record j is there, q, k, g_raw of
+    // chunk j + 2 and v of chunk j + 1
+    if (t == 32) {
+      if (nchunks > 0) issue_qkg(0);
+      if (nchunks > 1) issue_qkg(1);
+    }
+    if (t == 64 && !mrole && nchunks > 0) issue_v(0);
+    auto on_record = [&](int j, int sw) {
+      if (sw == 1 && j + 2 < nchunks) issue_qkg(j + 2);
+      if (sw == 2 && !mrole && j + 1 < nchunks) issue_v(j + 1);
+    };
     // a segmented launch writes every piece's final state to its fp32 workspace
     const bool final_bf16 = opts.state_bf16 && seg.P == 0;
     // 16-column snapshot pieces: the state warps run under the 152-register cap
@@ -197,11 +224,21 @@ fused_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restric
                             mrole ? seg.y : out,
                             state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
                                      state_base + static_cast<int64_t>(t) * kDim, final_bf16),
-                            final_bf16, err, smem + F_OST_OFF, release, mrole,
+                            final_bf16, err, smem + F_OST_OFF, release, on_record, mrole,
                             blockIdx.x == 0 ? stamps : nullptr, max_chunks);
   }
   tc_fence_before();
   __syncthreads();
+  // after an abort, copies still in flight must land before the CTA exits:
+  // each barrier has at most one phase pending, the last one issued
+  if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
+    const int nq = rb->qkg_n, nv = rb->v_n;
+    for (int b = 0; b < 2; ++b) {
+      const int last = nq - 1 - ((nq - 1 - b) & 1);  // last chunk in buffer b
+      if (last >= 0) mbar_wait(&rb->qkg[b], (last >> 1) & 1);
+    }
+    if (nv > 0) mbar_wait(&rb->v, (nv - 1) & 1);
+  }
   if (w == 0) tmem_dealloc(tb, TM_COLS);
 }
 
@@ -230,9 +267,12 @@ cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const vo
   const int64_t units = static_cast<int64_t>(N) * H * (seg.P > 0 ? 2 : 1);
   if (units == 0) return cudaSuccess;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  RawMaps maps;
+  if (const cudaError_t e = make_raw_maps(&maps, q, k, v, g, T_total, H, kGateScalar);
+      e != cudaSuccess)
+    return e;
   fused_kernel<kGateScalar, kTimed><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
+      maps, static_cast<const __nv_bfloat16*>(g),
       static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
       init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err,
       stamps, max_chunks);

@@ -90,7 +90,7 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
   state_rows<NST, 32, kTimed>(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h, out,
                           state_at(final_state, state_base + static_cast<int64_t>(t) * kDim,
                                    opts.state_bf16),
-                          opts.state_bf16, err, smem + K2_OST_OFF, refill, false,
+                          opts.state_bf16, err, smem + K2_OST_OFF, refill, [](int, int) {}, false,
                           blockIdx.x == 0 ? stamps : nullptr, max_chunks);
   if (t == 0 && *reinterpret_cast<volatile int*>(&ctl->abort)) {
     // copies still in flight must land before the CTA releases its memory

@@ -206,14 +206,19 @@ __device__ __forceinline__ void issue_mma2(uint32_t sb, uint32_t tb, uint64_t* b
 //   3 MMA2 complete, 4 next record there, 5 snapshot and decay done (MMA1 of
 //   chunk c + 1 issued), 6 outputs stored.
 // kSnapCols: the column width of the snapshot pass (snapshot_and_decay).
-template <int NST, int kSnapCols, bool kTimed = false, class StageFree>
+// on_record(j, w) runs on lane 0 of state warps w = 1, 2, 3 once record j is
+// there (after full[j % NST] passed; for j > 0 at the end of chunk j - 1):
+// the record's producer is done with every input of chunk j, so a caller may
+// reuse that chunk's input buffers.
+template <int NST, int kSnapCols, bool kTimed = false, class StageFree, class OnRecord>
 __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, int nchunks,
                                            uint32_t tb, uint32_t lane_off, int v, int64_t bos,
                                            int64_t eos, int H, int h,
                                            __nv_bfloat16* __restrict__ out, void* final_dst,
                                            bool state_bf16, int* err, uint8_t* ostage,
-                                           StageFree&& stage_free, bool u_zero = false,
-                                           long long* stamps = nullptr, int max_chunks = 0) {
+                                           StageFree&& stage_free, OnRecord&& on_record,
+                                           bool u_zero = false, long long* stamps = nullptr,
+                                           int max_chunks = 0) {
   auto stamp = [&](int c, int k) {
     if constexpr (kTimed) {
       if (v == 0 && stamps && c < max_chunks) stamps[8 * c + k] = clock64();
@@ -225,6 +230,7 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
   // chunk 0: snapshot the initial state and apply chunk 0's decay
   if (nchunks > 0) {
     ok = __all_sync(0xffffffffu, wait_or_abort(&ctl->full[0], 0, ctl, err));
+    if (ok && v >= 32 && (v & 31) == 0) on_record(0, v >> 5);
     if (ok) {
       snapshot_and_decay<kSnapCols>(tb, lane_off, reinterpret_cast<const float*>(ring + OFF_DL));
       tc_fence_before();
@@ -341,6 +347,9 @@ __device__ __forceinline__ void state_rows(StateCtl<NST>* ctl, uint8_t* ring, in
       __syncwarp();
     }
     stamp(c, 6);
+    // record c + 1 was there before the snapshot above (called here, where
+    // the outputs no longer hold registers)
+    if (ok && c + 1 < nchunks && v >= 32 && (v & 31) == 0) on_record(c + 1, v >> 5);
   }
   ok = state_all(ok && !*reinterpret_cast<volatile int*>(&ctl->abort));
   if (!ok && v == 0) {

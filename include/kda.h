@@ -34,7 +34,8 @@
  *                    checked by the forward calls, since the values live on
  *                    the device: kda_validate_cu_seqlens checks them).  Without it
  *                    there are N sequences of T_total / N tokens each.
- *   D must be 128 (the head size the kernels are built for).
+ *   D must be 128 (the head size the kernels are built for), and T_total
+ *   below 2^31 (the token coordinate of the kernels' tensor-map copies).
  *
  * Sequences of length 0 are allowed (their final state is the initial one).
  * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
