@@ -70,12 +70,12 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # is four times the b2 capture: b8 processes four times the units, and the
 # traffic is the per-unit inputs, outputs and states.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 538.522368e6 + 120.761088e6,
-    ("b8", "fused"): 4 * (538.522368e6 + 120.761088e6),
+    ("b2", "fused"): 538.000896e6 + 121.184768e6,
+    ("b8", "fused"): 4 * (538.000896e6 + 121.184768e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
     # the whole kda_fwd_segmented step: its four launches on the long workload
-    ("long", "segmented"): 16.128e3 + (4559.290368e6 + 1910.622720e6) + 18.883072e6
-                           + (1734.411264e6 + 813.662976e6),
+    ("long", "segmented"): 16.128e3 + (4925.083648e6 + 1915.559680e6) + (18.893824e6 + 2.048e3)
+                           + (1734.411008e6 + 813.599744e6),
 }
 
 
