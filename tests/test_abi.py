@@ -66,6 +66,7 @@ def call_fwd(lib, *, q=FAKE, out=FAKE, T=64, H=1, N=1, D=128, lb=-5.0, scale=0.1
     (dict(N=0), 1),
     (dict(T=-1), 1),
     (dict(T=65, N=2), 1),            # equal split impossible without cu_seqlens
+    (dict(T=1 << 31), 1),            # token coordinates of the tensor-map copies are int32
     (dict(q=0), 1),                  # null input
     (dict(q=FAKE + 8), 1),           # misaligned input
     (dict(beta=FAKE + 1), 1),        # misaligned bf16 beta
