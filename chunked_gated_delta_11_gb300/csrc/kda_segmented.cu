@@ -67,22 +67,28 @@ __global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total,
 // The scan.  Rows of S M + X depend only on the same rows of S, so each
 // (sequence, head) is split over 128 / ROWS CTAs of ROWS value rows (the
 // launcher takes the smallest ROWS whose grid fits one CTA per SM: few units,
-// more CTAs per unit and shorter steps).  256 threads, each owning a
-// (ROWS / 8) x 4 block of the CTA's rows.  The rows are kept transposed in
-// shared memory (St[k][v], row stride ROWS + 4 floats) so that a thread's
-// values of one key column are contiguous.  M_j is staged row-major in one of
-// two buffers by cp.async, M_{j+1} arriving while step j computes.  xs holds
-// the X role's final states [N P, H, V, K]; for every later segment j its
-// entry is replaced by that segment's starting state S_0 (read by the fix-up).
+// more CTAs per unit and shorter steps).  Every warp reads all of M_j from
+// shared memory in a step, so warps own RA = 4 rows each (8 for ROWS = 128,
+// at 16 warps): thread (warp w, lane l) owns rows RA w .. RA w + RA - 1 and
+// key columns 4 l .. 4 l + 3.  The rows are kept transposed in shared memory
+// (St[k][v], row stride ROWS + 4 floats) so that a thread's values of one key
+// column are contiguous.  The
+// steps are serial, so everything a step reads arrives during the previous
+// one: M_j is staged row-major in one of two buffers by cp.async, and each
+// thread loads its own elements of X_j into registers.  xs holds the X role's
+// final states [N P, H, V, K]; for every later segment j its entry is
+// replaced by that segment's starting state S_0 (read by the fix-up).
 // ---------------------------------------------------------------------------
-constexpr int SC_THREADS = 256;
+template <int ROWS>
+constexpr int sc_threads() { return 32 * (ROWS / 4 < 16 ? ROWS / 4 : 16); }
 
 template <int ROWS>
 constexpr int sc_smem() { return (kDim * (ROWS + 4) + 2 * kDim * kDim) * 4; }
 
+template <int NT>
 __device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) {
 #pragma unroll 4
-  for (int i = t; i < kDim * kDim / 4; i += SC_THREADS)
+  for (int i = t; i < kDim * kDim / 4; i += NT)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 4 * i)),
                  "l"(src + 4 * i)
                  : "memory");
@@ -90,10 +96,10 @@ __device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) 
 }
 
 template <int ROWS>
-__global__ void __launch_bounds__(SC_THREADS)
+__global__ void __launch_bounds__(sc_threads<ROWS>())
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
                    void* __restrict__ final_state, bool final_bf16) {
-  constexpr int SPLIT = kDim / ROWS, LD = ROWS + 4, RA = ROWS / 8;
+  constexpr int NT = sc_threads<ROWS>(), SPLIT = kDim / ROWS, LD = ROWS + 4, RA = ROWS / (NT / 32);
   extern __shared__ float4 sc_smem4[];
   float* St = reinterpret_cast<float*>(sc_smem4);
   float* Mbuf = St + kDim * LD;  // two [128][128] buffers
@@ -104,10 +110,20 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
   const int64_t row0 = static_cast<int64_t>(part) * ROWS * kDim;  // first row of the part
   auto base = [&](int64_t s) { return (s * H + h) * kDim * kDim; };
   const int64_t s0 = static_cast<int64_t>(n) * P;
-  if (P > 1) sc_stage_m(Mbuf, ms + base(s0 + 1), t);
+  // this thread's elements of X_j (rows rv.., columns ck..)
+  auto load_x = [&](float4 (&x)[RA], int j) {
+    const float* xj = xs + base(s0 + j) + row0;
+#pragma unroll
+    for (int a = 0; a < RA; ++a) x[a] = __ldcg(reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck));
+  };
+  float4 xn[RA];
+  if (P > 1) {
+    sc_stage_m<NT>(Mbuf, ms + base(s0 + 1), t);
+    load_x(xn, 1);
+  }
   {
     const float* x0 = xs + base(s0) + row0;
-    for (int i = t; i < ROWS * kDim; i += SC_THREADS) St[(i & 127) * LD + (i >> 7)] = x0[i];
+    for (int i = t; i < ROWS * kDim; i += NT) St[(i & 127) * LD + (i >> 7)] = x0[i];
   }
   for (int j = 1; j < P; ++j) {
     const float* Ms = Mbuf + ((j - 1) & 1) * kDim * kDim;
@@ -115,14 +131,16 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
     float acc[RA][4];
 #pragma unroll
     for (int a = 0; a < RA; ++a) {
-      const float4 x = *reinterpret_cast<const float4*>(xj + (rv + a) * kDim + ck);
-      acc[a][0] = x.x; acc[a][1] = x.y; acc[a][2] = x.z; acc[a][3] = x.w;
+      acc[a][0] = xn[a].x; acc[a][1] = xn[a].y; acc[a][2] = xn[a].z; acc[a][3] = xn[a].w;
     }
     // M_j has arrived; its other buffer was last read in step j - 1, which
     // every thread has finished (barrier at the end of the previous step)
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    if (j + 1 < P) sc_stage_m(Mbuf + (j & 1) * kDim * kDim, ms + base(s0 + j + 1), t);
+    if (j + 1 < P) {
+      sc_stage_m<NT>(Mbuf + (j & 1) * kDim * kDim, ms + base(s0 + j + 1), t);
+      load_x(xn, j + 1);  // used by the next step; its latency overlaps this one
+    }
 #pragma unroll 4
     for (int kk = 0; kk < kDim; ++kk) {
       float sv[RA];
@@ -135,7 +153,7 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
     }
-    // segment j starts from the S before this step (X_j was read above)
+    // segment j starts from the S before this step (X_j was read a step ago)
 #pragma unroll
     for (int a = 0; a < RA; ++a)
       *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
@@ -152,11 +170,11 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
     const int64_t f0 = (static_cast<int64_t>(n) * H + h) * kDim * kDim + row0;
     if (final_bf16) {
       __nv_bfloat16* f = static_cast<__nv_bfloat16*>(final_state) + f0;
-      for (int i = t; i < ROWS * kDim; i += SC_THREADS)
+      for (int i = t; i < ROWS * kDim; i += NT)
         f[i] = __float2bfloat16_rn(St[(i & 127) * LD + (i >> 7)]);
     } else {
       float* f = static_cast<float*>(final_state) + f0;
-      for (int i = t; i < ROWS * kDim; i += SC_THREADS) f[i] = St[(i & 127) * LD + (i >> 7)];
+      for (int i = t; i < ROWS * kDim; i += NT) f[i] = St[(i & 127) * LD + (i >> 7)];
     }
   }
 }
@@ -296,7 +314,7 @@ cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H
       e != cudaSuccess)
     return e;
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
-  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), SC_THREADS, sc_smem<ROWS>(), stream>>>(
+  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), sc_threads<ROWS>(), sc_smem<ROWS>(), stream>>>(
       xs, ms, N, P, H, final_state, final_bf16);
   return cudaGetLastError();
 }
