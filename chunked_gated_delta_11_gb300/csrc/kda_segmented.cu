@@ -67,23 +67,34 @@ __global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total,
 // The scan.  Rows of S M + X depend only on the same rows of S, so each
 // (sequence, head) is split over 128 / ROWS CTAs of ROWS value rows (the
 // launcher takes the smallest ROWS whose grid fits one CTA per SM: few units,
-// more CTAs per unit and shorter steps).  Every warp reads all of M_j from
-// shared memory in a step, so warps own RA = 4 rows each (8 for ROWS = 128,
-// at 16 warps): thread (warp w, lane l) owns rows RA w .. RA w + RA - 1 and
-// key columns 4 l .. 4 l + 3.  The rows are kept transposed in shared memory
-// (St[k][v], row stride ROWS + 4 floats) so that a thread's values of one key
-// column are contiguous.  The
-// steps are serial, so everything a step reads arrives during the previous
-// one: M_j is staged row-major in one of two buffers by cp.async, and each
-// thread loads its own elements of X_j into registers.  xs holds the X role's
-// final states [N P, H, V, K]; for every later segment j its entry is
-// replaced by that segment's starting state S_0 (read by the fix-up).
+// more CTAs per unit and shorter steps).  The steps are serial and short, so
+// the kernel is bound by latency; its warps are arranged so that M_j is read
+// from shared memory once per CTA and step while 16 warps cover each other's
+// latency:
+//   - RW row warps own RA = 4 rows each (8 when ROWS >= 64) and, lane l, key
+//     columns 4 l .. 4 l + 3;
+//   - KS = 16 / RW warps share each row block, warp ks taking the
+//     contraction indices ks 128 / KS .. (ks + 1) 128 / KS - 1; the KS - 1
+//     partial sums go through shared memory to the ks = 0 warp at the end of
+//     the step.
+// The rows are kept transposed in shared memory (St[k][v], row stride ROWS +
+// 4 floats) so that a thread's values of one key column are contiguous.
+// Everything a step reads arrives during the step before: M_{j+1} by cp.async
+// into the second of two buffers, and the ks = 0 threads' elements of X_{j+1}
+// into registers.  xs holds the X role's final states [N P, H, V, K]; for
+// every later segment j its entry is replaced by that segment's starting
+// state S_0 (read by the fix-up).
 // ---------------------------------------------------------------------------
 template <int ROWS>
-constexpr int sc_threads() { return 32 * (ROWS / 4 < 16 ? ROWS / 4 : 16); }
-
-template <int ROWS>
-constexpr int sc_smem() { return (kDim * (ROWS + 4) + 2 * kDim * kDim) * 4; }
+struct ScanShape {
+  static constexpr int RA = ROWS >= 64 ? 8 : 4;  // rows per thread
+  static constexpr int RW = ROWS / RA;            // row warps
+  static constexpr int KS = 16 / RW;              // warps per row block
+  static constexpr int NT = 32 * RW * KS;         // 512 threads
+  static constexpr int LD = ROWS + 4;             // St row stride (floats)
+  // floats: St, two M buffers, the KS - 1 partial tiles
+  static constexpr int SMEM = (kDim * LD + 2 * kDim * kDim + (KS - 1) * ROWS * kDim) * 4;
+};
 
 template <int NT>
 __device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) {
@@ -96,21 +107,26 @@ __device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) 
 }
 
 template <int ROWS>
-__global__ void __launch_bounds__(sc_threads<ROWS>())
+__global__ void __launch_bounds__(ScanShape<ROWS>::NT)
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
                    void* __restrict__ final_state, bool final_bf16) {
-  constexpr int NT = sc_threads<ROWS>(), SPLIT = kDim / ROWS, LD = ROWS + 4, RA = ROWS / (NT / 32);
+  using SS = ScanShape<ROWS>;
+  constexpr int NT = SS::NT, RA = SS::RA, RW = SS::RW, KS = SS::KS, LD = SS::LD;
+  constexpr int SPLIT = kDim / ROWS, KC = kDim / KS;
   extern __shared__ float4 sc_smem4[];
   float* St = reinterpret_cast<float*>(sc_smem4);
-  float* Mbuf = St + kDim * LD;  // two [128][128] buffers
+  float* Mbuf = St + kDim * LD;          // two [128][128] buffers
+  float* Red = Mbuf + 2 * kDim * kDim;   // [KS - 1][ROWS][128] partial sums
   const int unit = blockIdx.x / SPLIT, part = blockIdx.x - unit * SPLIT;
   const int n = unit / H, h = unit - (unit / H) * H;
-  const int t = threadIdx.x;
-  const int rv = (t >> 5) * RA, ck = (t & 31) * 4;  // local value rows rv.., key columns ck..
+  const int t = threadIdx.x, wi = t >> 5;
+  const int rw = wi % RW, ks = wi / RW;
+  const int rv = rw * RA, ck = (t & 31) * 4;  // local value rows rv.., key columns ck..
+  const int k0 = ks * KC;                     // this warp's contraction indices k0..
   const int64_t row0 = static_cast<int64_t>(part) * ROWS * kDim;  // first row of the part
   auto base = [&](int64_t s) { return (s * H + h) * kDim * kDim; };
   const int64_t s0 = static_cast<int64_t>(n) * P;
-  // this thread's elements of X_j (rows rv.., columns ck..)
+  // this thread's elements of X_j (rows rv.., columns ck..; ks = 0 only)
   auto load_x = [&](float4 (&x)[RA], int j) {
     const float* xj = xs + base(s0 + j) + row0;
 #pragma unroll
@@ -119,7 +135,7 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
   float4 xn[RA];
   if (P > 1) {
     sc_stage_m<NT>(Mbuf, ms + base(s0 + 1), t);
-    load_x(xn, 1);
+    if (ks == 0) load_x(xn, 1);
   }
   {
     const float* x0 = xs + base(s0) + row0;
@@ -131,7 +147,11 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
     float acc[RA][4];
 #pragma unroll
     for (int a = 0; a < RA; ++a) {
-      acc[a][0] = xn[a].x; acc[a][1] = xn[a].y; acc[a][2] = xn[a].z; acc[a][3] = xn[a].w;
+      if (ks == 0) {
+        acc[a][0] = xn[a].x; acc[a][1] = xn[a].y; acc[a][2] = xn[a].z; acc[a][3] = xn[a].w;
+      } else {
+        acc[a][0] = acc[a][1] = acc[a][2] = acc[a][3] = 0.f;
+      }
     }
     // M_j has arrived; its other buffer was last read in step j - 1, which
     // every thread has finished (barrier at the end of the previous step)
@@ -139,10 +159,10 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
     __syncthreads();
     if (j + 1 < P) {
       sc_stage_m<NT>(Mbuf + (j & 1) * kDim * kDim, ms + base(s0 + j + 1), t);
-      load_x(xn, j + 1);  // used by the next step; its latency overlaps this one
+      if (ks == 0) load_x(xn, j + 1);  // used by the next step; its latency overlaps this one
     }
 #pragma unroll 4
-    for (int kk = 0; kk < kDim; ++kk) {
+    for (int kk = k0; kk < k0 + KC; ++kk) {
       float sv[RA];
 #pragma unroll
       for (int a = 0; a < RA; ++a) sv[a] = St[kk * LD + rv + a];
@@ -153,17 +173,36 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
 #pragma unroll
         for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
     }
-    // segment j starts from the S before this step (X_j was read a step ago)
+    if (ks == 0) {
+      // segment j starts from the S before this step (X_j was read a step ago)
 #pragma unroll
-    for (int a = 0; a < RA; ++a)
-      *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
-          make_float4(St[ck * LD + rv + a], St[(ck + 1) * LD + rv + a],
-                      St[(ck + 2) * LD + rv + a], St[(ck + 3) * LD + rv + a]);
-    __syncthreads();  // every read of St and of this M buffer is done
+      for (int a = 0; a < RA; ++a)
+        *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
+            make_float4(St[ck * LD + rv + a], St[(ck + 1) * LD + rv + a],
+                        St[(ck + 2) * LD + rv + a], St[(ck + 3) * LD + rv + a]);
+    } else {
+      float* r = Red + (ks - 1) * ROWS * kDim;
 #pragma unroll
-    for (int a = 0; a < RA; ++a)
+      for (int a = 0; a < RA; ++a)
+        *reinterpret_cast<float4*>(r + (rv + a) * kDim + ck) =
+            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    }
+    __syncthreads();  // every read of St and of this M buffer is done; partials written
+    if (ks == 0) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) St[(ck + b) * LD + rv + a] = acc[a][b];
+      for (int q = 1; q < KS; ++q) {
+        const float* r = Red + (q - 1) * ROWS * kDim;
+#pragma unroll
+        for (int a = 0; a < RA; ++a) {
+          const float4 p4 = *reinterpret_cast<const float4*>(r + (rv + a) * kDim + ck);
+          acc[a][0] += p4.x; acc[a][1] += p4.y; acc[a][2] += p4.z; acc[a][3] += p4.w;
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < RA; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) St[(ck + b) * LD + rv + a] = acc[a][b];
+    }
   }
   __syncthreads();
   if (final_state) {
@@ -310,11 +349,12 @@ cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H
                                  void* final_state, bool final_bf16, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   if (const cudaError_t e = ensure_smem_limit(
-          reinterpret_cast<const void*>(affine_scan_kernel<ROWS>), sc_smem<ROWS>(), smem_set);
+          reinterpret_cast<const void*>(affine_scan_kernel<ROWS>), ScanShape<ROWS>::SMEM, smem_set);
       e != cudaSuccess)
     return e;
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
-  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), sc_threads<ROWS>(), sc_smem<ROWS>(), stream>>>(
+  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), ScanShape<ROWS>::NT, ScanShape<ROWS>::SMEM,
+                             stream>>>(
       xs, ms, N, P, H, final_state, final_bf16);
   return cudaGetLastError();
 }
