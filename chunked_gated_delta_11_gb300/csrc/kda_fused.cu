@@ -110,20 +110,10 @@ fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tb = ctl->tmem;
-  const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
-  const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
-  const int64_t init_base = (init_unit * H + h) * kDim * kDim;
-  if (w < 4)
-    load_state(tb, lane_off, state_at(init_u, init_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
-               opts.state_bf16, mrole ? t : -1);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
   // Raw input tiles: q, k, g_raw double-buffered, v single.  One state
   // thread issues each copy group (kda_tma.cuh): those of chunks 0 and 1 (v:
-  // chunk 0) at the start, then each as soon as record j is there
+  // chunk 0) as soon as the barriers exist, so that they arrive while the
+  // state loads, then each as soon as record j is there
   // (on_record): chunk j is done with its q, k, g_raw buffer, which takes
   // chunk j + 2, and with the v buffer, which takes chunk j + 1.  So the
   // copies cost the chunk threads nothing, and q, k, g_raw have a whole
@@ -142,6 +132,23 @@ fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restri
     issue_v_tma(maps, vt, h, chunk_t0(c), &rb->v);
     ++rb->v_n;
   };
+
+  if (t == 32) {
+    if (nchunks > 0) issue_qkg(0);
+    if (nchunks > 1) issue_qkg(1);
+  }
+  if (t == 64 && !mrole && nchunks > 0) issue_v(0);
+
+  const uint32_t tb = ctl->tmem;
+  const uint32_t lane_off = static_cast<uint32_t>((w & 3) * 32) << 16;
+  const int64_t state_base = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
+  const int64_t init_base = (init_unit * H + h) * kDim * kDim;
+  if (w < 4)
+    load_state(tb, lane_off, state_at(init_u, init_base + static_cast<int64_t>(t) * kDim, opts.state_bf16),
+               opts.state_bf16, mrole ? t : -1);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   if (w >= 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F_CHUNK_REGS));
@@ -205,14 +212,8 @@ fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restri
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F_STATE_REGS));
     // ---------------- state threads (thread 0 issues the MMAs) ----------------
     auto release = [&](int, int s) { mbar_arrive(&ctl->empty[s]); };
-    // the first copies: q, k, g_raw of chunks 0 and 1 (state warp 1), v of
-    // chunk 0 (state warp 2); then, once record j is there, q, k, g_raw of
-    // chunk j + 2 and v of chunk j + 1
-    if (t == 32) {
-      if (nchunks > 0) issue_qkg(0);
-      if (nchunks > 1) issue_qkg(1);
-    }
-    if (t == 64 && !mrole && nchunks > 0) issue_v(0);
+    // once record j is there: q, k, g_raw of chunk j + 2 (state warp 1), v
+    // of chunk j + 1 (state warp 2)
     auto on_record = [&](int j, int sw) {
       if (sw == 1 && j + 2 < nchunks) issue_qkg(j + 2);
       if (sw == 2 && !mrole && j + 1 < nchunks) issue_v(j + 1);
