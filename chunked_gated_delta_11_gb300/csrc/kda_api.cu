@@ -23,12 +23,14 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
                          cudaStream_t stream);
 cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, int32_t* cu_seg,
                             int32_t* blk, cudaStream_t stream);
+// s0_bf16 / sstart16 (optional): a bf16 copy of every later segment's S_0,
+// written by the scan and read by the fix-up instead of converting S_0
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
                                void* final_state, bool final_bf16, int sm_count,
-                               cudaStream_t stream);
+                               cudaStream_t stream, void* s0_bf16);
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const void* sstart16);
 cudaError_t launch_selftest_timeout(long long limit, int* err, cudaStream_t stream);
 cudaError_t launch_recurrence_timed(const void* ws, const void* init, const int32_t* cu,
                                     int64_t T_total, int H, int N, void* out, void* final_state,
@@ -334,9 +336,10 @@ int64_t round256(int64_t x) { return (x + 255) & ~static_cast<int64_t>(255); }
 
 // Byte offsets of the segmented pass's workspace parts (each 256-byte aligned):
 // cu_seg and blk [N P + 1] int32, the X and M final states [N P, H, 128, 128]
-// fp32, the M outputs y [T_total, H, 128] bf16.
+// fp32, the segments' starting states as bf16 [N P, H, 128, 128] (written by
+// the scan for the fix-up), the M outputs y [T_total, H, 128] bf16.
 struct SegLayout {
-  int64_t cu, blk, xs, ms, y, total;
+  int64_t cu, blk, xs, ms, sb, y, total;
 };
 SegLayout seg_layout(int64_t T_total, int32_t H, int32_t N, int32_t P) {
   SegLayout L;
@@ -346,7 +349,8 @@ SegLayout seg_layout(int64_t T_total, int32_t H, int32_t N, int32_t P) {
   L.blk = L.cu + round256((ns + 1) * 4);
   L.xs = L.blk + round256((ns + 1) * 4);
   L.ms = L.xs + round256(states);
-  L.y = L.ms + round256(states);
+  L.sb = L.ms + round256(states);
+  L.y = L.sb + round256(states / 2);
   L.total = L.y + round256(T_total * H * KDA_HEAD_DIM * 2);
   return L;
 }
@@ -432,15 +436,17 @@ kda_status segmented_forward(FwdOpts opts, const void* q, const void* k, const v
   float* xs = reinterpret_cast<float*>(wb + L.xs);
   float* ms = reinterpret_cast<float*>(wb + L.ms);
   __nv_bfloat16* y = reinterpret_cast<__nv_bfloat16*>(wb + L.y);
+  void* sb = wb + L.sb;
   const int Nseg = N * P;
   cudaError_t e = launch_seg_plan(cu_seqlens, T_total, N, P, cu_seg, blk, st);
   if (e == cudaSuccess)
     e = launch_fused(q, k, v, g_raw, beta_raw, scale, lower_bound, kNormEps, initial_state,
                      cu_seg, T_total, H, Nseg, out, xs, opts, SegArgs{P, y, ms}, info.err, st);
   if (e == cudaSuccess)
-    e = launch_affine_scan(xs, ms, N, P, H, final_state, opts.state_bf16 != 0, info.sm_count, st);
+    e = launch_affine_scan(xs, ms, N, P, H, final_state, opts.state_bf16 != 0, info.sm_count, st,
+                           sb);
   if (e == cudaSuccess)
-    e = launch_seg_fixup(cu_seg, blk, Nseg, H, xs, y, out, info.sm_count, st);
+    e = launch_seg_fixup(cu_seg, blk, Nseg, H, xs, y, out, info.sm_count, st, sb);
   if (!workspace) cudaFreeAsync(ws, st);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }

@@ -29,12 +29,14 @@ cudaError_t launch_fused(const void* q, const void* k, const void* v, const void
                          const void* init, const int32_t* cu, int64_t T_total, int H, int N,
                          void* out, void* final_state, FwdOpts opts, SegArgs seg, int* err,
                          cudaStream_t stream);
+// s0_bf16 / sstart16 (optional): a bf16 copy of every later segment's S_0,
+// written by the scan and read by the fix-up instead of converting S_0
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
                                void* final_state, bool final_bf16, int sm_count,
-                               cudaStream_t stream);
+                               cudaStream_t stream, void* s0_bf16);
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const void* sstart16);
 
 namespace {
 
@@ -137,7 +139,7 @@ extern "C" kda_status kda_pieces_scan(float* xs, const float* ms, int32_t P, int
   kda_status s = dev_info(d);
   if (s != KDA_OK) return s;
   return launch_affine_scan(xs, ms, 1, P, H, final_state, false, d.sm_count,
-                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            static_cast<cudaStream_t>(stream), nullptr) == cudaSuccess
              ? KDA_OK
              : KDA_ERR_LAUNCH;
 }
@@ -160,6 +162,6 @@ extern "C" kda_status kda_piece_fixup(void* out, const void* y, const float* s0,
   int32_t* dp = static_cast<int32_t*>(workspace);
   cudaError_t e = cudaMemcpyAsync(dp, plan, sizeof(plan), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
-    e = launch_seg_fixup(dp, dp + 2, 1, H, s0, y, out, d.sm_count, st);
+    e = launch_seg_fixup(dp, dp + 2, 1, H, s0, y, out, d.sm_count, st, nullptr);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }

@@ -109,7 +109,8 @@ __device__ __forceinline__ void sc_stage_m(float* dst, const float* src, int t) 
 template <int ROWS>
 __global__ void __launch_bounds__(ScanShape<ROWS>::NT)
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
-                   void* __restrict__ final_state, bool final_bf16) {
+                   void* __restrict__ final_state, bool final_bf16,
+                   __nv_bfloat16* __restrict__ s0_bf16) {
   using SS = ScanShape<ROWS>;
   constexpr int NT = SS::NT, RA = SS::RA, RW = SS::RW, KS = SS::KS, LD = SS::LD;
   constexpr int SPLIT = kDim / ROWS, KC = kDim / KS;
@@ -174,12 +175,18 @@ affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, 
         for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(sv[a], mv[b], acc[a][b]);
     }
     if (ks == 0) {
-      // segment j starts from the S before this step (X_j was read a step ago)
+      // segment j starts from the S before this step (X_j was read a step
+      // ago); the fix-up's bf16 copy of it, if asked for, beside it
+      __nv_bfloat16* bj = s0_bf16 ? s0_bf16 + base(s0 + j) + row0 : nullptr;
 #pragma unroll
-      for (int a = 0; a < RA; ++a)
-        *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) =
-            make_float4(St[ck * LD + rv + a], St[(ck + 1) * LD + rv + a],
-                        St[(ck + 2) * LD + rv + a], St[(ck + 3) * LD + rv + a]);
+      for (int a = 0; a < RA; ++a) {
+        const float4 sj = make_float4(St[ck * LD + rv + a], St[(ck + 1) * LD + rv + a],
+                                      St[(ck + 2) * LD + rv + a], St[(ck + 3) * LD + rv + a]);
+        *reinterpret_cast<float4*>(xj + (rv + a) * kDim + ck) = sj;
+        if (bj)
+          *reinterpret_cast<uint2*>(bj + (rv + a) * kDim + ck) =
+              make_uint2(pack_bf16(sj.x, sj.y), pack_bf16(sj.z, sj.w));
+      }
     } else {
       float* r = Red + (ks - 1) * ROWS * kDim;
 #pragma unroll
@@ -243,8 +250,8 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
 
 __global__ void __launch_bounds__(FX_THREADS, 3)
 seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__ blk, int Nseg,
-                 int H, const float* __restrict__ sstart, const __nv_bfloat16* __restrict__ y,
-                 __nv_bfloat16* __restrict__ out) {
+                 int H, const float* __restrict__ sstart, const __nv_bfloat16* __restrict__ sstart16,
+                 const __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ out) {
   extern __shared__ __align__(16) uint8_t fx_smem[];
   uint8_t* sb = fx_smem;
   uint8_t* yt = fx_smem + FX_S_BYTES;
@@ -287,12 +294,22 @@ seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (s != cur_s || h != cur_h) {
-      const float2* src = reinterpret_cast<const float2*>(
-          sstart + (static_cast<int64_t>(s) * H + h) * kDim * kDim);
-      for (int i = t; i < kDim * kDim / 2; i += FX_THREADS) {
-        const float2 x = __ldg(src + i);
-        const int v = i >> 6, kp = i & 63;
-        *reinterpret_cast<uint32_t*>(sb + v * SG_ROW + kp * 4) = pack_bf16(x.x, x.y);
+      const int64_t s0off = (static_cast<int64_t>(s) * H + h) * kDim * kDim;
+      if (sstart16) {
+        // the scan's bf16 copy: 16 pieces of 16 bytes per row, with the tiles
+        const __nv_bfloat16* src = sstart16 + s0off;
+#pragma unroll 4
+        for (int i = t; i < kDim * 16; i += FX_THREADS)
+          cp_async16_zfill(sb + (i >> 4) * SG_ROW + (i & 15) * 16, src + (i >> 4) * kDim + (i & 15) * 8,
+                           true);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      } else {
+        const float2* src = reinterpret_cast<const float2*>(sstart + s0off);
+        for (int i = t; i < kDim * kDim / 2; i += FX_THREADS) {
+          const float2 x = __ldg(src + i);
+          const int v = i >> 6, kp = i & 63;
+          *reinterpret_cast<uint32_t*>(sb + v * SG_ROW + kp * 4) = pack_bf16(x.x, x.y);
+        }
       }
       cur_s = s;
       cur_h = h;
@@ -346,7 +363,8 @@ cudaError_t launch_seg_plan(const int32_t* cu, int64_t T_total, int N, int P, in
 
 template <int ROWS>
 cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H,
-                                 void* final_state, bool final_bf16, cudaStream_t stream) {
+                                 void* final_state, bool final_bf16, __nv_bfloat16* s0_bf16,
+                                 cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   if (const cudaError_t e = ensure_smem_limit(
           reinterpret_cast<const void*>(affine_scan_kernel<ROWS>), ScanShape<ROWS>::SMEM, smem_set);
@@ -355,31 +373,32 @@ cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
   affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), ScanShape<ROWS>::NT, ScanShape<ROWS>::SMEM,
                              stream>>>(
-      xs, ms, N, P, H, final_state, final_bf16);
+      xs, ms, N, P, H, final_state, final_bf16, s0_bf16);
   return cudaGetLastError();
 }
 
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
                                void* final_state, bool final_bf16, int sm_count,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, void* s0_bf16) {
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units == 0) return cudaSuccess;
+  __nv_bfloat16* bf = static_cast<__nv_bfloat16*>(s0_bf16);
   // the most CTAs per (sequence, head) that still fit one per SM
   const int64_t slots = sm_count;
   if (units * 16 <= slots)
-    return launch_affine_scan_t<8>(xs, ms, N, P, H, final_state, final_bf16, stream);
+    return launch_affine_scan_t<8>(xs, ms, N, P, H, final_state, final_bf16, bf, stream);
   if (units * 8 <= slots)
-    return launch_affine_scan_t<16>(xs, ms, N, P, H, final_state, final_bf16, stream);
+    return launch_affine_scan_t<16>(xs, ms, N, P, H, final_state, final_bf16, bf, stream);
   if (units * 4 <= slots)
-    return launch_affine_scan_t<32>(xs, ms, N, P, H, final_state, final_bf16, stream);
+    return launch_affine_scan_t<32>(xs, ms, N, P, H, final_state, final_bf16, bf, stream);
   if (units * 2 <= slots)
-    return launch_affine_scan_t<64>(xs, ms, N, P, H, final_state, final_bf16, stream);
-  return launch_affine_scan_t<128>(xs, ms, N, P, H, final_state, final_bf16, stream);
+    return launch_affine_scan_t<64>(xs, ms, N, P, H, final_state, final_bf16, bf, stream);
+  return launch_affine_scan_t<128>(xs, ms, N, P, H, final_state, final_bf16, bf, stream);
 }
 
 cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg, int H,
                              const float* sstart, const void* y, void* out, int sm_count,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const void* sstart16) {
   static std::atomic<uint64_t> smem_set{0};
   if (const cudaError_t e =
           ensure_smem_limit(reinterpret_cast<const void*>(seg_fixup_kernel), FX_SMEM, smem_set);
@@ -387,7 +406,8 @@ cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg
     return e;
   if (Nseg == 0) return cudaSuccess;
   seg_fixup_kernel<<<static_cast<unsigned>(3 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
-      cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(y),
+      cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(sstart16),
+      static_cast<const __nv_bfloat16*>(y),
       static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }

@@ -120,8 +120,10 @@ def test_forward_rejects_bad_options(lib):
 
 
 def test_segmented_workspace_size(lib):
-    # boundaries and work list (256 B each), X and M states (N P H 64 KiB each), y (T H 256 B)
-    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=4) == 512 + 2 * 4 * 4 * 65536 + 4096 * 4 * 256
+    # boundaries and work list (256 B each), X and M states (N P H 64 KiB each), bf16 starting
+    # states (N P H 32 KiB), y (T H 256 B)
+    assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=4) == (512 + 2 * 4 * 4 * 65536 + 4 * 4 * 32768
+                                                                       + 4096 * 4 * 256)
     assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=1) == 0   # plain fused pass
     assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=65) == 0  # more than 64 pieces
     assert kda.kda_segmented_workspace_size(4096, 4, 1, segments=-1) == 0
