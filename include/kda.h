@@ -281,7 +281,8 @@ kda_status kda_chunk_recurrence(const void* workspace, size_t workspace_bytes,
  *   workspace  device memory of kda_segmented_workspace_size() bytes (16-byte
  *              aligned), or NULL (= cudaMallocAsync / cudaFreeAsync on the
  *              stream).  It holds the piece boundaries, the X and M states of
- *              every piece (2 N P H 64 KiB) and y (T_total H 256 bytes).
+ *              every piece (2 N P H 64 KiB), a bf16 copy of the pieces'
+ *              starting states (N P H 32 KiB) and y (T_total H 256 bytes).
  * T_total must be below 2^31 (piece boundaries are int32).  The runtime is set
  * by the longest piece: the pieces' units take N H (2 P - 1) CTAs of the fused
  * kernel, two per SM. */
