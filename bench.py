@@ -68,14 +68,18 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # dominant kernel (per step for the segmented path, whose roofline entry is the
 # whole step), from one ncu capture of the current kernels.  The b8 figure
 # is four times the b2 capture: b8 processes four times the units, and the
-# traffic is the per-unit inputs, outputs and states.  Absent = not captured.
+# traffic is the per-unit inputs, outputs and states.  The long figure comes
+# from the l32 capture (a quarter of long's tokens, split into the same 5
+# pieces): four times the plan, fused and fix-up launches, whose traffic
+# follows the tokens, plus the scan's once, which follows the pieces and
+# heads.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 538.000896e6 + 121.184768e6,
-    ("b8", "fused"): 4 * (538.000896e6 + 121.184768e6),
+    ("b2", "fused"): 538.241536e6 + 120.650496e6,
+    ("b8", "fused"): 4 * (538.241536e6 + 120.650496e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
-    # the whole kda_fwd_segmented step: its four launches on the long workload
-    ("long", "segmented"): 16.128e3 + (4925.083648e6 + 1915.559680e6) + (18.893824e6 + 2.048e3)
-                           + (1734.411008e6 + 813.599744e6),
+    # the whole kda_fwd_segmented step: its four launches
+    ("long", "segmented"): 4 * (15.616e3 + (1102.855424e6 + 459.103232e6)
+                                + (437.099776e6 + 169.138944e6)) + 18.886144e6,
 }
 
 
