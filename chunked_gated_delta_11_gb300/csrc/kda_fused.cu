@@ -28,11 +28,11 @@ namespace kda {
 constexpr int F_NST = 2;
 constexpr int F_THREADS = 256;
 // Registers per thread: the kernel is compiled for 128 (two CTAs of 256
-// threads per SM); after the prologue the state warpgroup takes 152 and the
-// chunk warpgroup 104 (setmaxnreg), 128 x 152 + 128 x 104 = 256 x 128, so the
+// threads per SM); after the prologue the state warpgroup takes 136 and the
+// chunk warpgroup 120 (setmaxnreg), 128 x 136 + 128 x 120 = 256 x 128, so the
 // increase is always covered by the decrease.  launch_fused checks the
 // compiled count before the first launch.
-constexpr int F_REGS = 128, F_STATE_REGS = 152, F_CHUNK_REGS = 104;
+constexpr int F_REGS = 128, F_STATE_REGS = 136, F_CHUNK_REGS = 120;
 static_assert(128 * F_STATE_REGS + 128 * F_CHUNK_REGS == F_THREADS * F_REGS,
               "register split must add up to the launch allocation");
 constexpr int F_CHUNK_OFF = F_NST * REC_STRIDE_SMEM;
@@ -220,7 +220,7 @@ fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restri
     };
     // a segmented launch writes every piece's final state to its fp32 workspace
     const bool final_bf16 = opts.state_bf16 && seg.P == 0;
-    // 16-column snapshot pieces: the state warps run under the 152-register cap
+    // 16-column snapshot pieces: the state warps run under the 136-register cap
     state_rows<NST, 16, kTimed>(ctl, smem, nchunks, tb, lane_off, t, bos, eos, H, h,
                             mrole ? seg.y : out,
                             state_at(mrole ? static_cast<void*>(seg.m_final) : final_state,
