@@ -74,8 +74,8 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # follows the tokens, plus the scan's once, which follows the pieces and
 # heads.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 538.241536e6 + 120.650496e6,
-    ("b8", "fused"): 4 * (538.241536e6 + 120.650496e6),
+    ("b2", "fused"): 537.99552e6 + 120.597504e6,
+    ("b8", "fused"): 4 * (537.99552e6 + 120.597504e6),
     ("decode", "decode"): 545.380864e6 + 491.383296e6,
     # the whole kda_fwd_segmented step: its four launches
     ("long", "segmented"): 4 * (15.616e3 + (1102.855424e6 + 459.103232e6)
