@@ -405,6 +405,34 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // Named barrier over the first `nthreads` threads (multiple of 32).
+// Programmatic dependent launch, for the chains of kernels on one stream
+// (the segmented pass): a kernel launched with launch_pdl may be scheduled
+// while the kernel before it still runs.  grid_dep_wait: wait until that
+// kernel has completed and its memory writes are visible (a no-op for a
+// kernel launched without the attribute).  grid_dep_launch: let the next
+// kernel, if launched with launch_pdl, be scheduled now.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with the programmatic-stream-serialization attribute (see above).
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

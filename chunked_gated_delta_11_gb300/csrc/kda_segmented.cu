@@ -41,6 +41,7 @@ constexpr int SG_ROW = 272;    // padded byte stride of a 128 x bf16 row in shar
 // One CTA.
 __global__ void seg_plan_kernel(const int32_t* __restrict__ cu, int64_t T_total, int N, int P,
                                 int32_t* __restrict__ cu_seg, int32_t* __restrict__ blk) {
+  grid_dep_launch();  // the fused launch may be scheduled now; it waits for this kernel
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
     int64_t bos, eos;
     seq_bounds(cu, T_total, N, n, bos, eos);
@@ -111,6 +112,8 @@ __global__ void __launch_bounds__(ScanShape<ROWS>::NT)
 affine_scan_kernel(float* __restrict__ xs, const float* __restrict__ ms, int N, int P, int H,
                    void* __restrict__ final_state, bool final_bf16,
                    __nv_bfloat16* __restrict__ s0_bf16) {
+  grid_dep_wait();  // the fused launch's states
+  grid_dep_launch();
   using SS = ScanShape<ROWS>;
   constexpr int NT = SS::NT, RA = SS::RA, RW = SS::RW, KS = SS::KS, LD = SS::LD;
   constexpr int SPLIT = kDim / ROWS, KC = kDim / KS;
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(FX_THREADS, 3)
 seg_fixup_kernel(const int32_t* __restrict__ cu_seg, const int32_t* __restrict__ blk, int Nseg,
                  int H, const float* __restrict__ sstart, const __nv_bfloat16* __restrict__ sstart16,
                  const __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ out) {
+  grid_dep_wait();  // the scan's starting states
   extern __shared__ __align__(16) uint8_t fx_smem[];
   uint8_t* sb = fx_smem;
   uint8_t* yt = fx_smem + FX_S_BYTES;
@@ -371,10 +375,9 @@ cudaError_t launch_affine_scan_t(float* xs, const float* ms, int N, int P, int H
       e != cudaSuccess)
     return e;
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / ROWS);
-  affine_scan_kernel<ROWS><<<static_cast<unsigned>(ctas), ScanShape<ROWS>::NT, ScanShape<ROWS>::SMEM,
-                             stream>>>(
-      xs, ms, N, P, H, final_state, final_bf16, s0_bf16);
-  return cudaGetLastError();
+  return launch_pdl(affine_scan_kernel<ROWS>, dim3(static_cast<unsigned>(ctas)),
+                    dim3(ScanShape<ROWS>::NT), ScanShape<ROWS>::SMEM, stream, xs, ms, N, P, H,
+                    final_state, final_bf16, s0_bf16);
 }
 
 cudaError_t launch_affine_scan(float* xs, const float* ms, int N, int P, int H,
@@ -405,11 +408,10 @@ cudaError_t launch_seg_fixup(const int32_t* cu_seg, const int32_t* blk, int Nseg
       e != cudaSuccess)
     return e;
   if (Nseg == 0) return cudaSuccess;
-  seg_fixup_kernel<<<static_cast<unsigned>(3 * sm_count), FX_THREADS, FX_SMEM, stream>>>(
-      cu_seg, blk, Nseg, H, sstart, static_cast<const __nv_bfloat16*>(sstart16),
-      static_cast<const __nv_bfloat16*>(y),
-      static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_pdl(seg_fixup_kernel, dim3(static_cast<unsigned>(3 * sm_count)), dim3(FX_THREADS),
+                    FX_SMEM, stream, cu_seg, blk, Nseg, H, sstart,
+                    static_cast<const __nv_bfloat16*>(sstart16), static_cast<const __nv_bfloat16*>(y),
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace kda
