@@ -62,8 +62,8 @@ fused_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __restri
              const void* init, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
              __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts, SegArgs seg,
              int* __restrict__ err, long long* stamps, int max_chunks) {
-  // in a segmented pass this launch may start while the plan kernel runs:
-  // its cu_seqlens are read below
+  // this launch may start while the previous kernel on the stream runs (in
+  // a segmented pass, the plan kernel whose cu_seqlens are read below)
   grid_dep_wait();
   grid_dep_launch();
   constexpr int NST = F_NST;
@@ -276,20 +276,16 @@ cudaError_t launch_fused_t(const void* q, const void* k, const void* v, const vo
   if (const cudaError_t e = make_raw_maps(&maps, q, k, v, g, T_total, H, kGateScalar);
       e != cudaSuccess)
     return e;
-  // the segmented pass chains its launches (plan, this kernel, scan, fix-up)
-  if (seg.P > 0)
-    return launch_pdl(fused_kernel<kGateScalar, kTimed>, dim3(static_cast<unsigned>(units)),
-                      dim3(F_THREADS), F_SMEM, stream,
-      maps, static_cast<const __nv_bfloat16*>(g),
-      static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err,
-      stamps, max_chunks);
-  fused_kernel<kGateScalar, kTimed><<<static_cast<unsigned>(units), F_THREADS, F_SMEM, stream>>>(
-      maps, static_cast<const __nv_bfloat16*>(g),
-      static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err,
-      stamps, max_chunks);
-  return cudaGetLastError();
+  // programmatic dependent launch: the kernel's first action is to wait for
+  // the previous kernel on the stream, so its launch may overlap that
+  // kernel's tail (the segmented pass chains its plan, this kernel, the scan
+  // and the fix-up this way)
+  return launch_pdl(fused_kernel<kGateScalar, kTimed>, dim3(static_cast<unsigned>(units)),
+                    dim3(F_THREADS), F_SMEM, stream, maps, static_cast<const __nv_bfloat16*>(g),
+                    static_cast<const __nv_bfloat16*>(beta_raw), scale,
+                    lower_bound * 1.4426950408889634f, eps, init, cu, T_total, H, N,
+                    static_cast<__nv_bfloat16*>(out), final_state, opts, seg, err, stamps,
+                    max_chunks);
 }
 
 cudaError_t launch_fused(const void* q, const void* k, const void* v, const void* g,
