@@ -31,6 +31,11 @@ decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restri
               const __nv_bfloat16* __restrict__ beta_raw, float scale, float lb_log2e,
               float eps, const void* init, const int32_t* __restrict__ cu, int64_t T_total,
               int H, int N, __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts) {
+  // this launch may start while the previous kernel on the stream (say, the
+  // previous decode step, whose final state is this one's initial state)
+  // runs: wait for it before the first read
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float4 sk4[kDim / 4], sq4[kDim / 4], sa4[kDim / 4];
   __shared__ float red[2][4];
   const int t = threadIdx.x, l = t & 31, w = t >> 5;
@@ -152,12 +157,12 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const voi
                           void* out, void* final_state, FwdOpts opts, cudaStream_t stream) {
   const int64_t ctas = static_cast<int64_t>(N) * H * (kDim / DEC_ROWS);
   if (ctas == 0) return cudaSuccess;
-  decode_kernel<<<static_cast<unsigned>(ctas), DEC_THREADS, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
-      static_cast<const __nv_bfloat16*>(beta_raw), scale, lower_bound * 1.4426950408889634f, eps,
-      init, cu, T_total, H, N, static_cast<__nv_bfloat16*>(out), final_state, opts);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel, dim3(static_cast<unsigned>(ctas)), dim3(DEC_THREADS), 0, stream,
+                    static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                    static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(g),
+                    static_cast<const __nv_bfloat16*>(beta_raw), scale,
+                    lower_bound * 1.4426950408889634f, eps, init, cu, T_total, H, N,
+                    static_cast<__nv_bfloat16*>(out), final_state, opts);
 }
 
 }  // namespace kda
