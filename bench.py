@@ -76,12 +76,12 @@ PATH_LAUNCHES = {"fused": 1, "split": 2, "decode": 1, "segmented": 4}
 # follows the tokens, plus the scan's once, which follows the pieces and
 # heads.  Absent = not captured.
 MEASURED_TRAFFIC = {
-    ("b2", "fused"): 537.99552e6 + 120.597504e6,
-    ("b8", "fused"): 4 * (537.99552e6 + 120.597504e6),
-    ("decode", "decode"): 545.380864e6 + 491.383296e6,
+    ("b2", "fused"): 538.023168e6 + 120.249344e6,
+    ("b8", "fused"): 4 * (538.023168e6 + 120.249344e6),
+    ("decode", "decode"): 545.300224e6 + 491.147776e6,
     # the whole kda_fwd_segmented step: its four launches
-    ("long", "segmented"): 4 * (15.616e3 + (1102.855424e6 + 459.103232e6)
-                                + (437.099776e6 + 169.138944e6)) + 18.886144e6,
+    ("long", "segmented"): 4 * (16.128e3 + (1136.457216e6 + 460.735232e6)
+                                + (437.124608e6 + 169.482496e6)) + 18.886912e6,
 }
 
 
