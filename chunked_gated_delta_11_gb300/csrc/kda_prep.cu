@@ -23,6 +23,7 @@ chunk_prep_kernel(const __grid_constant__ RawMaps maps, const __nv_bfloat16* __r
                   float eps, const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
                   uint8_t* __restrict__ ws, int64_t n_items, int gate_scalar,
                   int* __restrict__ err) {
+  grid_dep_launch();  // the recurrence kernel may be scheduled now; it waits for this one
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // 128-byte aligned base (the TMA destinations inside are 128-byte aligned)
   PrepSmem& P = *reinterpret_cast<PrepSmem*>(smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u));

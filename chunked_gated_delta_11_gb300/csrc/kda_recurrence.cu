@@ -24,6 +24,8 @@ recurrence_kernel(const uint8_t* __restrict__ ws, const void* init,
                   const int32_t* __restrict__ cu, int64_t T_total, int H, int N,
                   __nv_bfloat16* __restrict__ out, void* final_state, FwdOpts opts,
                   int* __restrict__ err, long long* stamps, int max_chunks) {
+  // this launch may start while the chunk kernel runs: wait for its records
+  grid_dep_wait();
   constexpr int NST = K2_NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -114,10 +116,9 @@ cudaError_t launch_recurrence_t(const void* ws, const void* init, const int32_t*
     return e;
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units == 0) return cudaSuccess;
-  recurrence_kernel<kTimed><<<static_cast<unsigned>(units), K2_THREADS, K2_SMEM, stream>>>(
-      static_cast<const uint8_t*>(ws), init, cu, T_total, H, N,
-      static_cast<__nv_bfloat16*>(out), final_state, opts, err, stamps, max_chunks);
-  return cudaGetLastError();
+  return launch_pdl(recurrence_kernel<kTimed>, dim3(static_cast<unsigned>(units)), dim3(K2_THREADS),
+                    K2_SMEM, stream, static_cast<const uint8_t*>(ws), init, cu, T_total, H, N,
+                    static_cast<__nv_bfloat16*>(out), final_state, opts, err, stamps, max_chunks);
 }
 
 cudaError_t launch_recurrence(const void* ws, const void* init, const int32_t* cu,
