@@ -357,14 +357,14 @@ SegLayout seg_layout(int64_t T_total, int32_t H, int32_t N, int32_t P) {
 
 // Segments per sequence for a device with `sms` SMs: the fused kernel runs
 // two CTAs per SM, and P segments take N H (2 P - 1) CTAs (X roles for all,
-// M roles for all but the first); each segment keeps at least 32 chunks
+// M roles for all but the first); each segment keeps at least 24 chunks
 // (fewer cost more in the scan and fix-up than they save in the chain).
 int32_t auto_segments(int64_t T_total, int32_t H, int32_t N, int sms) {
   const int64_t units = static_cast<int64_t>(N) * H;
   if (units <= 0 || sms <= 0) return 1;
   int64_t P = (2 * static_cast<int64_t>(sms) / units + 1) / 2;
   const int64_t chunks = (T_total / N + 15) / 16;
-  if (P > chunks / 32) P = chunks / 32;
+  if (P > chunks / 24) P = chunks / 24;
   if (P > kMaxSegments) P = kMaxSegments;
   return static_cast<int32_t>(P < 1 ? 1 : P);
 }

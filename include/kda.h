@@ -299,7 +299,7 @@ size_t kda_segmented_workspace_size(int64_t T_total, int32_t H, int32_t N, int32
                                     int32_t segments);
 
 /* The automatic piece count on the current device: the largest P with
- * N H (2 P - 1) <= 2 x (SM count), at most 64, and at least 32 chunks per
+ * N H (2 P - 1) <= 2 x (SM count), at most 64, and at least 24 chunks per
  * piece on average; 1 means no split. */
 int32_t kda_segments_auto(int64_t T_total, int32_t H, int32_t N);
 
