@@ -387,3 +387,30 @@ def test_profile_phases_diagnostic(kernel):
         assert st[c, 0] < st[c + 1, 0]
     table = phases.table(st)
     assert table["period"][0] > table["MMA1"][0] > 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_concurrent_calls_on_two_streams(path):
+    # Two different batches, each launched several times on its own stream
+    # with its own outputs, so that the calls overlap on the GPU: the library
+    # holds no state between calls that concurrent calls could share (the
+    # bench's two-stream throughput runs this way).
+    a = to_dev(synth.make_inputs(0, 3, lengths=[200, 77, 330], seed=71, init_std=0.02))
+    b = to_dev(synth.make_inputs(0, 2, lengths=[513, 9], seed=72, init_std=0.02))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    fn = kda.kda_fwd if path == "split" else kda.kda_fwd_fused
+    results = []
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for inp, st in zip((a, b), streams):
+            out, fs = fn(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+                         inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"], N=inp["N"],
+                         stream=st)
+            if rep == 2:
+                results.append((inp, out, fs))
+    torch.cuda.synchronize()
+    assert kda.kda_device_status() == 0
+    for inp, out, fs in results:
+        ro, rs = oracle_case(inp)
+        assert_close(f64(out), ro, f"{path} two streams out")
+        assert_close(f64(fs), rs, f"{path} two streams final_state")
