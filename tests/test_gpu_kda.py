@@ -414,3 +414,35 @@ def test_concurrent_calls_on_two_streams(path):
         ro, rs = oracle_case(inp)
         assert_close(f64(out), ro, f"{path} two streams out")
         assert_close(f64(fs), rs, f"{path} two streams final_state")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_cuda_graph_capture_and_replay(path):
+    # The calls launch with the programmatic-dependent-launch attribute and
+    # (split, no workspace) allocate stream-ordered; both must capture into a
+    # CUDA graph, and each replay must give the oracle's result.
+    inp = to_dev(synth.make_inputs(0, 2, lengths=[150, 64, 300], seed=81, init_std=0.02))
+    fn = kda.kda_fwd if path == "split" else kda.kda_fwd_fused
+    out = torch.empty_like(inp["q"])
+    fs = torch.empty((inp["N"], 2, 128, 128), dtype=torch.float32, device="cuda")
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):  # one eager call first (library load, attributes)
+        fn(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+           inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"], N=inp["N"], out=out,
+           final_state=fs, stream=st)
+    st.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        fn(inp["q"], inp["k"], inp["v"], inp["g_raw"], inp["beta_raw"], inp["scale"],
+           inp["lower_bound"], inp["initial_state"], inp["cu_seqlens"], N=inp["N"], out=out,
+           final_state=fs, stream=st)
+    ro, rs = oracle_case(inp)
+    for _ in range(2):
+        out.zero_()
+        fs.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert kda.kda_device_status() == 0
+        assert_close(f64(out), ro, f"{path} graph replay out")
+        assert_close(f64(fs), rs, f"{path} graph replay final_state")
