@@ -416,13 +416,23 @@ def test_concurrent_calls_on_two_streams(path):
         assert_close(f64(fs), rs, f"{path} two streams final_state")
 
 
-@pytest.mark.parametrize("path", PATHS)
+GRAPH_CALLS = {
+    "split": kda.kda_fwd,
+    "fused": kda.kda_fwd_fused,
+    "decode": kda.kda_decode,
+    # four launches chained by programmatic dependent launch, workspace
+    # allocated stream-ordered
+    "segmented": lambda *a, **kw: kda.kda_fwd_segmented(*a, segments=3, **kw),
+}
+
+
+@pytest.mark.parametrize("path", list(GRAPH_CALLS))
 def test_cuda_graph_capture_and_replay(path):
     # The calls launch with the programmatic-dependent-launch attribute and
-    # (split, no workspace) allocate stream-ordered; both must capture into a
+    # (without a workspace) allocate stream-ordered; they must capture into a
     # CUDA graph, and each replay must give the oracle's result.
     inp = to_dev(synth.make_inputs(0, 2, lengths=[150, 64, 300], seed=81, init_std=0.02))
-    fn = kda.kda_fwd if path == "split" else kda.kda_fwd_fused
+    fn = GRAPH_CALLS[path]
     out = torch.empty_like(inp["q"])
     fs = torch.empty((inp["N"], 2, 128, 128), dtype=torch.float32, device="cuda")
     st = torch.cuda.Stream()
